@@ -1,0 +1,224 @@
+/*
+ * rlloss.h — C ABI of the fused RL policy-loss library (GB300, sm_103a).
+ *
+ * The library computes the data-parallel hot path of an LLM reinforcement-
+ * learning update: reward normalisation into advantages, then, in ONE kernel
+ * launch, the per-token log-softmax over the vocabulary, the clipped
+ * surrogate objective with a KL penalty and an entropy bonus, the masked-mean
+ * loss and the gradient of that loss with respect to the logits.
+ *
+ * Sources (RL.cu, "LLM Reinforcement Learning in Pure CUDA"):
+ *   - ainews.cool RL.cu article, section "技术深度解析" (technical deep dive),
+ *     bullet "PPO 更新内核" (PPO update kernel): advantage estimation, clipped
+ *     surrogate objective and entropy bonus fused into a single kernel launch
+ *     to cut global-memory round trips; bullet "滚动缓冲区" (rollout buffer):
+ *     a fixed-size, preallocated GPU buffer of states, actions, rewards and
+ *     log-probabilities, memory managed by the caller;
+ *   - the same article, paragraph after its benchmark table: KL-divergence
+ *     penalty and reward normalisation, and CUDA-graph capture of the whole
+ *     training step;
+ *   - pitchhut.com RL.cu listing, "Key Features" item 3 and mlllm.io RL.cu
+ *     article, "Что произошло": the method is GRPO (group-relative policy
+ *     optimisation), i.e. group-normalised rewards as advantages;
+ *   - pitchhut.com RL.cu listing, "Key Features" item 1: FP16 inputs with FP32
+ *     accumulation.
+ * The pages print no formula; each entry point below states the standard
+ * definition it computes.
+ *
+ * Conventions for every entry point:
+ *   - Every array pointer is DEVICE memory owned by the caller.  The library
+ *     never allocates or frees memory and keeps no per-call host state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous and stream-ordered; none synchronises
+ *     except rl_read_device_status.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned synchronously; nothing is written in that case.  A launch
+ *     failure returns RL_ERR_CUDA.
+ *   - Device-detected errors never trap: they set bits in the call's status
+ *     (rl_loss_stats.device_error and the workspace status word), the
+ *     affected outputs become NaN, and the kernel returns normally.
+ */
+#ifndef RLLOSS_H
+#define RLLOSS_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RL_OK = 0,
+  RL_ERR_NULL = 1,       /* a required pointer is NULL */
+  RL_ERR_SHAPE = 2,      /* a size is negative, zero where it must not be, or too large */
+  RL_ERR_DTYPE = 3,      /* unknown element type or advantage layout */
+  RL_ERR_ALIGN = 4,      /* a logits/dlogits base or row stride is not 16-byte aligned */
+  RL_ERR_ALIAS = 5,      /* dlogits partially overlaps logits */
+  RL_ERR_WORKSPACE = 6,  /* workspace NULL or smaller than rl_policy_loss_workspace_size() */
+  RL_ERR_ID_RANGE = 7,   /* (device) a sampled id outside [0, V) on a valid token */
+  RL_ERR_TIMEOUT = 8,    /* (device) a bounded on-chip wait gave up; outputs are garbage */
+  RL_ERR_CUDA = 9,       /* a CUDA runtime call or launch failed */
+  RL_ERR_ARG = 10        /* a scalar argument is out of range (NaN, negative eps, ...) */
+} rl_status;
+
+typedef enum { RL_F32 = 0, RL_BF16 = 1, RL_F16 = 2 } rl_dtype;
+
+typedef enum {
+  RL_ADV_PER_SEQ = 0,    /* adv[B]: one advantage per sequence (GRPO) */
+  RL_ADV_PER_TOKEN = 1   /* adv[B*T]: one advantage per token (PPO-GAE) */
+} rl_adv_layout;
+
+/* Device-error bits of rl_loss_stats.device_error and of the workspace word. */
+#define RL_DEVERR_ID_RANGE 1u
+#define RL_DEVERR_TIMEOUT 2u
+
+/*
+ * Scalar results of one rl_policy_loss_fwd_bwd call, written by the kernel
+ * into caller-owned device memory.  All means are over the N valid tokens
+ * (N = 0 gives all zeros).
+ *   loss      = -(1/N) sum_t m_t J_t
+ *   pg_term   =  (1/N) sum_t m_t pg_t       (clipped surrogate)
+ *   kl_term   =  (1/N) sum_t m_t kl_t       (k3 estimator)
+ *   ent_term  =  (1/N) sum_t m_t H_t        (entropy)
+ *   clip_frac = n_clipped / N, n_clipped = tokens whose surrogate gradient is
+ *               cut by the clip: (A > 0 and r > 1+eps) or (A < 0 and r < 1-eps)
+ */
+typedef struct {
+  double loss;
+  double pg_term;
+  double kl_term;
+  double ent_term;
+  double clip_frac;
+  long long n_tokens;
+  long long n_clipped;
+  int device_error;      /* RL_DEVERR_* bits seen during this call */
+  int reserved;
+} rl_loss_stats;
+
+/*
+ * Group-relative advantages (GRPO reward normalisation).
+ *   For group g with rewards R_{g,0..G-1} (sequence i = g*G + j, group-major):
+ *     mean = (1/G) sum_j R_j,  std = sqrt( sum_j (R_j - mean)^2 / (G - ddof) )
+ *     adv_out[i] = (R_i - mean) / (std + std_eps)
+ *   rewards  : float[n_groups * group_size], device, read only.
+ *   adv_out  : float[n_groups * group_size], device, written (may equal rewards).
+ *   std_eps  : the stabiliser added to std (1e-4 in the usual GRPO recipe).
+ *   ddof     : 1 (unbiased, default reading) or 0.
+ * Arithmetic in fp64, result rounded to fp32.  One launch, one warp per group.
+ * Errors: RL_ERR_NULL, RL_ERR_SHAPE (n_groups < 0, group_size < 1,
+ * group_size <= ddof), RL_ERR_ARG (ddof not 0/1, std_eps negative or NaN).
+ * n_groups == 0 launches nothing and returns RL_OK.
+ */
+rl_status rl_group_advantages(const float* rewards, int n_groups, int group_size,
+                              double std_eps, int ddof, float* adv_out, void* stream);
+
+/*
+ * PPO generalised advantage estimation, reverse scan over time.
+ *   For sequence b with length L = clamp(lengths[b], 0, T), t = L-1 .. 0:
+ *     delta_t = r_t + gamma * (t+1 < L ? v_{t+1} : 0) - v_t
+ *     A_t     = delta_t + gamma * lam * (t+1 < L ? A_{t+1} : 0)
+ *     ret_t   = A_t + v_t
+ *   and A_t = ret_t = 0 for t >= L (the episode ends at L-1; bootstrap 0).
+ *   rewards, values : float[B*T] row-major [B, T], device, read only.
+ *   lengths         : int[B], device (values outside [0, T] are clamped).
+ *   adv_out         : float[B*T], device, written.
+ *   returns_out     : float[B*T], device, written; may be NULL.
+ * Arithmetic in fp64 (a warp-parallel affine scan over the sequence),
+ * result rounded to fp32.  One launch, one warp per sequence.
+ * Errors: RL_ERR_NULL, RL_ERR_SHAPE (B < 0, T < 0), RL_ERR_ARG (NaN gamma/lam).
+ */
+rl_status rl_gae_reverse_scan(const float* rewards, const float* values, const int* lengths,
+                              int B, int T, float gamma, float lam,
+                              float* adv_out, float* returns_out, void* stream);
+
+/*
+ * Bytes of device workspace rl_policy_loss_fwd_bwd needs for n_rows rows.
+ * The workspace must be zero-filled once before its first use (e.g. with
+ * cudaMemset); every call that completes leaves it ready for the next.  A
+ * workspace serves one call at a time: two calls in flight on it race.
+ */
+size_t rl_policy_loss_workspace_size(long long n_rows);
+
+/*
+ * The fused policy-loss forward and backward, in one kernel launch.
+ *
+ * Rows: row = b*T + t for sequence b, position t; R = B*T rows of V logits.
+ * For every row with mask[row] != 0 (a valid token; N = number of them):
+ *   z = logits row, y = ids[row]
+ *   lse = log sum_v exp(z_v),  logp = z_y - lse,  p_v = exp(z_v - lse)
+ *   H   = -sum_v p_v log p_v                                  (entropy)
+ *   r   = exp(logp - logp_old[row])            (r = 1 if logp_old == NULL)
+ *   A   = adv[b] (RL_ADV_PER_SEQ) or adv[row] (RL_ADV_PER_TOKEN)
+ *   pg  = min(r A, clamp(r, 1-eps, 1+eps) A)                  (clipped surrogate)
+ *   d   = ref_logp[row] - logp,  kl = exp(d) - d - 1          (k3; 0 if beta == 0
+ *                                                              and ref_logp == NULL)
+ *   J   = pg - beta kl + c_ent H
+ * loss = -(1/N) sum_rows J.  The gradient written to dlogits is
+ *   dz_v = grad_scale (1/N) [ g (p_v - [v == y]) + c_ent p_v (log p_v + H) ]
+ *   g    = pg' + beta (exp(d) - 1),  pg' = r A unless (A > 0 and r > 1+eps) or
+ *          (A < 0 and r < 1-eps), where pg' = 0 (the clip is inclusive at 1+-eps).
+ * Rows with mask 0 get an all-zero dlogits row, logp_out = entropy_out = 0,
+ * and neither their logits nor their id is read.  N = 0 gives loss 0 and an
+ * all-zero gradient.
+ *
+ * Arguments:
+ *   logits      : [R, ld] elements of `dtype`, row-major, device, read only.
+ *                 Base address 16-byte aligned; ld * sizeof(dtype) a multiple
+ *                 of 16 (pad rows if V is odd); ld >= V.
+ *   dtype       : RL_F32, RL_BF16 or RL_F16 (for logits and dlogits alike).
+ *   B, T, V, ld : B >= 0, T >= 0, V >= 1.  V up to the on-chip row limit of
+ *                 the device (every valid row is held on chip across a
+ *                 cluster of up to 8 CTAs: about 1.6 MB per row; larger
+ *                 rows return RL_ERR_SHAPE).
+ *   ids         : int64[R], the sampled token of each row.  An id outside
+ *                 [0, V) on a valid row sets RL_DEVERR_ID_RANGE and makes
+ *                 that row's logp, entropy, loss and gradient NaN.
+ *   logp_old    : float[R] behaviour-policy log-probs, or NULL (on-policy).
+ *   ref_logp    : float[R] reference-policy log-probs; NULL only if beta == 0.
+ *   mask        : uint8[R], nonzero = valid token.
+ *   adv         : float[B] or float[R] according to adv_layout.
+ *   eps         : clip range, finite, >= 0.   beta, c_ent, grad_scale: finite.
+ *   dlogits     : [R, ld] of `dtype`, written (columns >= V untouched), or
+ *                 NULL for a forward-only call.  It may be the same pointer as
+ *                 logits (in place); any other overlap returns RL_ERR_ALIAS.
+ *   logp_out, entropy_out : float[R] written, or NULL.
+ *   stats_dev   : one rl_loss_stats in device memory, written at the end.
+ *   workspace   : device scratch of workspace_bytes >= rl_policy_loss_workspace_size(R),
+ *                 zero-filled before its first use (see above).
+ * Deterministic: the same inputs on the same device give bitwise identical
+ * outputs (fixed-order fp64 reductions, no floating-point atomics).
+ */
+rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype,
+                                 long long B, long long T, long long V, long long ld,
+                                 const long long* ids, const float* logp_old,
+                                 const float* ref_logp, const unsigned char* mask,
+                                 const float* adv, rl_adv_layout adv_layout,
+                                 float eps, float beta, float c_ent, float grad_scale,
+                                 void* dlogits, float* logp_out, float* entropy_out,
+                                 rl_loss_stats* stats_dev,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The launch shape rl_policy_loss_fwd_bwd would use on the current device for
+ * this row shape: CTAs per cluster (one vocabulary slice each), clusters in
+ * the persistent grid and dynamic shared memory per CTA.  Host-only query.
+ * Errors as for rl_policy_loss_fwd_bwd's shape checks.
+ */
+rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, long long n_rows,
+                                      int* cluster_size, int* n_clusters, int* smem_bytes);
+
+/*
+ * Synchronises `stream`, then reads the device status word the last
+ * rl_policy_loss_fwd_bwd call on `workspace` left: RL_OK, RL_ERR_ID_RANGE or
+ * RL_ERR_TIMEOUT (the first of the bits set), or RL_ERR_CUDA.
+ */
+rl_status rl_read_device_status(const void* workspace, void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* rl_status_string(rl_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLLOSS_H */

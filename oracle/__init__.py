@@ -1,0 +1,344 @@
+"""Plain fp64 CPU oracle for the fused RL policy-loss step.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  The CUDA library never
+loads it and shares no code with it: the heavy per-row loops live in
+``rlref.c`` (built here with gcc, no fast-math, no FMA contraction) and the
+per-token objective is numpy in float64.
+
+Sources.  The three pages on RL.cu ("LLM Reinforcement Learning in Pure CUDA")
+name the parts of the update without writing their formulas:
+
+* pitchhut.com RL.cu listing, "Project Highlights" and "Key Features" item 3:
+  the method is GRPO (group relative policy optimisation) alongside SFT;
+* mlllm.io RL.cu article, section "Что произошло": the full SFT + GRPO loop;
+* ainews.cool RL.cu article, section "技术深度解析" (technical deep dive):
+  the rollout buffer holds states, actions, rewards and log-probabilities;
+  the "PPO 更新内核" (PPO update kernel) bullet fuses advantage estimation,
+  the clipped surrogate objective and the entropy bonus into one launch; the
+  paragraph after the benchmark table adds a KL penalty against policy
+  collapse and reward normalisation.
+
+Each function below states the standard definition it writes out for the part
+the pages name.  Readings taken where the pages are silent:
+
+* group advantage: A = (R - mean_g) / (std_g + 1e-4) with the unbiased
+  (ddof = 1) standard deviation; ddof = 0 is a flag;
+* GAE: terminal bootstrap value 0 at the end of each sequence, no whitening;
+* KL: the k3 estimator exp(d) - d - 1 with d = ref_logp - logp;
+* masked mean: one global token mean, loss = -(1/N) sum_t m_t J_t, N = sum m;
+  N = 0 gives loss 0 and an all-zero gradient;
+* clip gradient: flows at r = 1 +/- eps exactly (inclusive boundary);
+* no ``logp_old`` means on-policy (r = 1, dr/dlogp = 1); no ``ref_logp`` means
+  no KL term.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rlref.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_OUT_DIR, "librlref.so")
+
+F32, BF16, F16, F64 = 0, 1, 2, 3
+DTYPE_CODES = {"f32": F32, "bf16": BF16, "f16": F16, "f64": F64}
+STORAGE = {F32: np.float32, BF16: np.uint16, F16: np.uint16, F64: np.float64}
+
+_lib_handle = None
+
+
+def build(force: bool = False) -> str:
+    """Compile rlref.c into a shared object next to it (plain C11, -O2)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _lib():
+    global _lib_handle
+    if _lib_handle is None:
+        lib = ctypes.CDLL(build())
+        P, LL, I, D = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_double
+        lib.rlref_decode.argtypes = [P, I, LL, P]
+        lib.rlref_encode.argtypes = [P, LL, I, P]
+        lib.rlref_count.argtypes = [P, LL]
+        lib.rlref_count.restype = LL
+        lib.rlref_row_stats.argtypes = [P, I, LL, LL, P, P, LL, LL, P, P, P]
+        lib.rlref_dlogits_rows.argtypes = [P, I, LL, LL, P, P, LL, P, P, P, P, D, I, P, LL]
+        _lib_handle = lib
+    return _lib_handle
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _code(dtype) -> int:
+    return DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+# --------------------------------------------------------------------------- formats
+def decode(storage: np.ndarray, dtype) -> np.ndarray:
+    """Exact decode of bf16/f16 (uint16 storage), f32 or f64 elements to float64."""
+    src = np.ascontiguousarray(storage)
+    out = np.empty(src.shape, np.float64)
+    _lib().rlref_decode(_ptr(src), _code(dtype), src.size, _ptr(out))
+    return out
+
+
+def encode(x: np.ndarray, dtype) -> np.ndarray:
+    """Round float64 values once to ``dtype`` (round to nearest even, subnormals kept)."""
+    code = _code(dtype)
+    src = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(src.shape, STORAGE[code])
+    _lib().rlref_encode(_ptr(src), src.size, code, _ptr(out))
+    return out
+
+
+def ulp(x: np.ndarray, dtype) -> np.ndarray:
+    """Spacing of ``dtype`` at |x| (the subnormal quantum below the normal range)."""
+    p, emin = {F32: (24, -126), BF16: (8, -126), F16: (11, -14), F64: (53, -1022)}[_code(dtype)]
+    a = np.abs(np.asarray(x, np.float64))
+    _, k = np.frexp(a)
+    lead = np.maximum(k - 1, emin)
+    return np.ldexp(1.0, lead - (p - 1))
+
+
+# --------------------------------------------------------------------------- advantages
+def group_advantages(rewards: np.ndarray, group_size: int, std_eps: float = 1e-4,
+                     ddof: int = 1) -> np.ndarray:
+    """Group-relative advantage (GRPO reward normalisation).
+
+    Pages: pitchhut.com RL.cu listing, "Key Features" item 3 (GRPO) and the
+    ainews.cool article's "reward normalisation" sentence after its benchmark
+    table.  Sequences are group-major: sequence i = g * G + j.  For each
+    group, mean and standard deviation (ddof 1 by default) of its G rewards,
+    then A_i = (R_i - mean) / (std + std_eps).
+    """
+    R = np.asarray(rewards, np.float64).reshape(-1)
+    G = int(group_size)
+    if G <= 0 or R.size % G:
+        raise ValueError("rewards length must be a multiple of group_size")
+    if G - ddof <= 0:
+        raise ValueError("group_size must exceed ddof")
+    A = np.empty_like(R)
+    for g in range(R.size // G):
+        grp = R[g * G:(g + 1) * G]
+        mean = sum(grp) / G
+        var = sum((x - mean) ** 2 for x in grp) / (G - ddof)
+        std = math.sqrt(var)
+        A[g * G:(g + 1) * G] = [(x - mean) / (std + std_eps) for x in grp]
+    return A
+
+
+def gae(rewards: np.ndarray, values: np.ndarray, lengths: np.ndarray,
+        gamma: float, lam: float):
+    """Generalised advantage estimation by a reverse scan over time.
+
+    Page: ainews.cool RL.cu article, "PPO 更新内核" bullet (advantage
+    estimation inside the PPO update) and the actor/critic bullet before it.
+    For a sequence of length L, walking t = L-1 down to 0:
+        delta_t = r_t + gamma * V_{t+1} - V_t      (V_L = 0: the episode ends)
+        A_t     = delta_t + gamma * lam * A_{t+1}  (A_L = 0)
+        ret_t   = A_t + V_t
+    Positions t >= L get A = ret = 0; lengths are clamped to [0, T].
+    """
+    r = np.asarray(rewards, np.float64)
+    v = np.asarray(values, np.float64)
+    B, T = r.shape
+    A = np.zeros((B, T))
+    ret = np.zeros((B, T))
+    for b in range(B):
+        L = min(max(int(lengths[b]), 0), T)
+        nxt_v, nxt_a = 0.0, 0.0
+        for t in range(L - 1, -1, -1):
+            delta = r[b, t] + gamma * nxt_v - v[b, t]
+            a = delta + gamma * lam * nxt_a
+            A[b, t] = a
+            ret[b, t] = a + v[b, t]
+            nxt_v, nxt_a = v[b, t], a
+    return A, ret
+
+
+# --------------------------------------------------------------------------- loss
+def count(mask: np.ndarray) -> int:
+    """N = number of valid tokens (nonzero mask bytes)."""
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    return int(_lib().rlref_count(_ptr(m), m.size))
+
+
+def row_stats(logits: np.ndarray, dtype, V: int, ids: np.ndarray, mask: np.ndarray,
+              threads: int | None = None):
+    """Per-row lse, logp of the sampled id and entropy (log-softmax over V).
+
+    ``logits`` is a 2-D array [rows, ld] of the element storage (uint16 for
+    bf16/f16).  Rows with mask 0 give zeros.  Rows are split over threads; the
+    arithmetic of each row is the sequential loop in rlref.c.
+    """
+    lg = np.ascontiguousarray(logits)
+    n_rows, ld = lg.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    lse, logp, ent = (np.zeros(n_rows) for _ in range(3))
+    lib, code = _lib(), _code(dtype)
+    threads = threads or default_threads()
+    step = max(1, -(-n_rows // (threads * 4)))
+
+    def work(r0):
+        lib.rlref_row_stats(_ptr(lg), code, ld, V, _ptr(ids), _ptr(m), r0, min(n_rows, r0 + step),
+                            _ptr(lse), _ptr(logp), _ptr(ent))
+
+    if threads == 1 or n_rows <= step:
+        for r0 in range(0, n_rows, step):
+            work(r0)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(work, range(0, n_rows, step)))
+    return lse, logp, ent
+
+
+def surrogate(r, A, eps):
+    """Clipped surrogate pg = min(r A, clip(r, 1 - eps, 1 + eps) A) and its
+    derivative with respect to logp (r = exp(logp - logp_old), dr/dlogp = r).
+
+    Page: ainews.cool RL.cu article, "PPO 更新内核" bullet (clipped surrogate
+    objective).  Where the two branches differ, the smaller is the clipped one
+    exactly when (A > 0 and r > 1 + eps) or (A < 0 and r < 1 - eps); its
+    derivative is 0 there and r A elsewhere (ties, including r = 1 +/- eps,
+    take r A).  Returns (pg, dpg, clipped).
+    """
+    r = np.asarray(r, np.float64)
+    A = np.asarray(A, np.float64)
+    s1 = r * A
+    s2 = np.clip(r, 1.0 - eps, 1.0 + eps) * A
+    pg = np.minimum(s1, s2)
+    clipped = ((A > 0) & (r > 1.0 + eps)) | ((A < 0) & (r < 1.0 - eps))
+    dpg = np.where(clipped, 0.0, r * A)
+    return pg, dpg, clipped
+
+
+def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent):
+    """Per-token PPO/GRPO objective J_t and its derivative g_t = dJ_t/dlogp_t.
+
+    Page: ainews.cool RL.cu article, "PPO 更新内核" bullet (clipped surrogate,
+    entropy bonus) and the KL-penalty sentence after the benchmark table.
+        r   = exp(logp - logp_old)                (r = 1 without logp_old)
+        pg  = min(r A, clip(r, 1 - eps, 1 + eps) A)
+        kl  = exp(d) - d - 1,  d = ref - logp     (k3 estimator; 0 without ref)
+        J   = pg - beta kl + c_ent H
+    Derivative with respect to logp: pg' = r A, except 0 when the clipped
+    branch is strictly the smaller one, i.e. (A > 0 and r > 1 + eps) or
+    (A < 0 and r < 1 - eps); kl' = 1 - exp(d); so g = pg' + beta (exp(d) - 1).
+    Masked tokens give zeros everywhere.
+    """
+    m = np.asarray(mask).astype(bool)
+    logp = np.where(m, logp, 0.0)
+    A = np.where(m, np.asarray(adv, np.float64), 0.0)
+    r = np.exp(logp - np.where(m, logp_old, 0.0)) if logp_old is not None else np.ones_like(logp)
+    r = np.where(m, r, 1.0)
+    pg, dpg, clipped = surrogate(r, A, eps)
+    if ref_logp is not None:
+        d = np.where(m, np.asarray(ref_logp, np.float64) - logp, 0.0)
+        kl = np.exp(d) - d - 1.0
+        dkl = np.exp(d) - 1.0
+    else:
+        kl = np.zeros_like(logp)
+        dkl = np.zeros_like(logp)
+    H = np.where(m, ent, 0.0)
+    J = pg - beta * kl + c_ent * H
+    g = dpg + beta * dkl
+    z = lambda x: np.where(m, x, 0.0)
+    return dict(r=z(r), pg=z(pg), kl=z(kl), H=H, J=z(J), g=z(g), clipped=m & clipped)
+
+
+def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=None,
+                eps=0.2, beta=0.0, c_ent=0.0, grad_scale=1.0, grad_rows=None,
+                out_dtype=None, threads=None, stats=None):
+    """The whole fused step on CPU: loss, statistics, per-row outputs and dlogits.
+
+    ``adv_row`` is the advantage of each row (a per-sequence advantage already
+    broadcast over its T positions).  ``grad_rows`` lists the rows whose
+    logits gradient is wanted (all rows if None); the gradient is returned in
+    ``out_dtype`` (default: the logits' format) as rows [len(grad_rows), V].
+    ``stats`` may carry precomputed (lse, logp, ent) to skip the row pass.
+
+    Loss = -(1/N) sum_t m_t J_t; N = 0 gives loss 0 and zero gradients.
+    dz_v = grad_scale (m_t / N) [ g_t (p_v - [v = y_t]) + c_ent p_v (ln p_v + H_t) ]
+    (d logp / dz_v = [v = y] - p_v and dH / dz_v = -p_v (ln p_v + H)).
+    """
+    lg = np.ascontiguousarray(logits)
+    n_rows, ld = lg.shape
+    m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
+    ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+    N = count(m)
+    lse, logp, ent = stats if stats is not None else row_stats(lg, dtype, V, ids, m, threads)
+    obj = token_objective(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent)
+    mb = m.astype(bool)
+    if N > 0:
+        loss = -math.fsum(obj["J"][mb]) / N
+        pg_term = math.fsum(obj["pg"][mb]) / N
+        kl_term = math.fsum(obj["kl"][mb]) / N
+        ent_term = math.fsum(obj["H"][mb]) / N
+    else:
+        loss = pg_term = kl_term = ent_term = 0.0
+    n_clipped = int(obj["clipped"].sum())
+    out = dict(loss=loss, pg_term=pg_term, kl_term=kl_term, ent_term=ent_term,
+               n_tokens=N, n_clipped=n_clipped, clip_frac=(n_clipped / N if N else 0.0),
+               lse=lse, logp=np.where(mb, logp, 0.0), entropy=np.where(mb, ent, 0.0), **obj)
+    if grad_rows is not False:
+        rows = np.arange(n_rows, dtype=np.int64) if grad_rows is None else \
+            np.ascontiguousarray(grad_rows, dtype=np.int64)
+        out["grad_rows"] = rows
+        out["dlogits"] = dlogits_rows(lg, dtype, V, ids, rows, lse[rows], ent[rows],
+                                      obj["g"][rows],
+                                      np.where(mb[rows], grad_scale / N if N else 0.0, 0.0),
+                                      c_ent, out_dtype if out_dtype is not None else dtype,
+                                      threads)
+    return out
+
+
+def dlogits_rows(logits, dtype, V, ids, rows, lse, ent, g, scale, c_ent, out_dtype,
+                 threads=None):
+    """dz for the listed rows; see rlref.c for the formula (one row per call site)."""
+    lg = np.ascontiguousarray(logits)
+    ld = lg.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (lse, ent, g, scale)]
+    ocode = _code(out_dtype)
+    out = np.zeros((rows.size, V), STORAGE[ocode])
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    lib, code = _lib(), _code(dtype)
+    threads = threads or default_threads()
+    step = max(1, -(-rows.size // (threads * 4)))
+
+    def work(i0):
+        i1 = min(rows.size, i0 + step)
+        sub = [np.ascontiguousarray(a[i0:i1]) for a in arrs]
+        r = np.ascontiguousarray(rows[i0:i1])
+        o = out[i0:i1]
+        lib.rlref_dlogits_rows(_ptr(lg), code, ld, V, _ptr(ids), _ptr(r), r.size,
+                               _ptr(sub[0]), _ptr(sub[1]), _ptr(sub[2]), _ptr(sub[3]),
+                               float(c_ent), ocode, o.ctypes.data, V)
+
+    if threads == 1 or rows.size <= step:
+        for i0 in range(0, rows.size, step):
+            work(i0)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(work, range(0, rows.size, step)))
+    return out

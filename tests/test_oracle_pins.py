@@ -1,0 +1,409 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test pins one part of the oracle to a library routine, a closed form, an
+invariant of the mathematics, a brute-force computation or a hand-worked table
+(tests/golden/).  A plausible slip in the oracle (a dropped term, a wrong
+sign or index, a transposed operand) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- formats
+def test_decode_bf16_all_patterns_match_torch():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ours = oracle.decode(bits, "bf16")
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_decode_f16_all_patterns_match_numpy():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ours = oracle.decode(bits, "f16")
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def _float32_values(n, seed):
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 1 << 32, size=n, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    extra = np.array([0.0, -0.0, 1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 65504.0, 65520.0,
+                      3.3895314e38, 3.40282347e38, 1e-45, 2 ** -126, 2 ** -133, 2 ** -24,
+                      2 ** -25, 3 * 2 ** -26, 6.1e-5], np.float32)
+    return np.concatenate([x, extra, -extra])
+
+
+def test_encode_bf16_matches_torch_on_float32_inputs():
+    # torch rounds binary32 -> bfloat16 to nearest even; every binary32 value is a double,
+    # so on these inputs the oracle's single rounding must agree bit for bit.
+    x = _float32_values(200_000, 1)
+    ours = oracle.encode(x.astype(np.float64), "bf16")
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_encode_bf16_rounds_once_from_double():
+    # 1 + 2^-8 + 2^-30 lies above the midpoint between 1 and 1 + 2^-7: one rounding gives
+    # 1 + 2^-7 (0x3F81); rounding through binary32 first would tie and give 1.0.
+    got = oracle.encode(np.array([1 + 2 ** -8 + 2 ** -30, 1 + 2 ** -8, 1 + 3 * 2 ** -8]), "bf16")
+    assert list(got) == [0x3F81, 0x3F80, 0x3F82]
+
+
+def test_encode_f16_matches_numpy():
+    rng = np.random.default_rng(2)
+    x = np.concatenate([rng.normal(0, 1, 100_000) * 10.0 ** rng.integers(-9, 6, 100_000),
+                        [65504.0, 65519.99, 65520.0, 1e6, 2 ** -24, 2 ** -25, 1.5 * 2 ** -25,
+                         2 ** -14, 1 + 2 ** -11 + 2 ** -40, 0.0, -0.0]])
+    ours = oracle.encode(x, "f16")
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_encode_f32_matches_numpy():
+    x = np.random.default_rng(3).normal(0, 1, 10_000) * 1e-30
+    assert np.array_equal(oracle.encode(x, "f32"), x.astype(np.float32))
+
+
+def test_ulp_matches_numpy_spacing():
+    x = np.array([1.0, 3.0, 1e-3, 100.0, 6e-5])
+    assert np.array_equal(oracle.ulp(x, "f32"), np.spacing(x.astype(np.float32)).astype(np.float64))
+    assert np.array_equal(oracle.ulp(x, "f16"), np.spacing(x.astype(np.float16)).astype(np.float64))
+
+
+# ----------------------------------------------------------------------------- row statistics
+def _stats64(z, ids, mask=None):
+    z = np.ascontiguousarray(z, np.float64)
+    m = np.ones(z.shape[0], np.uint8) if mask is None else mask
+    return oracle.row_stats(z, "f64", z.shape[1], ids, m, threads=1)
+
+
+def test_row_stats_match_scipy():
+    rng = np.random.default_rng(4)
+    z = rng.normal(0, 3, (7, 513))
+    ids = rng.integers(0, 513, 7)
+    lse, logp, H = _stats64(z, ids)
+    ref_lse = scipy.special.logsumexp(z, axis=1)
+    ref_lsm = scipy.special.log_softmax(z, axis=1)
+    ref_H = scipy.stats.entropy(scipy.special.softmax(z, axis=1), axis=1)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-13)
+    np.testing.assert_allclose(logp, ref_lsm[np.arange(7), ids], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(H, ref_H, rtol=1e-12)
+
+
+def test_uniform_logits_closed_form():
+    for V in (1, 2, 1024, 151936):
+        z = np.full((1, V), 1.7)
+        lse, logp, H = _stats64(z, np.array([V - 1]))
+        assert abs(logp[0] + math.log(V)) < 1e-12
+        assert abs(H[0] - math.log(V)) < 1e-10 * max(1.0, math.log(V))
+        assert abs(lse[0] - (1.7 + math.log(V))) < 1e-12
+
+
+def test_one_hot_logits_closed_form():
+    V, k = 1000, 17
+    z = np.zeros((2, V))
+    z[:, k] = 100.0
+    lse, logp, H = _stats64(z, np.array([k, 3]))
+    q = math.exp(-100.0)                         # p_v / p_k for v != k
+    pk = 1.0 / (1.0 + (V - 1) * q)
+    assert abs(logp[0] - math.log(pk)) < 1e-15
+    assert abs(logp[1] - (-100.0 + math.log(pk))) < 1e-12
+    H_exact = -(pk * math.log(pk) + (V - 1) * (q * pk) * math.log(q * pk))
+    assert abs(H[0] - H_exact) < 1e-30
+
+
+def test_two_logits_binary_closed_form():
+    a, b = 0.3, -1.9
+    lse, logp, H = _stats64(np.array([[a, b]]), np.array([0]))
+    p0 = 1.0 / (1.0 + math.exp(b - a))
+    assert abs(logp[0] - math.log(p0)) < 1e-15
+    assert abs(H[0] - (-(p0 * math.log(p0) + (1 - p0) * math.log(1 - p0)))) < 1e-15
+
+
+def test_shift_invariance():
+    rng = np.random.default_rng(5)
+    z = rng.normal(0, 2, (3, 300))
+    ids = np.array([0, 150, 299])
+    lse0, logp0, H0 = _stats64(z, ids)
+    lse1, logp1, H1 = _stats64(z + 37.25, ids)
+    np.testing.assert_allclose(logp1, logp0, atol=1e-12)
+    np.testing.assert_allclose(H1, H0, atol=1e-12)
+    np.testing.assert_allclose(lse1, lse0 + 37.25, atol=1e-12)
+
+
+def test_large_vocab_lse_aggregate():
+    # For z ~ N(0, sd) iid, lse = ln V + ln mean(e^z) -> ln V + sd^2/2 as V grows.
+    rng = np.random.default_rng(6)
+    V, sd = 151936, 1.0
+    z = rng.normal(0, sd, (4, V))
+    lse, _, _ = _stats64(z, np.zeros(4, np.int64))
+    assert np.all(np.abs(lse - (math.log(V) + sd * sd / 2)) < 0.02)
+
+
+def test_masked_rows_and_bad_ids():
+    z = np.random.default_rng(7).normal(0, 1, (3, 10))
+    lse, logp, H = oracle.row_stats(z, "f64", 10, np.array([1, 10, -1]),
+                                    np.array([0, 1, 1], np.uint8), threads=1)
+    assert lse[0] == 0 and logp[0] == 0 and H[0] == 0
+    assert np.isnan(logp[1]) and np.isnan(logp[2])
+
+
+def test_low_precision_rows_decode_exactly():
+    # A bf16 row and the same row widened to f64 must give identical statistics.
+    x = torch.randn(2, 777, generator=torch.Generator().manual_seed(8)).mul(3).to(torch.bfloat16)
+    st = x.view(torch.int16).numpy().view(np.uint16)
+    ids = np.array([5, 700])
+    a = oracle.row_stats(st, "bf16", 777, ids, np.ones(2, np.uint8), threads=1)
+    b = _stats64(x.double().numpy(), ids)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+# ----------------------------------------------------------------------------- advantages
+def test_group_advantages_vs_numpy_std():
+    rng = np.random.default_rng(9)
+    R = rng.random(8 * 6)
+    for ddof in (0, 1):
+        A = oracle.group_advantages(R, 6, 1e-4, ddof)
+        g = R.reshape(8, 6)
+        ref = (g - g.mean(1, keepdims=True)) / (g.std(1, ddof=ddof, keepdims=True) + 1e-4)
+        np.testing.assert_allclose(A, ref.reshape(-1), rtol=1e-12, atol=1e-13)
+        assert np.all(np.abs(A.reshape(8, 6).sum(1)) < 1e-12)
+
+
+def test_group_advantages_equal_rewards_are_zero():
+    R = np.array([1, 1, 1, 1, 0, 0, 0, 0, 1, 0, 1, 1], np.float64)
+    A = oracle.group_advantages(R, 4)
+    assert np.all(A[:8] == 0.0)
+    assert np.all(A[8:] != 0.0)
+
+
+def test_group_advantages_pair_closed_form():
+    # G = 2, ddof = 1: std = |dR| / sqrt(2), so A = +/- (|dR|/2) / (|dR|/sqrt(2) + eps).
+    R = np.array([0.25, 1.0])
+    A = oracle.group_advantages(R, 2)
+    d = 0.75
+    expect = (d / 2) / (d / math.sqrt(2) + 1e-4)
+    assert abs(A[1] - expect) < 1e-15 and abs(A[0] + expect) < 1e-15
+
+
+def _gae_inputs(seed, B=5, T=40):
+    rng = np.random.default_rng(seed)
+    r = rng.normal(0, 1, (B, T))
+    v = rng.normal(0, 0.5, (B, T))
+    L = np.array([T, 1, 0, T // 2, T - 3])[:B]
+    return r, v, L
+
+
+def test_gae_lambda_zero_is_td_error():
+    r, v, L = _gae_inputs(10)
+    A, ret = oracle.gae(r, v, L, 0.9, 0.0)
+    for b in range(r.shape[0]):
+        for t in range(L[b]):
+            vn = v[b, t + 1] if t + 1 < L[b] else 0.0
+            assert abs(A[b, t] - (r[b, t] + 0.9 * vn - v[b, t])) < 1e-12
+        assert np.all(A[b, L[b]:] == 0) and np.all(ret[b, L[b]:] == 0)
+
+
+def test_gae_gamma_lambda_one_is_reward_to_go():
+    r, v, L = _gae_inputs(11)
+    A, ret = oracle.gae(r, v, L, 1.0, 1.0)
+    for b in range(r.shape[0]):
+        for t in range(L[b]):
+            assert abs(A[b, t] - (r[b, t:L[b]].sum() - v[b, t])) < 1e-10
+            assert abs(ret[b, t] - r[b, t:L[b]].sum()) < 1e-10
+
+
+def test_gae_brute_force_sum():
+    r, v, L = _gae_inputs(12)
+    gamma, lam = 0.99, 0.95
+    A, ret = oracle.gae(r, v, L, gamma, lam)
+    for b in range(r.shape[0]):
+        Lb = L[b]
+        delta = [r[b, k] + gamma * (v[b, k + 1] if k + 1 < Lb else 0.0) - v[b, k] for k in range(Lb)]
+        for t in range(Lb):
+            bf = sum((gamma * lam) ** (k - t) * delta[k] for k in range(t, Lb))
+            assert abs(A[b, t] - bf) < 1e-10
+            assert abs(ret[b, t] - (bf + v[b, t])) < 1e-10
+
+
+def test_gae_constant_delta_geometric():
+    # r_t = d + V_t - gamma V_{t+1} makes delta_t = d everywhere.
+    T, gamma, lam, d = 30, 0.97, 0.9, 0.3
+    v = np.linspace(-1, 1, T)[None, :]
+    vn = np.append(v[0, 1:], 0.0)
+    r = (d + v[0] - gamma * vn)[None, :]
+    A, _ = oracle.gae(r, v, np.array([T]), gamma, lam)
+    c = gamma * lam
+    for t in range(T):
+        n = T - t
+        assert abs(A[0, t] - d * (1 - c ** n) / (1 - c)) < 1e-12
+
+
+# ----------------------------------------------------------------------------- objective
+def _golden_clip():
+    rows = []
+    with open(os.path.join(GOLDEN, "clip_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([float(x) for x in line.split()])
+    return np.array(rows)
+
+
+def test_surrogate_hand_table():
+    tab = _golden_clip()
+    A, r, pg, dpg, clipped = tab.T
+    got_pg, got_dpg, got_clipped = oracle.surrogate(r, A, 0.2)
+    np.testing.assert_allclose(got_pg, pg, atol=1e-15)
+    np.testing.assert_allclose(got_dpg, dpg, atol=1e-15)
+    assert np.array_equal(got_clipped, clipped.astype(bool))
+
+
+def test_surrogate_brute_force_derivative():
+    # Away from the clip boundaries, dpg equals the numerical derivative of
+    # pg(exp(l - l_old)) in l: brute force over a grid of A and r.
+    eps, h = 0.2, 1e-7
+    for A in (-2.0, -0.3, 0.0, 0.7, 1.5):
+        for r in np.linspace(0.5, 1.5, 41):
+            if min(abs(r - 0.8), abs(r - 1.2)) < 1e-3:
+                continue
+            l = math.log(r)
+            pg_p = oracle.surrogate(math.exp(l + h), A, eps)[0]
+            pg_m = oracle.surrogate(math.exp(l - h), A, eps)[0]
+            fd = (pg_p - pg_m) / (2 * h)
+            assert abs(oracle.surrogate(r, A, eps)[1] - fd) < 1e-6
+
+
+def test_kl_k3_zero_at_reference_and_quadratic_small():
+    logp = np.array([-3.0, -1.0, -0.5])
+    m = np.ones(3, np.uint8)
+    o = oracle.token_objective(logp, np.zeros(3), m, np.zeros(3), None, logp.copy(), 0.2, 1.0, 0.0)
+    assert np.all(o["kl"] == 0) and np.all(o["g"] == 0)
+    d = 1e-3
+    o = oracle.token_objective(logp, np.zeros(3), m, np.zeros(3), None, logp + d, 0.2, 1.0, 0.0)
+    np.testing.assert_allclose(o["kl"], d * d / 2 + d ** 3 / 6, rtol=1e-6)
+
+
+def _problem(seed, R=12, V=9, T=4, **kw):
+    rng = np.random.default_rng(seed)
+    z = rng.normal(0, 1.5, (R, V))
+    ids = rng.integers(0, V, R)
+    mask = (rng.random(R) < 0.75).astype(np.uint8)
+    mask[0] = 1
+    adv = rng.normal(0, 1, R)
+    noise_old = rng.normal(0, 0.1, R)
+    noise_ref = rng.normal(0, 0.3, R)
+    return z, ids, mask, adv, noise_old, noise_ref
+
+
+def test_on_policy_no_kl_loss_identity():
+    # logp == logp_old and beta = 0: r = 1 (never clipped), so
+    # loss = -mean(A) - c_ent mean(H) over the valid tokens.
+    z, ids, mask, adv, _, _ = _problem(13)
+    V = z.shape[1]
+    _, logp, H = oracle.row_stats(z, "f64", V, ids, mask, threads=1)
+    out = oracle.policy_loss(z, "f64", V, ids, mask, adv, logp_old=logp, ref_logp=None,
+                             eps=0.2, beta=0.0, c_ent=0.05, grad_rows=False)
+    mb = mask.astype(bool)
+    assert abs(out["loss"] - (-adv[mb].mean() - 0.05 * H[mb].mean())) < 1e-12
+    assert out["n_clipped"] == 0
+
+
+def test_loss_linear_and_odd_in_advantage():
+    z, ids, mask, adv, _, _ = _problem(14)
+    V = z.shape[1]
+    _, logp, _ = oracle.row_stats(z, "f64", V, ids, mask, threads=1)
+    f = lambda a: oracle.policy_loss(z, "f64", V, ids, mask, a, logp_old=logp, eps=0.2,
+                                     grad_rows=False)["loss"]
+    assert abs(f(2.5 * adv) - 2.5 * f(adv)) < 1e-12
+    assert abs(f(-adv) + f(adv)) < 1e-12
+
+
+def test_zero_valid_tokens():
+    z, ids, _, adv, _, _ = _problem(15)
+    mask = np.zeros(z.shape[0], np.uint8)
+    out = oracle.policy_loss(z, "f64", z.shape[1], ids, mask, adv, eps=0.2, beta=0.1, c_ent=0.1,
+                             ref_logp=np.zeros(z.shape[0]), out_dtype="f64")
+    assert out["loss"] == 0 and out["n_tokens"] == 0
+    assert np.all(out["dlogits"] == 0)
+
+
+# ----------------------------------------------------------------------------- gradient
+@pytest.mark.parametrize("V", [2, 3, 8, 17])
+def test_dlogits_central_differences(V):
+    z, ids, mask, adv, n_old, n_ref = _problem(20 + V, R=10, V=V)
+    _, logp0, _ = oracle.row_stats(z, "f64", V, ids, mask, threads=1)
+    logp_old = logp0 + n_old
+    ref = logp0 + n_ref
+    # keep every ratio well away from the clip boundaries, where pg is not differentiable
+    r = np.exp(logp0 - logp_old)
+    for i in range(len(r)):
+        if min(abs(r[i] - 0.8), abs(r[i] - 1.2)) < 1e-3:
+            logp_old[i] += 0.01
+    # force a clipped token on each side
+    logp_old[0] = logp0[0] - 0.5
+    adv[0] = abs(adv[0]) + 0.1
+    kw = dict(eps=0.2, beta=0.07, c_ent=0.03, logp_old=logp_old, ref_logp=ref)
+    out = oracle.policy_loss(z, "f64", V, ids, mask, adv, grad_scale=1.0, out_dtype="f64", **kw)
+    assert out["n_clipped"] >= 1
+    h = 1e-6
+    fd = np.zeros_like(z)
+    for i in range(z.shape[0]):
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[i, v] += h
+            zm[i, v] -= h
+            lp = oracle.policy_loss(zp, "f64", V, ids, mask, adv, grad_rows=False, **kw)["loss"]
+            lm = oracle.policy_loss(zm, "f64", V, ids, mask, adv, grad_rows=False, **kw)["loss"]
+            fd[i, v] = (lp - lm) / (2 * h)
+    np.testing.assert_allclose(out["dlogits"], fd, rtol=1e-6, atol=1e-9)
+
+
+def test_dlogits_rows_sum_to_zero_and_masked_rows_zero():
+    z, ids, mask, adv, n_old, n_ref = _problem(30, R=16, V=200)
+    _, logp0, _ = oracle.row_stats(z, "f64", 200, ids, mask, threads=1)
+    out = oracle.policy_loss(z, "f64", 200, ids, mask, adv, logp_old=logp0 + n_old,
+                             ref_logp=logp0 + n_ref, eps=0.2, beta=0.04, c_ent=0.01,
+                             grad_scale=16.0, out_dtype="f64")
+    d = out["dlogits"]
+    assert np.all(np.abs(d.sum(1)) < 1e-13)
+    assert np.all(d[mask == 0] == 0)
+    assert np.any(d[mask == 1] != 0)
+
+
+def test_sft_corner_is_softmax_minus_onehot():
+    # A = 1, on-policy, beta = c_ent = 0, grad_scale = N: dz = softmax(z) - onehot(y),
+    # the textbook cross-entropy gradient (torch.softmax in float64 as the reference).
+    z, ids, _, _, _, _ = _problem(31, R=6, V=50)
+    mask = np.ones(6, np.uint8)
+    out = oracle.policy_loss(z, "f64", 50, ids, mask, np.ones(6), eps=0.2,
+                             grad_scale=6.0, out_dtype="f64")
+    ref = torch.softmax(torch.from_numpy(z), dim=1).numpy()
+    ref[np.arange(6), ids] -= 1.0
+    np.testing.assert_allclose(out["dlogits"], ref, atol=1e-15)
+    # and the loss is the mean cross-entropy minus... nothing: -mean(A r) = -1
+    assert abs(out["loss"] + 1.0) < 1e-15
+
+
+def test_dlogits_rounding_to_bf16_is_single_rounding():
+    z, ids, mask, adv, _, _ = _problem(32, R=8, V=64)
+    kw = dict(eps=0.2, c_ent=0.02, grad_scale=8.0)
+    d64 = oracle.policy_loss(z, "f64", 64, ids, mask, adv, out_dtype="f64", **kw)["dlogits"]
+    d16 = oracle.policy_loss(z, "f64", 64, ids, mask, adv, out_dtype="bf16", **kw)["dlogits"]
+    assert np.array_equal(d16, oracle.encode(d64, "bf16"))

@@ -1,0 +1,459 @@
+"""Benchmark of the fused GRPO policy-loss step on GB300.
+
+One step = the whole hot path over one batch: rl_group_advantages (reward
+normalisation) then rl_policy_loss_fwd_bwd (log-softmax, clipped surrogate,
+k3 KL, entropy bonus, masked-mean loss and the bf16 logits gradient in one
+launch).  Workload: Qwen3-0.6B-shaped GRPO, 4 prompts x group 8 = 32
+sequences x T=1024 positions x V=151936 bf16 logits ~N(0, 3), ragged lengths
+U{256..1024}; synthetic inputs (seeded), 10 GB of logits, far larger than L2,
+so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own
+replica of the workload on its GPU (the path has no cross-rank exchange
+step); value = all ranks' tokens / max-over-ranks time.  ``--impl reference``
+times the fp64 CPU oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused GRPO loss+dlogits tokens/s at V=151936 bf16; % of HBM roofline"
+WORKLOAD = "qwen3_0p6b_grpo"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "policy_loss_qwen3_0p6b_grpo_traffic.txt")
+KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sha") != kernel_sha():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- inputs
+def make_inputs(w, dev):
+    """Device inputs of the workload.  logp_old / ref_logp are composed from the
+    current policy's own log-probs (computed once here with torch, untimed) plus
+    the workload's noise draws."""
+    import torch
+    from ppo_policy_loss_gb300 import synth
+
+    small = synth.small_inputs(w)
+    logits = synth.logits(w, device=dev)
+    ids = torch.from_numpy(small["ids"]).to(dev)
+    mask = torch.from_numpy(small["mask"]).to(dev)
+    rewards = torch.from_numpy(small["rewards"]).to(dev)
+    logp = torch.empty(w.R, dtype=torch.float32, device=dev)
+    for r0 in range(0, w.R, 1024):  # torch log_softmax, chunked (input preparation only)
+        blk = logits[r0:r0 + 1024].float()
+        lse = torch.logsumexp(blk, dim=1)
+        logp[r0:r0 + 1024] = blk.gather(1, ids[r0:r0 + 1024, None])[:, 0] - lse
+        del blk
+    m = mask.bool()
+    logp_old = torch.where(m, logp + torch.from_numpy(small["noise_old"]).to(dev).float(), 0.0)
+    ref = torch.where(m, logp + torch.from_numpy(small["noise_ref"]).to(dev).float(), 0.0)
+    return dict(small=small, logits=logits, ids=ids, mask=mask, rewards=rewards,
+                logp_old=logp_old.contiguous(), ref=ref.contiguous())
+
+
+def alg_bytes(w, n_valid):
+    """Algorithmic bytes of one rl_policy_loss_fwd_bwd launch: one read of each
+    valid logits row, one write of every dlogits row, plus the per-row arrays
+    (ids 8, logp_old 4, ref 4, mask 1, logp_out 4, entropy_out 4) and the
+    per-sequence advantages."""
+    es = w.elem_bytes
+    return n_valid * w.V * es + w.R * w.V * es + w.R * (8 + 4 + 4 + 1 + 4 + 4) + w.B * 4
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+
+    import ppo_policy_loss_gb300 as rl
+    from ppo_policy_loss_gb300 import STATS_BYTES, synth, torch_api
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    rl.build()
+    rl.load()
+    w = synth.WORKLOADS[WORKLOAD]
+    inp = make_inputs(w, dev)
+    n_valid = int(inp["small"]["mask"].sum())
+    stream = torch.cuda.current_stream(dev)
+    adv = torch.empty(w.B, dtype=torch.float32, device=dev)
+    dlogits = torch.empty_like(inp["logits"])
+    logp_out = torch.empty(w.R, dtype=torch.float32, device=dev)
+    ent_out = torch.empty(w.R, dtype=torch.float32, device=dev)
+    ws = torch_api.new_workspace(w.R, dev)
+    stats = torch_api.new_stats(dev)
+    ld = inp["logits"].stride(0)
+
+    def step(ev=None):
+        rl.rl_group_advantages(inp["rewards"], w.B // w.group, w.group, 1e-4, 1, adv, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        rl.rl_policy_loss_fwd_bwd(inp["logits"], "bf16", w.B, w.T, w.V, ld, inp["ids"],
+                                  inp["logp_old"], inp["ref"], inp["mask"], adv,
+                                  rl.RL_ADV_PER_SEQ, w.eps, w.beta, w.c_ent, 1.0, dlogits,
+                                  logp_out, ent_out, stats, ws, ws.numel(), stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    st = torch_api.read_stats(stats)
+    assert st["device_error"] == 0 and st["n_tokens"] == n_valid, st
+
+    # ---- timed region: K steps, inputs resident in HBM
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    sampler.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(kev[i])
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    k_ms = [a.elapsed_time(b) for a, b in kev]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = world * w.R / (ms_step / 1e3)
+
+    # ---- roofline of the dominant kernel (rl_policy_loss_fwd_bwd)
+    kern_ms = statistics.mean(k_ms)
+    bytes_launch = alg_bytes(w, n_valid)
+    peak, peak_kind = hbm_peak()
+    achieved = bytes_launch / (kern_ms / 1e3) / 1e9
+    traffic = recorded_traffic()
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, ws, ld)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the Qwen3-0.6B GRPO workload)",
+        "config": {"workload": f"{WORKLOAD}: 4 prompts x group 8 = 32 seqs, T=1024, V=151936 bf16, "
+                               "lengths U{256..1024}, eps=0.2 beta=0.04 c_ent=0",
+                   "B": w.B, "T": w.T, "V": w.V, "rows": w.R, "valid_tokens": n_valid,
+                   "valid_tokens_per_s": world * n_valid / (ms_step / 1e3),
+                   "l2": "inputs (10 GB logits) far larger than the 129 MB L2; no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch_shape": dict(zip(("cluster", "clusters", "smem"),
+                                            rl.rl_policy_loss_launch_shape("bf16", w.V, w.R)))},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": traffic, "alg_bytes_per_launch": bytes_launch,
+                     "kernel": "rl_policy_loss_fwd_bwd", "kernel_ms": kern_ms},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, inp["logits"], budget_s=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, ws, ld):
+    """Same step through the public C-ABI calls, with every input copied from
+    pinned host memory and the gradient and statistics copied back, inside the
+    timed region."""
+    import torch
+
+    import ppo_policy_loss_gb300 as rl
+    from ppo_policy_loss_gb300 import STATS_BYTES
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    h = {}
+    for k in ("logits", "ids", "mask", "rewards", "logp_old", "ref"):
+        h[k] = torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
+        h[k].copy_(inp[k])
+    h_dlogits = torch.empty(dlogits.shape, dtype=dlogits.dtype, pin_memory=True)
+    h_stats = torch.empty(STATS_BYTES, dtype=torch.uint8, pin_memory=True)
+    d = {k: torch.empty_like(inp[k]) for k in h}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = h_dlogits.numel() * h_dlogits.element_size() + STATS_BYTES
+
+    def one():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        rl.rl_group_advantages(d["rewards"], w.B // w.group, w.group, 1e-4, 1, adv, stream)
+        rl.rl_policy_loss_fwd_bwd(d["logits"], "bf16", w.B, w.T, w.V, ld, d["ids"], d["logp_old"],
+                                  d["ref"], d["mask"], adv, rl.RL_ADV_PER_SEQ, w.eps, w.beta,
+                                  w.c_ent, 1.0, dlogits, logp_out, ent_out, stats, ws, ws.numel(),
+                                  stream)
+        h_dlogits.copy_(dlogits, non_blocking=True)
+        h_stats.copy_(stats, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    world = dist_env()[0]
+    del d, h, h_dlogits
+    return {"value": world * w.R / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def sample_rows(w, n):
+    """n rows spread evenly over the batch (keeps the batch's valid fraction)."""
+    return np.unique(np.linspace(0, w.R - 1, max(1, n)).round().astype(np.int64))
+
+
+def sample_logits(w, rows, dev_logits=None):
+    """Host copy (uint16 storage) of the given rows of the workload's logits."""
+    import torch
+    from ppo_policy_loss_gb300 import synth
+
+    if dev_logits is not None:
+        t = dev_logits.index_select(0, torch.from_numpy(rows).to(dev_logits.device)).cpu()
+    else:
+        device = "cuda" if torch.cuda.is_available() else "cpu"
+        parts = []
+        for b in np.unique(rows // synth.ROW_BLOCK):
+            blk = synth.logits_block(w, int(b), device)
+            sel = rows[(rows // synth.ROW_BLOCK) == b] - b * synth.ROW_BLOCK
+            parts.append(blk[torch.from_numpy(sel).to(blk.device)].cpu())
+        t = torch.cat(parts)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_sample(w, rows, dev_logits=None):
+    """Oracle inputs for the sampled rows; logp_old / ref composed from the
+    oracle's own logp plus the workload's noise (input preparation)."""
+    import oracle
+    from ppo_policy_loss_gb300 import synth
+
+    small = synth.small_inputs(w)
+    host = sample_logits(w, rows, dev_logits)
+    mask, ids = small["mask"][rows], small["ids"][rows]
+    _, logp, _ = oracle.row_stats(host, w.dtype, w.V, ids, mask)
+    lo = np.where(mask != 0, logp + small["noise_old"][rows], 0.0).astype(np.float32)
+    rf = np.where(mask != 0, logp + small["noise_ref"][rows], 0.0).astype(np.float32)
+    return dict(host=host, mask=mask, ids=ids, rewards=small["rewards"], rows=rows, lo=lo, rf=rf)
+
+
+def oracle_step(w, s, threads):
+    """One oracle pass of the whole step over the sample: group advantages of
+    the batch, then loss, statistics and the bf16 gradient of every sample row."""
+    import oracle
+
+    A = oracle.group_advantages(s["rewards"], w.group)
+    arow = np.repeat(A, w.T)[s["rows"]]
+    return oracle.policy_loss(s["host"], w.dtype, w.V, s["ids"], s["mask"], arow,
+                              logp_old=s["lo"], ref_logp=s["rf"], eps=w.eps, beta=w.beta,
+                              c_ent=w.c_ent, grad_scale=1.0, threads=threads)
+
+
+def _sample_text(w, s, threads, extra=""):
+    n, nv = s["rows"].size, int(s["mask"].sum())
+    return (f"{n} rows spread evenly over the {w.R}-row batch ({nv} valid, V={w.V} bf16){extra}; "
+            f"fp64 C oracle on {threads} host threads")
+
+
+def cpu_baseline(w, dev_logits=None, budget_s=15.0, n_rows=512):
+    """The oracle as it stands, timed on the host cores over a bounded sample."""
+    import oracle
+
+    threads = oracle.default_threads()
+    s = cpu_sample(w, sample_rows(w, n_rows), dev_logits)
+    t0 = time.time()
+    done = 0
+    while True:
+        oracle_step(w, s, threads)
+        done += s["rows"].size
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": _sample_text(w, s, threads, f", repeated for {dt:.1f} s")}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, each step a bounded sample."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from ppo_policy_loss_gb300 import synth
+
+    w = synth.WORKLOADS[WORKLOAD]
+    threads = oracle.default_threads()
+    # size each step so that warm-up + timed steps take about args.ref_seconds
+    probe = cpu_sample(w, sample_rows(w, 64))
+    t0 = time.time()
+    oracle_step(w, probe, threads)
+    per_row = (time.time() - t0) / probe["rows"].size
+    n = int(args.ref_seconds / (args.steps + args.warmup) / max(per_row, 1e-9))
+    s = cpu_sample(w, sample_rows(w, min(max(n, 16), 4096)))
+    for _ in range(args.warmup):
+        oracle_step(w, s, threads)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle_step(w, s, threads)
+    dt = time.time() - t0
+    value = args.steps * s["rows"].size / dt
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": WORKLOAD, "B": w.B, "T": w.T, "V": w.V,
+                      "step_sample_rows": int(s["rows"].size)},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                            "sample": "each step: " + _sample_text(w, s, threads)},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -266,27 +266,16 @@ def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent):
     return dict(r=z(r), pg=z(pg), kl=z(kl), H=H, J=z(J), g=z(g), clipped=m & clipped)
 
 
-def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=None,
-                eps=0.2, beta=0.0, c_ent=0.0, grad_scale=1.0, grad_rows=None,
-                out_dtype=None, threads=None, stats=None):
-    """The whole fused step on CPU: loss, statistics, per-row outputs and dlogits.
+def loss_from_stats(logp, ent, mask, adv_row, logp_old=None, ref_logp=None, eps=0.2,
+                    beta=0.0, c_ent=0.0):
+    """Loss and monitoring statistics from per-row (logp, H) (fp64, math.fsum sums).
 
-    ``adv_row`` is the advantage of each row (a per-sequence advantage already
-    broadcast over its T positions).  ``grad_rows`` lists the rows whose
-    logits gradient is wanted (all rows if None); the gradient is returned in
-    ``out_dtype`` (default: the logits' format) as rows [len(grad_rows), V].
-    ``stats`` may carry precomputed (lse, logp, ent) to skip the row pass.
-
-    Loss = -(1/N) sum_t m_t J_t; N = 0 gives loss 0 and zero gradients.
-    dz_v = grad_scale (m_t / N) [ g_t (p_v - [v = y_t]) + c_ent p_v (ln p_v + H_t) ]
-    (d logp / dz_v = [v = y] - p_v and dH / dz_v = -p_v (ln p_v + H)).
+    loss = -(1/N) sum_t m_t J_t; pg_term, kl_term, ent_term the masked means of
+    pg, kl and H; n_clipped the tokens whose surrogate gradient the clip cuts.
+    N = 0 gives zeros.  Also returns the per-token arrays of token_objective.
     """
-    lg = np.ascontiguousarray(logits)
-    n_rows, ld = lg.shape
     m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
-    ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
     N = count(m)
-    lse, logp, ent = stats if stats is not None else row_stats(lg, dtype, V, ids, m, threads)
     obj = token_objective(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent)
     mb = m.astype(bool)
     if N > 0:
@@ -297,18 +286,42 @@ def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=No
     else:
         loss = pg_term = kl_term = ent_term = 0.0
     n_clipped = int(obj["clipped"].sum())
-    out = dict(loss=loss, pg_term=pg_term, kl_term=kl_term, ent_term=ent_term,
-               n_tokens=N, n_clipped=n_clipped, clip_frac=(n_clipped / N if N else 0.0),
-               lse=lse, logp=np.where(mb, logp, 0.0), entropy=np.where(mb, ent, 0.0), **obj)
+    return dict(loss=loss, pg_term=pg_term, kl_term=kl_term, ent_term=ent_term, n_tokens=N,
+                n_clipped=n_clipped, clip_frac=(n_clipped / N if N else 0.0),
+                logp=np.where(mb, logp, 0.0), entropy=np.where(mb, ent, 0.0), **obj)
+
+
+def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=None,
+                eps=0.2, beta=0.0, c_ent=0.0, grad_scale=1.0, grad_rows=None,
+                out_dtype=None, threads=None):
+    """The whole fused step on CPU: loss, statistics, per-row outputs and dlogits.
+
+    ``adv_row`` is the advantage of each row (a per-sequence advantage already
+    broadcast over its T positions).  ``grad_rows`` lists the rows whose
+    logits gradient is wanted (all rows if None, none if False); the gradient
+    is returned in ``out_dtype`` (default: the logits' format) as rows
+    [len(grad_rows), V].
+
+    Loss = -(1/N) sum_t m_t J_t; N = 0 gives loss 0 and zero gradients.
+    dz_v = grad_scale (m_t / N) [ g_t (p_v - [v = y_t]) + c_ent p_v (ln p_v + H_t) ]
+    (d logp / dz_v = [v = y] - p_v and dH / dz_v = -p_v (ln p_v + H)).
+    """
+    lg = np.ascontiguousarray(logits)
+    n_rows = lg.shape[0]
+    m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
+    ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+    lse, logp, ent = row_stats(lg, dtype, V, ids, m, threads)
+    out = loss_from_stats(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent)
+    out["lse"] = lse
     if grad_rows is not False:
+        N = out["n_tokens"]
         rows = np.arange(n_rows, dtype=np.int64) if grad_rows is None else \
             np.ascontiguousarray(grad_rows, dtype=np.int64)
+        scale = np.where(m[rows] != 0, grad_scale / N if N else 0.0, 0.0)
         out["grad_rows"] = rows
         out["dlogits"] = dlogits_rows(lg, dtype, V, ids, rows, lse[rows], ent[rows],
-                                      obj["g"][rows],
-                                      np.where(mb[rows], grad_scale / N if N else 0.0, 0.0),
-                                      c_ent, out_dtype if out_dtype is not None else dtype,
-                                      threads)
+                                      out["g"][rows], scale, c_ent,
+                                      out_dtype if out_dtype is not None else dtype, threads)
     return out
 
 

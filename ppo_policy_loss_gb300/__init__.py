@@ -1,0 +1,154 @@
+"""Python binding of librlloss, the GB300-native fused RL policy-loss library.
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name declared in include/rlloss.h, with the same arguments in the
+same order.  Array arguments may be torch CUDA tensors (their data_ptr() is
+passed), plain integer device addresses, or None for NULL.  ``stream`` may be
+a torch.cuda.Stream, an integer cudaStream_t, or None for torch's current
+stream.  A status other than RL_OK raises RlLossError.
+
+There is no fallback: if librlloss.so has not been built (``build()``), every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH, build
+
+RL_OK, RL_ERR_NULL, RL_ERR_SHAPE, RL_ERR_DTYPE, RL_ERR_ALIGN, RL_ERR_ALIAS, \
+    RL_ERR_WORKSPACE, RL_ERR_ID_RANGE, RL_ERR_TIMEOUT, RL_ERR_CUDA, RL_ERR_ARG = range(11)
+RL_F32, RL_BF16, RL_F16 = 0, 1, 2
+RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN = 0, 1
+RL_DEVERR_ID_RANGE, RL_DEVERR_TIMEOUT = 1, 2
+
+DTYPES = {"f32": RL_F32, "bf16": RL_BF16, "f16": RL_F16}
+
+__all__ = [
+    "rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_workspace_size",
+    "rl_policy_loss_fwd_bwd", "rl_policy_loss_launch_shape", "rl_read_device_status",
+    "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
+]
+
+
+class RlLossError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rl_status_string(status)} (status {status})")
+
+
+class rl_loss_stats(ctypes.Structure):
+    _fields_ = [("loss", ctypes.c_double), ("pg_term", ctypes.c_double),
+                ("kl_term", ctypes.c_double), ("ent_term", ctypes.c_double),
+                ("clip_frac", ctypes.c_double), ("n_tokens", ctypes.c_longlong),
+                ("n_clipped", ctypes.c_longlong), ("device_error", ctypes.c_int),
+                ("reserved", ctypes.c_int)]
+
+
+STATS_BYTES = ctypes.sizeof(rl_loss_stats)
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load librlloss.so (built in-tree by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"librlloss.so is not built ({path}); run ppo_policy_loss_gb300.build()")
+    lib = ctypes.CDLL(path)
+    P, LL, I, F, D, SZ = (ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float,
+                          ctypes.c_double, ctypes.c_size_t)
+    lib.rl_group_advantages.argtypes = [P, I, I, D, I, P, P]
+    lib.rl_gae_reverse_scan.argtypes = [P, P, P, I, I, F, F, P, P, P]
+    lib.rl_policy_loss_workspace_size.argtypes = [LL]
+    lib.rl_policy_loss_workspace_size.restype = SZ
+    lib.rl_policy_loss_fwd_bwd.argtypes = [P, I, LL, LL, LL, LL, P, P, P, P, P, I, F, F, F, F,
+                                           P, P, P, P, P, SZ, P]
+    lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
+                                                ctypes.POINTER(I)]
+    lib.rl_read_device_status.argtypes = [P, P]
+    lib.rl_status_string.argtypes = [I]
+    lib.rl_status_string.restype = ctypes.c_char_p
+    for fn in ("rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_fwd_bwd",
+               "rl_policy_loss_launch_shape", "rl_read_device_status"):
+        getattr(lib, fn).restype = I
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype(dt):
+    return DTYPES[dt] if isinstance(dt, str) else int(dt)
+
+
+def _check(status: int, where: str):
+    if status != RL_OK:
+        raise RlLossError(status, where)
+
+
+def rl_status_string(status: int) -> str:
+    return load().rl_status_string(int(status)).decode()
+
+
+def rl_group_advantages(rewards, n_groups, group_size, std_eps, ddof, adv_out, stream=None):
+    _check(load().rl_group_advantages(_ptr(rewards), n_groups, group_size, std_eps, ddof,
+                                      _ptr(adv_out), _stream(stream)), "rl_group_advantages")
+
+
+def rl_gae_reverse_scan(rewards, values, lengths, B, T, gamma, lam, adv_out, returns_out,
+                        stream=None):
+    _check(load().rl_gae_reverse_scan(_ptr(rewards), _ptr(values), _ptr(lengths), B, T, gamma, lam,
+                                      _ptr(adv_out), _ptr(returns_out), _stream(stream)),
+           "rl_gae_reverse_scan")
+
+
+def rl_policy_loss_workspace_size(n_rows) -> int:
+    return int(load().rl_policy_loss_workspace_size(n_rows))
+
+
+def rl_policy_loss_fwd_bwd(logits, dtype, B, T, V, ld, ids, logp_old, ref_logp, mask, adv,
+                           adv_layout, eps, beta, c_ent, grad_scale, dlogits, logp_out,
+                           entropy_out, stats_dev, workspace, workspace_bytes, stream=None):
+    _check(load().rl_policy_loss_fwd_bwd(
+        _ptr(logits), _dtype(dtype), B, T, V, ld, _ptr(ids), _ptr(logp_old), _ptr(ref_logp),
+        _ptr(mask), _ptr(adv), adv_layout, eps, beta, c_ent, grad_scale, _ptr(dlogits),
+        _ptr(logp_out), _ptr(entropy_out), _ptr(stats_dev), _ptr(workspace), workspace_bytes,
+        _stream(stream)), "rl_policy_loss_fwd_bwd")
+
+
+def rl_policy_loss_launch_shape(dtype, V, n_rows):
+    c, n, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().rl_policy_loss_launch_shape(_dtype(dtype), V, n_rows, ctypes.byref(c),
+                                              ctypes.byref(n), ctypes.byref(s)),
+           "rl_policy_loss_launch_shape")
+    return c.value, n.value, s.value
+
+
+def rl_read_device_status(workspace, stream=None) -> int:
+    """Synchronises the stream; returns the status code (does not raise)."""
+    return int(load().rl_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+def stats_from_bytes(raw: bytes) -> dict:
+    """Decode a host copy of one rl_loss_stats record."""
+    st = rl_loss_stats.from_buffer_copy(bytes(raw))
+    return {name: getattr(st, name) for name, _ in rl_loss_stats._fields_}

@@ -1,0 +1,136 @@
+// advantages.cu — rl_group_advantages and rl_gae_reverse_scan (sm_103a).
+//
+// The RL.cu pages name reward normalisation (ainews.cool RL.cu article, the
+// paragraph after its benchmark table) for GRPO, the group-relative method of
+// the pitchhut.com listing ("Key Features" item 3), and advantage estimation
+// inside the PPO update (same article, "PPO 更新内核" bullet).  Both steps
+// touch O(B*T) bytes, so they are latency kernels: one warp per group or per
+// sequence, fp64 arithmetic (cheap at this size, and exact enough that the
+// result is the fp64 definition rounded once to fp32).
+#include <cmath>
+
+#include "rl_device.cuh"
+
+namespace rl {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp per group: two-pass mean and standard deviation, then
+// A = (R - mean) / (std + std_eps).
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+group_advantages_kernel(const float* rewards, int n_groups, int G, double std_eps,
+                        int ddof, float* adv) {
+  const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= n_groups) return;
+  const float* r = rewards + static_cast<long long>(gw) * G;
+  double sum = 0.0;
+  for (int j = lane; j < G; j += 32) sum += static_cast<double>(r[j]);
+  const double mean = warp_sum(sum) / G;
+  double sq = 0.0;
+  for (int j = lane; j < G; j += 32) {
+    const double d = static_cast<double>(r[j]) - mean;
+    sq += d * d;
+  }
+  const double std = sqrt(warp_sum(sq) / (G - ddof));
+  const double inv = 1.0 / (std + std_eps);
+  // Every index is read and written by the same lane, after the reductions
+  // above have consumed all reads, so adv may alias rewards.
+  float* a = adv + static_cast<long long>(gw) * G;
+  for (int j = lane; j < G; j += 32) a[j] = static_cast<float>((static_cast<double>(r[j]) - mean) * inv);
+}
+
+// One warp per sequence.  Lane l owns the contiguous time chunk
+// [l*cs, min(L, (l+1)*cs)).  Each lane folds its chunk into an affine map
+// A_start = P + Q * A_after_chunk (Q = c^len, c = gamma*lam); a suffix scan of
+// these maps across lanes (shuffles, composition from the high lanes down)
+// gives every chunk its incoming A; a second pass over the chunk writes A and
+// ret.  The terminal bootstrap is 0: delta_{L-1} = r_{L-1} - v_{L-1}.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+gae_kernel(const float* __restrict__ rewards, const float* __restrict__ values,
+           const int* __restrict__ lengths, int B, int T, double gamma, double lam, float* adv,
+           float* ret) {
+  const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= B) return;
+  const long long base = static_cast<long long>(b) * T;
+  int L = lengths[b];
+  L = L < 0 ? 0 : (L > T ? T : L);
+  const double c = gamma * lam;
+  const int cs = (L + 31) / 32;
+  const int t0 = min(L, lane * cs), t1 = min(L, t0 + cs);
+
+  auto delta = [&](int t) -> double {
+    const double vn = (t + 1 < L) ? static_cast<double>(values[base + t + 1]) : 0.0;
+    return static_cast<double>(rewards[base + t]) + gamma * vn - static_cast<double>(values[base + t]);
+  };
+
+  double P = 0.0, Q = 1.0;
+  for (int t = t1 - 1; t >= t0; --t) {
+    P = delta(t) + c * P;
+    Q = c * Q;
+  }
+  // inclusive suffix composition: lane l ends with F_l o F_{l+1} o ... o F_31
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double P2 = __shfl_down_sync(0xffffffffu, P, o);
+    const double Q2 = __shfl_down_sync(0xffffffffu, Q, o);
+    if (lane + o < 32) {
+      P = P + Q * P2;
+      Q = Q * Q2;
+    }
+  }
+  double a_next = __shfl_down_sync(0xffffffffu, P, 1);  // A at the start of lane+1's chunk
+  if (lane == 31) a_next = 0.0;
+  // second pass: outputs
+  double a = a_next;
+  for (int t = t1 - 1; t >= t0; --t) {
+    a = delta(t) + c * a;
+    adv[base + t] = static_cast<float>(a);
+    if (ret) ret[base + t] = static_cast<float>(a + static_cast<double>(values[base + t]));
+  }
+  for (int t = L + lane; t < T; t += 32) {
+    adv[base + t] = 0.f;
+    if (ret) ret[base + t] = 0.f;
+  }
+}
+
+}  // namespace
+}  // namespace rl
+
+using namespace rl;
+
+extern "C" rl_status rl_group_advantages(const float* rewards, int n_groups, int group_size,
+                                         double std_eps, int ddof, float* adv_out, void* stream) {
+  if (n_groups < 0 || group_size < 1) return RL_ERR_SHAPE;
+  if (ddof != 0 && ddof != 1) return RL_ERR_ARG;
+  if (!(std_eps >= 0.0) || !std::isfinite(std_eps)) return RL_ERR_ARG;
+  if (group_size <= ddof) return RL_ERR_SHAPE;
+  if (n_groups == 0) return RL_OK;
+  if (!rewards || !adv_out) return RL_ERR_NULL;
+  const int blocks = (n_groups + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  group_advantages_kernel<<<blocks, kWarpsPerBlock * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      rewards, n_groups, group_size, std_eps, ddof, adv_out);
+  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+extern "C" rl_status rl_gae_reverse_scan(const float* rewards, const float* values,
+                                         const int* lengths, int B, int T, float gamma, float lam,
+                                         float* adv_out, float* returns_out, void* stream) {
+  if (B < 0 || T < 0) return RL_ERR_SHAPE;
+  if (!std::isfinite(gamma) || !std::isfinite(lam)) return RL_ERR_ARG;
+  if (B == 0 || T == 0) return RL_OK;
+  if (!rewards || !values || !lengths || !adv_out) return RL_ERR_NULL;
+  const int blocks = (B + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  gae_kernel<<<blocks, kWarpsPerBlock * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      rewards, values, lengths, B, T, static_cast<double>(gamma), static_cast<double>(lam), adv_out,
+      returns_out);
+  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}

@@ -1,0 +1,736 @@
+// policy_loss.cu — rl_policy_loss_fwd_bwd: the fused policy loss and its
+// logits gradient in one launch (sm_103a).
+//
+// The RL.cu pages describe a single fused "PPO update kernel" (ainews.cool
+// RL.cu article, section "技术深度解析", bullet "PPO 更新内核") that computes
+// the whole loss, with the KL penalty and reward normalisation of the
+// paragraph after its benchmark table, in one launch to avoid global-memory
+// round trips.  This kernel is that step for GB300, designed around HBM:
+//
+//   * Persistent grid of thread-block clusters; cluster q takes rows
+//     q, q + Q, q + 2Q, ...  Each of the C CTAs of a cluster owns one slice of
+//     the vocabulary, so that a whole row sits in the cluster's shared memory
+//     (C = 2 for a 151936-wide bf16 row): logits are read from HBM once and
+//     the gradient is written once.
+//   * One producer warp streams slices with 1-D bulk copies (cp.async.bulk,
+//     L2 evict-first) into a ring of 16 KB chunks guarded by mbarriers, and
+//     runs ahead into the next rows while the consumers work.
+//   * Sixteen consumer warps: pass 1 computes per-thread online (max, sum of
+//     exp, sum of exp * x) statistics from shared memory; warp shuffles and a
+//     named barrier combine them per CTA; the CTAs of the cluster exchange
+//     their partials through distributed shared memory with remote mbarrier
+//     arrives; pass 2 re-reads the chunks from shared memory, writes the
+//     gradient with 16-byte streaming stores and frees each chunk.
+//   * Masked rows: all-zero gradient stores only, their logits are not read.
+//   * N (valid tokens) is counted by every CTA at start (R bytes from L2);
+//     the loss is reduced in fp64: per-CTA partials in a fixed row order,
+//     then the last CTA (atomic ticket, no spinning) sums them in CTA order.
+//     Same inputs, same device -> bitwise identical results.
+//   * Every wait on an mbarrier is bounded (1 s); on timeout the kernel
+//     raises RL_DEVERR_TIMEOUT, stops, drains its own bulk copies and exits
+//     through the final cluster barrier.  No trap, no unbounded spin.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "rl_device.cuh"
+
+namespace rl {
+namespace {
+
+constexpr int kChunkBytes = 16384;
+constexpr int kSlots = 13;
+constexpr int kLookaheadChunks = 3;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kMaxCluster = 8;
+constexpr int kVecsPerChunk = kChunkBytes / 16;
+constexpr int kVecsPerThread = kVecsPerChunk / kConsumerThreads;
+static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly over consumers");
+constexpr uint32_t kConsumerBarrier = 1;  // named barrier id (0 is __syncthreads)
+
+struct LossSmem {
+  alignas(128) unsigned char ring[kSlots][kChunkBytes];
+  unsigned long long full[kSlots];
+  unsigned long long empty[kSlots];
+  unsigned long long xbar[2];
+  float4 xpart[2][kMaxCluster];
+  float4 wpart[kConsumerWarps];
+  long long wcount[kConsumerWarps];
+  double wred[kConsumerWarps][5];
+  float zy;
+  int abort;
+  int is_last;
+};
+
+struct LossArgs {
+  const unsigned char* logits;
+  unsigned char* dlogits;
+  const long long* ids;
+  const float* logp_old;
+  const float* ref_logp;
+  const unsigned char* mask;
+  const float* adv;
+  float* logp_out;
+  float* entropy_out;
+  rl_loss_stats* stats;
+  WsHeader* ws;
+  WsPartial* partials;
+  long long R, T, V;
+  long long row_bytes;  // ld * element bytes
+  long long slice;      // vocabulary elements per cluster rank
+  int adv_per_token;
+  float eps, beta, c_ent, grad_scale;
+};
+
+// ------------------------------------------------------------------ element formats
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<RL_F32> {
+  static constexpr int kBytes = 4, kVec = 4;
+  __device__ static void unpack(const uint4& w, float (&z)[kVec]) {
+    z[0] = __uint_as_float(w.x);
+    z[1] = __uint_as_float(w.y);
+    z[2] = __uint_as_float(w.z);
+    z[3] = __uint_as_float(w.w);
+  }
+  __device__ static uint4 pack(const float (&z)[kVec]) {
+    return make_uint4(__float_as_uint(z[0]), __float_as_uint(z[1]), __float_as_uint(z[2]),
+                      __float_as_uint(z[3]));
+  }
+  __device__ static void store1(unsigned char* p, float v) { *reinterpret_cast<float*>(p) = v; }
+};
+
+template <>
+struct Elem<RL_BF16> {
+  static constexpr int kBytes = 2, kVec = 8;
+  __device__ static void unpack(const uint4& w, float (&z)[kVec]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      z[2 * k] = __uint_as_float(u[k] << 16);
+      z[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+    }
+  }
+  __device__ static uint4 pack(const float (&z)[kVec]) {
+    uint32_t u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(z[2 * k], z[2 * k + 1]);
+      u[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+  __device__ static void store1(unsigned char* p, float v) {
+    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+  }
+};
+
+template <>
+struct Elem<RL_F16> {
+  static constexpr int kBytes = 2, kVec = 8;
+  __device__ static void unpack(const uint4& w, float (&z)[kVec]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[k]));
+      z[2 * k] = f.x;
+      z[2 * k + 1] = f.y;
+    }
+  }
+  __device__ static uint4 pack(const float (&z)[kVec]) {
+    uint32_t u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 h = __floats2half2_rn(z[2 * k], z[2 * k + 1]);
+      u[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+  __device__ static void store1(unsigned char* p, float v) {
+    *reinterpret_cast<__half*>(p) = __float2half_rn(v);
+  }
+};
+
+// ------------------------------------------------------------------ online statistics
+// A partial (m, s, t) over a set of logits z: m = max z, s = sum 2^x,
+// t = sum 2^x * x with x = (z - m) * log2(e).  Then for the full row
+// lse = m + ln s and H = ln 2 * (log2 s - t / s).
+__device__ __forceinline__ void merge_stats(float& m, float& s, float& t, float m2, float s2,
+                                            float t2) {
+  if (m2 > m) {
+    float tmp = m; m = m2; m2 = tmp;
+    tmp = s; s = s2; s2 = tmp;
+    tmp = t; t = t2; t2 = tmp;
+  }
+  if (s2 == 0.f) return;  // empty partner (a NaN s2 falls through and poisons)
+  const float d = (m - m2) * kLog2e;
+  const float f = ex2_approx(-d);
+  s = fmaf(f, s2, s);
+  t = fmaf(f, t2 - d * s2, t);
+}
+
+template <int NV>
+__device__ __forceinline__ void accumulate(const float (&z)[NV], int nv, float& m, float& s,
+                                           float& t) {
+  float vm = z[0];
+#pragma unroll
+  for (int i = 1; i < NV; ++i)
+    if (i < nv) vm = max_nan(vm, z[i]);
+  if (vm > m) {
+    if (m != -INFINITY) {
+      const float d = (vm - m) * kLog2e;
+      const float f = ex2_approx(-d);
+      t = f * fmaf(-d, s, t);
+      s = f * s;
+    }
+    m = vm;
+  }
+  if (m == -INFINITY) {  // nothing finite yet: only a NaN must be remembered
+    if (vm != vm) s = vm;
+    return;
+  }
+  const float mL = m * kLog2e;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    if (i < nv) {
+      const float x = max_nan(fmaf(z[i], kLog2e, -mL), -250.f);
+      const float e = ex2_approx(x);
+      s += e;
+      t = fmaf(e, x, t);
+    }
+  }
+}
+
+template <class E>
+__device__ __forceinline__ void zero_slice(unsigned char* drow, long long nelem, int tid) {
+  const long long nvec = nelem / E::kVec;
+  for (long long j = tid; j < nvec; j += kConsumerThreads)
+    st_global_cs_v4(drow + j * 16, make_uint4(0u, 0u, 0u, 0u));
+  for (long long e = nvec * E::kVec + tid; e < nelem; e += kConsumerThreads)
+    E::store1(drow + e * E::kBytes, 0.f);
+}
+
+// Wait for a bulk copy to land regardless of the abort flag (used to drain).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs a) {
+  using E = Elem<DT>;
+  constexpr int kVec = E::kVec;
+  constexpr int kChunkElems = kChunkBytes / E::kBytes;
+
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  LossSmem& sm = *reinterpret_cast<LossSmem*>(smem_raw);
+  volatile int* abort_flag = &sm.abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank(), csize = cluster_size();
+  const uint32_t cid = cluster_id(), ncl = cluster_count();
+
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_addr(&sm.full[s]), 1);
+      mbar_init(smem_addr(&sm.empty[s]), kConsumerWarps);
+    }
+    mbar_init(smem_addr(&sm.xbar[0]), csize);
+    mbar_init(smem_addr(&sm.xbar[1]), csize);
+    sm.abort = 0;
+    sm.is_last = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync_all();  // every peer's barriers exist before any remote arrive
+
+  const long long lo = static_cast<long long>(rank) * a.slice;
+  const long long hi = min(a.V, lo + a.slice);
+  const long long nelem = hi > lo ? hi - lo : 0;
+  const long long slice_bytes = (nelem * E::kBytes + 15) & ~15LL;
+  const int nchunks = static_cast<int>((slice_bytes + kChunkBytes - 1) / kChunkBytes);
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      bool stop = false;
+      for (long long row = cid; row < a.R && !stop; row += ncl) {
+        if (!a.mask[row] || nchunks == 0) continue;
+        const unsigned char* src = a.logits + row * a.row_bytes + lo * E::kBytes;
+        for (int c = 0; c < nchunks; ++c, ++it) {
+          const uint32_t slot = it % kSlots, round = it / kSlots;
+          if (round > 0 &&
+              !wait_bounded<false>(smem_addr(&sm.empty[slot]), (round - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          if (*abort_flag) {
+            stop = true;
+            break;
+          }
+          const uint32_t bytes = static_cast<uint32_t>(
+              min(static_cast<long long>(kChunkBytes), slice_bytes - static_cast<long long>(c) * kChunkBytes));
+          const uint32_t fb = smem_addr(&sm.full[slot]);
+          mbar_arrive_expect_tx(fb, bytes);
+          bulk_load(smem_addr(sm.ring[slot]), src + static_cast<long long>(c) * kChunkBytes, bytes, fb,
+                    pol);
+        }
+      }
+      if (stop) {  // let every copy already issued land before this CTA can exit
+        for (uint32_t k = it > kSlots ? it - kSlots : 0; k < it; ++k)
+          drain_wait(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    // N = number of valid tokens; every CTA counts the whole mask.
+    long long cnt = 0;
+    {
+      long long i0 = 0;
+      if ((reinterpret_cast<uintptr_t>(a.mask) & 15) == 0) {
+        const long long nv = a.R >> 4;
+        const uint4* mv = reinterpret_cast<const uint4*>(a.mask);
+        for (long long i = tid; i < nv; i += kConsumerThreads) {
+          const uint4 w = __ldg(mv + i);
+          cnt += (__popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
+                  __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u))) >> 3;
+        }
+        i0 = nv << 4;
+      }
+      for (long long i = i0 + tid; i < a.R; i += kConsumerThreads) cnt += a.mask[i] != 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (lane == 0) sm.wcount[warp] = cnt;
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      cnt = 0;
+      for (int w = 0; w < kConsumerWarps; ++w) cnt += sm.wcount[w];
+    }
+    const long long N = cnt;
+    const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
+
+    double acc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // J, pg, kl, H, clipped (rank 0, thread 0)
+    unsigned int err = 0;
+    uint32_t it = 0, vrow = 0;
+    bool aborted = false;
+
+    for (long long row = cid; row < a.R; row += ncl) {
+      const bool valid = a.mask[row] != 0;  // the same for every CTA of the cluster
+      unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes + lo * E::kBytes : nullptr;
+      if (!valid) {
+        if (drow) zero_slice<E>(drow, nelem, tid);
+        if (rank == 0 && tid == 0) {
+          if (a.logp_out) a.logp_out[row] = 0.f;
+          if (a.entropy_out) a.entropy_out[row] = 0.f;
+        }
+        continue;
+      }
+      const long long y = a.ids[row];
+      const float A = a.adv[a.adv_per_token ? row : row / a.T];
+      const float lpo = a.logp_old ? a.logp_old[row] : 0.f;
+      const float rf = a.ref_logp ? a.ref_logp[row] : 0.f;
+      const bool y_here = (y >= lo) && (y < hi);
+
+      // ---- pass 1: online statistics of this thread's share of the slice
+      float m = -INFINITY, s = 0.f, t = 0.f;
+      for (int c = 0; c < nchunks; ++c) {
+        const uint32_t k = it + c, slot = k % kSlots;
+        wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
+        const uint32_t buf = smem_addr(sm.ring[slot]);
+        const long long c0 = lo + static_cast<long long>(c) * kChunkElems;
+#pragma unroll
+        for (int q = 0; q < kVecsPerThread; ++q) {
+          const int j = tid + q * kConsumerThreads;
+          const long long e0 = c0 + static_cast<long long>(j) * kVec;
+          if (e0 < hi) {
+            float z[kVec];
+            E::unpack(ld_shared_v4(buf + j * 16), z);
+            const int nv = (hi - e0 >= kVec) ? kVec : static_cast<int>(hi - e0);
+            if (y_here && static_cast<unsigned long long>(y - e0) < static_cast<unsigned long long>(kVec)) {
+#pragma unroll
+              for (int i = 0; i < kVec; ++i)
+                if (i == y - e0) sm.zy = z[i];
+            }
+            accumulate<kVec>(z, nv, m, s, t);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
+        merge_stats(m, s, t, m2, s2, t2);
+      }
+      if (lane == 0) sm.wpart[warp] = make_float4(m, s, t, 0.f);
+      if (named_barrier_or(kConsumerBarrier, kConsumerThreads, *abort_flag != 0)) {
+        aborted = true;
+        break;
+      }
+
+      // ---- exchange the CTA partials across the cluster (DSMEM + remote arrive)
+      const uint32_t b = vrow & 1;
+      if (tid == 0) {
+        float M = sm.wpart[0].x, S = sm.wpart[0].y, Tt = sm.wpart[0].z;
+        for (int w = 1; w < kConsumerWarps; ++w)
+          merge_stats(M, S, Tt, sm.wpart[w].x, sm.wpart[w].y, sm.wpart[w].z);
+        const float4 P = make_float4(M, S, Tt, y_here ? sm.zy : 0.f);
+        const uint32_t xa = smem_addr(&sm.xpart[b][rank]);
+        const uint32_t ba = smem_addr(&sm.xbar[b]);
+        for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
+        for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
+      }
+      wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
+
+      float M = -INFINITY, S = 0.f, Tt = 0.f;
+      for (uint32_t q = 0; q < csize; ++q) {
+        const float4 P = sm.xpart[b][q];
+        merge_stats(M, S, Tt, P.x, P.y, P.z);
+      }
+      const bool y_ok = (y >= 0) && (y < a.V);
+      const float zy = y_ok ? sm.xpart[b][static_cast<uint32_t>(y / a.slice)].w : __int_as_float(0x7fc00000);
+      const float log2S = log2f(S);
+      const float lse = fmaf(log2S, kLn2, M);
+      const float H = kLn2 * (log2S - Tt / S);
+      const float logp = zy - lse;
+
+      // ---- per-token objective and its derivative with respect to logp
+      const float r = a.logp_old ? expf(logp - lpo) : 1.f;
+      const float rA = r * A;
+      const float pg = fminf(rA, fminf(fmaxf(r, 1.f - a.eps), 1.f + a.eps) * A);
+      const bool clipped = (A > 0.f && r > 1.f + a.eps) || (A < 0.f && r < 1.f - a.eps);
+      const float dpg = clipped ? 0.f : rA;
+      float kl = 0.f, dkl = 0.f;
+      if (a.ref_logp) {
+        const float d = rf - logp;
+        dkl = expm1f(d);
+        kl = dkl - d;
+      }
+      float J = pg - a.beta * kl + a.c_ent * H;
+      float g = dpg + a.beta * dkl;
+      if (logp != logp) {  // NaN logp (bad id or NaN logits): poison the row
+        J = logp;
+        g = logp;
+      }
+      if (rank == 0 && tid == 0) {
+        acc[0] += J;
+        acc[1] += pg;
+        acc[2] += kl;
+        acc[3] += H;
+        acc[4] += clipped ? 1.0 : 0.0;
+        if (!y_ok) err |= RL_DEVERR_ID_RANGE;
+        if (a.logp_out) a.logp_out[row] = logp;
+        if (a.entropy_out) a.entropy_out[row] = H;
+      }
+
+      // ---- pass 2: dz_v = sc [g (p_v - [v == y]) + c_ent p_v (ln p_v + H)]
+      //      with x_v = z_v log2(e) - (M log2(e) + log2 S):  p_v = 2^x_v, ln p_v = x_v ln 2
+      const float cL = fmaf(M, kLog2e, log2S);
+      const float a0 = sc * fmaf(a.c_ent, H, g);
+      const float a1 = sc * a.c_ent * kLn2;
+      const float gy = sc * g;
+      for (int c = 0; c < nchunks; ++c) {
+        const uint32_t slot = (it + c) % kSlots;
+        if (drow) {
+          const uint32_t buf = smem_addr(sm.ring[slot]);
+          const long long c0 = lo + static_cast<long long>(c) * kChunkElems;
+#pragma unroll
+          for (int q = 0; q < kVecsPerThread; ++q) {
+            const int j = tid + q * kConsumerThreads;
+            const long long e0 = c0 + static_cast<long long>(j) * kVec;
+            if (e0 < hi) {
+              float z[kVec], d[kVec];
+              E::unpack(ld_shared_v4(buf + j * 16), z);
+#pragma unroll
+              for (int i = 0; i < kVec; ++i) {
+                const float x = max_nan(fmaf(z[i], kLog2e, -cL), -250.f);
+                d[i] = ex2_approx(x) * fmaf(a1, x, a0);
+              }
+              if (y_here && static_cast<unsigned long long>(y - e0) < static_cast<unsigned long long>(kVec)) {
+#pragma unroll
+                for (int i = 0; i < kVec; ++i)
+                  if (i == y - e0) d[i] -= gy;
+              }
+              unsigned char* dst = drow + (e0 - lo) * E::kBytes;
+              if (hi - e0 >= kVec) {
+                st_global_cs_v4(dst, E::pack(d));
+              } else {
+#pragma unroll
+                for (int i = 0; i < kVec; ++i)
+                  if (i < hi - e0) E::store1(dst + i * E::kBytes, d[i]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+      }
+      it += nchunks;
+      ++vrow;
+    }
+
+    // ---- per-CTA partial, then the last CTA reduces all partials in CTA order
+    if (tid == 0) {
+      WsPartial& P = a.partials[blockIdx.x];
+      for (int k = 0; k < 5; ++k) P.v[k] = acc[k];
+      if (aborted || *abort_flag) err |= RL_DEVERR_TIMEOUT;
+      if (err) atomicOr(&a.ws->status, err);
+      __threadfence();
+      const unsigned int ticket = atomicInc(&a.ws->ticket, gridDim.x - 1);
+      sm.is_last = (ticket == gridDim.x - 1);
+    }
+    named_barrier(kConsumerBarrier, kConsumerThreads);
+    if (sm.is_last) {
+      __threadfence();
+      double v[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+      for (int i = tid; i < static_cast<int>(gridDim.x); i += kConsumerThreads)
+        for (int k = 0; k < 5; ++k) v[k] += __ldcg(&a.partials[i].v[k]);
+      for (int k = 0; k < 5; ++k) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+      }
+      if (lane == 0)
+        for (int k = 0; k < 5; ++k) sm.wred[warp][k] = v[k];
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      if (tid == 0) {
+        double tot[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+        for (int w = 0; w < kConsumerWarps; ++w)
+          for (int k = 0; k < 5; ++k) tot[k] += sm.wred[w][k];
+        const unsigned int st = atomicExch(&a.ws->status, 0u);
+        a.ws->last_status = st;
+        rl_loss_stats out;
+        const double inv = N > 0 ? 1.0 / static_cast<double>(N) : 0.0;
+        out.loss = -tot[0] * inv;
+        out.pg_term = tot[1] * inv;
+        out.kl_term = tot[2] * inv;
+        out.ent_term = tot[3] * inv;
+        out.clip_frac = tot[4] * inv;
+        out.n_tokens = N;
+        out.n_clipped = static_cast<long long>(tot[4]);
+        out.device_error = static_cast<int>(st);
+        out.reserved = 0;
+        *a.stats = out;
+      }
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still touch its shared memory
+}
+
+// ------------------------------------------------------------------ host side
+int elem_bytes(rl_dtype dt) {
+  switch (dt) {
+    case RL_F32: return 4;
+    case RL_BF16: return 2;
+    case RL_F16: return 2;
+  }
+  return 0;
+}
+
+// Smallest cluster whose per-CTA slice fits the ring with room to prefetch
+// the next row (else without that room).  Returns 0 if no cluster fits.
+int choose_cluster(int es, long long V, long long* slice_out) {
+  const long long align = 16 / es;
+  for (int pass = 0; pass < 2; ++pass) {
+    const long long budget = pass == 0 ? kSlots - kLookaheadChunks : kSlots;
+    for (int c = 1; c <= kMaxCluster; ++c) {
+      long long s = (V + c - 1) / c;
+      s = (s + align - 1) / align * align;
+      const long long chunks = (s * es + kChunkBytes - 1) / kChunkBytes;
+      if (chunks <= budget) {
+        *slice_out = s;
+        return c;
+      }
+    }
+  }
+  return 0;
+}
+
+template <int DT>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(&policy_loss_kernel<DT>);
+}
+
+void* kernel_for(rl_dtype dt) {
+  switch (dt) {
+    case RL_F32: return kernel_ptr<RL_F32>();
+    case RL_BF16: return kernel_ptr<RL_BF16>();
+    case RL_F16: return kernel_ptr<RL_F16>();
+  }
+  return nullptr;
+}
+
+// Per (device, dtype, cluster size): attributes set once and the number of
+// co-resident clusters.
+std::mutex g_occ_mu;
+std::map<std::tuple<int, int, int>, int> g_occ;
+
+rl_status max_clusters(rl_dtype dt, int cluster, int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
+  const auto key = std::make_tuple(dev, static_cast<int>(dt), cluster);
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  auto found = g_occ.find(key);
+  if (found != g_occ.end()) {
+    *out = found->second;
+    return RL_OK;
+  }
+  void* fn = kernel_for(dt);
+  const int smem = static_cast<int>(sizeof(LossSmem));
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return RL_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) return RL_ERR_CUDA;
+  g_occ[key] = n;
+  *out = n;
+  return RL_OK;
+}
+
+rl_status plan(rl_dtype dt, long long V, long long R, int* cluster, int* n_clusters,
+               long long* slice) {
+  const int es = elem_bytes(dt);
+  if (es == 0) return RL_ERR_DTYPE;
+  if (V < 1 || R < 0) return RL_ERR_SHAPE;
+  const int c = choose_cluster(es, V, slice);
+  if (c == 0) return RL_ERR_SHAPE;
+  int occ = 0;
+  const rl_status st = max_clusters(dt, c, &occ);
+  if (st != RL_OK) return st;
+  long long n = occ;
+  if (n > R) n = R > 0 ? R : 1;
+  if (n * c > kMaxGrid) n = kMaxGrid / c;
+  *cluster = c;
+  *n_clusters = static_cast<int>(n);
+  return RL_OK;
+}
+
+bool finite(float x) { return std::isfinite(x); }
+
+}  // namespace
+}  // namespace rl
+
+using namespace rl;
+
+extern "C" size_t rl_policy_loss_workspace_size(long long n_rows) {
+  (void)n_rows;
+  return kWorkspaceBytes;
+}
+
+extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, long long n_rows,
+                                                 int* cluster_size, int* n_clusters,
+                                                 int* smem_bytes) {
+  if (!cluster_size || !n_clusters || !smem_bytes) return RL_ERR_NULL;
+  long long slice = 0;
+  int c = 0, n = 0;
+  const rl_status st = plan(dtype, V, n_rows, &c, &n, &slice);
+  if (st != RL_OK) return st;
+  *cluster_size = c;
+  *n_clusters = n;
+  *smem_bytes = static_cast<int>(sizeof(LossSmem));
+  return RL_OK;
+}
+
+extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, long long B,
+                                            long long T, long long V, long long ld,
+                                            const long long* ids, const float* logp_old,
+                                            const float* ref_logp, const unsigned char* mask,
+                                            const float* adv, rl_adv_layout adv_layout, float eps,
+                                            float beta, float c_ent, float grad_scale,
+                                            void* dlogits, float* logp_out, float* entropy_out,
+                                            rl_loss_stats* stats_dev, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  const int es = elem_bytes(dtype);
+  if (es == 0) return RL_ERR_DTYPE;
+  if (adv_layout != RL_ADV_PER_SEQ && adv_layout != RL_ADV_PER_TOKEN) return RL_ERR_DTYPE;
+  if (B < 0 || T < 0 || V < 1 || ld < V) return RL_ERR_SHAPE;
+  if (B > 0 && T > (1LL << 40) / B) return RL_ERR_SHAPE;
+  const long long R = B * T;
+  if (!stats_dev) return RL_ERR_NULL;
+  if (!workspace || workspace_bytes < rl_policy_loss_workspace_size(R)) return RL_ERR_WORKSPACE;
+  if (R > 0 && (!logits || !ids || !mask || !adv)) return RL_ERR_NULL;
+  if (beta != 0.f && !ref_logp) return RL_ERR_NULL;
+  if (!finite(eps) || eps < 0.f || !finite(beta) || !finite(c_ent) || !finite(grad_scale))
+    return RL_ERR_ARG;
+  const long long row_bytes = ld * es;
+  if ((row_bytes & 15) != 0) return RL_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(logits) & 15) != 0) return RL_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(dlogits) & 15) != 0) return RL_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return RL_ERR_ALIGN;
+  if (dlogits && dlogits != logits && R > 0) {
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(logits), d0 = reinterpret_cast<uintptr_t>(dlogits);
+    const uintptr_t n = static_cast<uintptr_t>(R) * static_cast<uintptr_t>(row_bytes);
+    if (l0 < d0 + n && d0 < l0 + n) return RL_ERR_ALIAS;
+  }
+
+  int cluster = 0, n_clusters = 0;
+  long long slice = 0;
+  const rl_status st = plan(dtype, V, R, &cluster, &n_clusters, &slice);
+  if (st != RL_OK) return st;
+
+  LossArgs args;
+  args.logits = static_cast<const unsigned char*>(logits);
+  args.dlogits = static_cast<unsigned char*>(dlogits);
+  args.ids = ids;
+  args.logp_old = logp_old;
+  args.ref_logp = ref_logp;
+  args.mask = mask;
+  args.adv = adv;
+  args.logp_out = logp_out;
+  args.entropy_out = entropy_out;
+  args.stats = stats_dev;
+  args.ws = static_cast<WsHeader*>(workspace);
+  args.partials = reinterpret_cast<WsPartial*>(static_cast<unsigned char*>(workspace) + sizeof(WsHeader));
+  args.R = R;
+  args.T = T > 0 ? T : 1;
+  args.V = V;
+  args.row_bytes = row_bytes;
+  args.slice = slice;
+  args.adv_per_token = adv_layout == RL_ADV_PER_TOKEN;
+  args.eps = eps;
+  args.beta = beta;
+  args.c_ent = c_ent;
+  args.grad_scale = grad_scale;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster * n_clusters));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(LossSmem);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (dtype) {
+    case RL_F32: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32>, args); break;
+    case RL_BF16: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_BF16>, args); break;
+    case RL_F16: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16>, args); break;
+  }
+  return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}

@@ -1,0 +1,152 @@
+"""Shared helpers for the GPU parity tests: build inputs, run both sides, compare.
+
+Inputs come from ppo_policy_loss_gb300.synth; the oracle's inputs are host
+copies of the same bytes.  The behaviour-policy and reference log-probs are
+the ORACLE's logp plus the drawn noise (never the GPU's).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from ppo_policy_loss_gb300 import synth
+
+# ---------------------------------------------------------------- tolerances
+LOGP_ATOL = 2e-3          # per-token logp and entropy, absolute
+LOSS_RTOL = 1e-4          # scalar loss and the masked means, relative
+LOSS_ATOL_FLOOR = 1e-7    # absolute floor when |value| < 1e-3
+ADV_TOL = 1e-5            # advantages / GAE: |d| <= 1e-5 * max(|ref|, 1)
+DLOGIT_ATOL = 1e-6
+# fp32 dlogits: the kernel computes p_v = 2^x in fp32 with |x| up to ~60, so x
+# carries an absolute rounding error up to ~8e-6 and p_v a relative one up to
+# ~6e-6; 2^-16 (1.5e-5) bounds it.  bf16 and fp16 outputs need no such term:
+# one ulp of theirs (2^-8, 2^-11 relative) dominates.
+DLOGIT_F32_RTOL = 2.0 ** -16
+CLIP_BAND = 1e-4          # |r - (1 +/- eps)| below this: clip decision may flip
+
+
+def storage_np(t: torch.Tensor) -> np.ndarray:
+    """Host numpy view of a tensor's element storage (uint16 for bf16/f16)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def adv_rows(w, small, T=None):
+    """Per-row advantage from the oracle (group advantages or GAE)."""
+    T = w.T if T is None else T
+    if w.advantage == "gae":
+        A, _ = oracle.gae(small["rewards"], small["values"], small["lengths"], w.gamma, w.lam)
+        return A.reshape(-1), A
+    A = oracle.group_advantages(small["rewards"], w.group)
+    return np.repeat(A, T), A
+
+
+def oracle_stats_chunked(logits_t, dtype, V, ids, mask, chunk=2048):
+    """Oracle (lse, logp, H) for every row, copying only valid rows to the host."""
+    R = mask.size
+    lse, logp, ent = np.zeros(R), np.zeros(R), np.zeros(R)
+    idx = np.nonzero(mask)[0]
+    for i0 in range(0, idx.size, chunk):
+        sel = idx[i0:i0 + chunk]
+        host = storage_np(logits_t.index_select(0, torch.from_numpy(sel).to(logits_t.device))[:, :V])
+        l, p, h = oracle.row_stats(host, dtype, V, ids[sel], np.ones(sel.size, np.uint8))
+        lse[sel], logp[sel], ent[sel] = l, p, h
+    return lse, logp, ent
+
+
+def band_mask(o, eps):
+    r = o["r"]
+    return (np.abs(r - (1 + eps)) < CLIP_BAND) | (np.abs(r - (1 - eps)) < CLIP_BAND)
+
+
+def assert_scalar_close(name, got, ref):
+    tol = LOSS_RTOL * abs(ref)
+    if abs(ref) < 1e-3:
+        tol = max(tol, LOSS_ATOL_FLOOR)
+    assert abs(got - ref) <= tol, f"{name}: gpu {got!r} oracle {ref!r} (|d| {abs(got - ref):.3g} > {tol:.3g})"
+
+
+def assert_stats_match(st, ref, n_band=0):
+    """Scalars within LOSS_RTOL; counts bit-exact (n_clipped up to the n_band
+    valid tokens whose ratio lies within CLIP_BAND of a clip boundary)."""
+    assert st["device_error"] == 0, st
+    assert st["n_tokens"] == ref["n_tokens"]
+    assert abs(st["n_clipped"] - ref["n_clipped"]) <= n_band, (st["n_clipped"], ref["n_clipped"], n_band)
+    for k in ("loss", "pg_term", "kl_term", "ent_term"):
+        assert_scalar_close(k, st[k], ref[k])
+
+
+def assert_rows_close(logp_gpu, H_gpu, ref, mask):
+    mb = mask.astype(bool)
+    assert np.all(logp_gpu[~mb] == 0) and np.all(H_gpu[~mb] == 0)
+    dl = np.abs(logp_gpu[mb] - ref["logp"][mb])
+    dh = np.abs(H_gpu[mb] - ref["entropy"][mb])
+    assert dl.size == 0 or dl.max() <= LOGP_ATOL, f"logp max err {dl.max():.3g}"
+    assert dh.size == 0 or dh.max() <= LOGP_ATOL, f"entropy max err {dh.max():.3g}"
+    return (dl.max() if dl.size else 0.0), (dh.max() if dh.size else 0.0)
+
+
+def assert_dlogits_close(gpu_store, ref_store, dtype, where=""):
+    g = oracle.decode(gpu_store, dtype)
+    r = oracle.decode(ref_store, dtype)
+    tol = oracle.ulp(r, dtype) + DLOGIT_ATOL
+    if dtype == "f32":
+        tol = tol + DLOGIT_F32_RTOL * np.abs(r)
+    err = np.abs(g - r)
+    bad = ~(err <= tol)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{where} dlogits: {int(bad.sum())} elements out of tolerance; first at "
+                             f"{tuple(i)}: gpu {g[tuple(i)]!r} oracle {r[tuple(i)]!r} tol {tol[tuple(i)]!r}")
+    return float((err / np.maximum(oracle.ulp(r, dtype), 1e-300)).max()) if err.size else 0.0
+
+
+def build_case(w, device="cuda", ld=None, n_rows=None):
+    """Inputs for workload w (optionally only its first n_rows rows, T kept)."""
+    small = synth.small_inputs(w)
+    V = w.V
+    ld = V if ld is None else ld
+    logits = synth.logits(w, device=device, ld=ld)
+    if n_rows is not None:
+        logits = logits[:n_rows].contiguous() if ld == V else logits[:n_rows]
+    return small, logits
+
+
+def composed_old_ref(logp_oracle, small, mask, R):
+    """logp_old = oracle logp + N(0, old_sd); ref = oracle logp + N(0, ref_sd); stored fp32."""
+    lo = (logp_oracle + small["noise_old"][:R]).astype(np.float32)
+    rf = (logp_oracle + small["noise_ref"][:R]).astype(np.float32)
+    lo[mask == 0] = 0.0
+    rf[mask == 0] = 0.0
+    return lo, rf
+
+
+def to_dev(x, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def valid_and_masked_sample(mask, k, seed=0):
+    rng = np.random.default_rng(seed)
+    v = np.nonzero(mask)[0]
+    m = np.nonzero(mask == 0)[0]
+    pick = list(rng.choice(v, size=min(k, v.size), replace=False)) if v.size else []
+    pick += list(rng.choice(m, size=min(max(1, k // 4), m.size), replace=False)) if m.size else []
+    if v.size:
+        pick += [int(v[0]), int(v[-1])]
+    return np.unique(np.array(pick, np.int64))
+
+
+def rel(a, b):
+    return abs(a - b) / max(abs(b), 1e-30)
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+__all__ = [n for n in dir() if not n.startswith("_")] + ["math"]

@@ -1,0 +1,140 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every function include/rlloss.h declares, and rejects bad arguments on the
+host before anything is launched (no GPU needed; fake device addresses are
+never dereferenced on these paths)."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+import ppo_policy_loss_gb300 as rl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rlloss.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists(
+    "/usr/local/cuda/bin/nvcc"), reason="no CUDA toolkit")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rl.build()
+    return rl.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rl_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_fwd_bwd",
+              "rl_policy_loss_workspace_size", "rl_read_device_status", "rl_status_string",
+              "rl_policy_loss_launch_shape"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", rl.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for s in range(11):
+        assert rl.rl_status_string(s) and rl.rl_status_string(s) != "unknown status"
+    assert rl.rl_status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    n = rl.rl_policy_loss_workspace_size(131072)
+    assert n >= 256 and n % 16 == 0
+    assert rl.rl_policy_loss_workspace_size(0) == n
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced on error paths
+
+
+def call_loss(lib, **over):
+    a = dict(logits=FAKE, dtype=rl.RL_BF16, B=2, T=4, V=1024, ld=1024, ids=FAKE + 0x100000,
+             logp_old=None, ref_logp=None, mask=FAKE + 0x200000, adv=FAKE + 0x300000,
+             adv_layout=rl.RL_ADV_PER_SEQ, eps=0.2, beta=0.0, c_ent=0.0, grad_scale=1.0,
+             dlogits=FAKE + 0x400000, logp_out=None, entropy_out=None, stats=FAKE + 0x500000,
+             workspace=FAKE + 0x600000, ws_bytes=rl.rl_policy_loss_workspace_size(8), stream=None)
+    a.update(over)
+    return lib.rl_policy_loss_fwd_bwd(a["logits"], a["dtype"], a["B"], a["T"], a["V"], a["ld"],
+                                      a["ids"], a["logp_old"], a["ref_logp"], a["mask"], a["adv"],
+                                      a["adv_layout"], a["eps"], a["beta"], a["c_ent"],
+                                      a["grad_scale"], a["dlogits"], a["logp_out"],
+                                      a["entropy_out"], a["stats"], a["workspace"], a["ws_bytes"],
+                                      a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(dtype=7), rl.RL_ERR_DTYPE),
+    (dict(adv_layout=3), rl.RL_ERR_DTYPE),
+    (dict(V=0), rl.RL_ERR_SHAPE),
+    (dict(ld=1000), rl.RL_ERR_SHAPE),
+    (dict(B=-1), rl.RL_ERR_SHAPE),
+    (dict(T=-3), rl.RL_ERR_SHAPE),
+    (dict(stats=None), rl.RL_ERR_NULL),
+    (dict(ids=None), rl.RL_ERR_NULL),
+    (dict(mask=None), rl.RL_ERR_NULL),
+    (dict(adv=None), rl.RL_ERR_NULL),
+    (dict(logits=None), rl.RL_ERR_NULL),
+    (dict(beta=0.1), rl.RL_ERR_NULL),                      # KL without ref_logp
+    (dict(workspace=None), rl.RL_ERR_WORKSPACE),
+    (dict(ws_bytes=16), rl.RL_ERR_WORKSPACE),
+    (dict(eps=float("nan")), rl.RL_ERR_ARG),
+    (dict(eps=-0.1), rl.RL_ERR_ARG),
+    (dict(grad_scale=float("inf")), rl.RL_ERR_ARG),
+    (dict(c_ent=float("nan")), rl.RL_ERR_ARG),
+    (dict(V=1001, ld=1001), rl.RL_ERR_ALIGN),             # 2002-byte rows
+    (dict(logits=FAKE + 8), rl.RL_ERR_ALIGN),
+    (dict(dlogits=FAKE + 0x400002), rl.RL_ERR_ALIGN),
+    (dict(dlogits=FAKE + 16), rl.RL_ERR_ALIAS),           # partial overlap
+])
+def test_loss_argument_errors(lib, over, status):
+    assert call_loss(lib, **over) == status
+
+
+def test_group_advantages_argument_errors(lib):
+    f = lib.rl_group_advantages
+    assert f(FAKE, 4, 0, 1e-4, 1, FAKE, None) == rl.RL_ERR_SHAPE
+    assert f(FAKE, -1, 4, 1e-4, 1, FAKE, None) == rl.RL_ERR_SHAPE
+    assert f(FAKE, 4, 1, 1e-4, 1, FAKE, None) == rl.RL_ERR_SHAPE   # G = 1 with ddof = 1
+    assert f(FAKE, 4, 4, 1e-4, 2, FAKE, None) == rl.RL_ERR_ARG
+    assert f(FAKE, 4, 4, float("nan"), 1, FAKE, None) == rl.RL_ERR_ARG
+    assert f(None, 4, 4, 1e-4, 1, FAKE, None) == rl.RL_ERR_NULL
+    assert f(None, 0, 4, 1e-4, 1, None, None) == rl.RL_OK         # nothing to do
+
+
+def test_gae_argument_errors(lib):
+    f = lib.rl_gae_reverse_scan
+    assert f(FAKE, FAKE, FAKE, -1, 4, 1.0, 0.95, FAKE, None, None) == rl.RL_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 4, -1, 1.0, 0.95, FAKE, None, None) == rl.RL_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 4, 4, float("nan"), 0.95, FAKE, None, None) == rl.RL_ERR_ARG
+    assert f(None, FAKE, FAKE, 4, 4, 1.0, 0.95, FAKE, None, None) == rl.RL_ERR_NULL
+    assert f(None, None, None, 0, 4, 1.0, 0.95, None, None, None) == rl.RL_OK
+
+
+def test_read_status_null(lib):
+    assert lib.rl_read_device_status(None, None) == rl.RL_ERR_NULL
+
+
+def test_binding_raises_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        saved = rl._lib
+        rl._lib = None
+        try:
+            rl.load(str(tmp_path / "missing.so"))
+        finally:
+            rl._lib = saved

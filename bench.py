@@ -127,6 +127,22 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Positions per second over all ranks: every rank runs its own replica."""
+    return world * rows_per_rank / (ms_per_step / 1e3)
+
+
 # ----------------------------------------------------------------------------- inputs
 def make_inputs(w, dev):
     """Device inputs of the workload.  logp_old / ref_logp are composed from the
@@ -178,6 +194,9 @@ def run_gpu(args):
     rl.build()
     rl.load()
     w = synth.WORKLOADS[WORKLOAD]
+    if args.seqs:  # a slice of the workload (profiling captures): same T, V and distributions
+        w = (w.scaled(n_prompts=max(1, args.seqs // w.group)) if args.seqs >= w.group
+             else w.scaled(n_prompts=1, group=max(2, args.seqs)))
     inp = make_inputs(w, dev)
     n_valid = int(inp["small"]["mask"].sum())
     stream = torch.cuda.current_stream(dev)
@@ -229,13 +248,9 @@ def run_gpu(args):
     clocks = sampler.stop()
     ms_total = t0.elapsed_time(t1)
     k_ms = [a.elapsed_time(b) for a, b in kev]
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
-    value = world * w.R / (ms_step / 1e3)
+    value = whole_job_rate(w.R, world, ms_step)
 
     # ---- roofline of the dominant kernel (rl_policy_loss_fwd_bwd)
     kern_ms = statistics.mean(k_ms)
@@ -255,6 +270,7 @@ def run_gpu(args):
         "config": {"workload": f"{WORKLOAD}: 4 prompts x group 8 = 32 seqs, T=1024, V=151936 bf16, "
                                "lengths U{256..1024}, eps=0.2 beta=0.04 c_ent=0",
                    "B": w.B, "T": w.T, "V": w.V, "rows": w.R, "valid_tokens": n_valid,
+                   "slice": (f"profiling slice: first {w.B} sequences" if args.seqs else None),
                    "valid_tokens_per_s": world * n_valid / (ms_step / 1e3),
                    "l2": "inputs (10 GB logits) far larger than the 129 MB L2; no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -446,6 +462,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="profiling only: keep the first SEQS sequences (whole groups)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -1,0 +1,83 @@
+"""Host-side logic of bench.py, including its multi-rank timing reduction run as
+two gloo ranks on the CPU (the GPU data path has no cross-rank step)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from ppo_policy_loss_gb300 import synth  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = bench.max_over_ranks(10.0 + rank * 2.5, "cpu")
+    q.put((rank, ms, bench.whole_job_rate(32768, world, ms)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [12.5, 12.5]
+    assert res[0][2] == pytest.approx(2 * 32768 / 0.0125)
+
+
+def test_single_process_identity():
+    assert bench.max_over_ranks(3.0, "cpu") == 3.0
+    assert bench.whole_job_rate(100, 1, 1000.0) == 100.0
+
+
+def test_alg_bytes_counts_one_read_of_valid_rows_and_one_write_of_all():
+    w = synth.WORKLOADS["qwen3_0p6b_grpo"]
+    n_valid = int(synth.small_inputs(w)["mask"].sum())
+    b = bench.alg_bytes(w, n_valid)
+    assert b == n_valid * w.V * 2 + w.R * w.V * 2 + w.R * 25 + w.B * 4
+    assert 15e9 < b < 17e9
+
+
+def test_sample_rows_spread_and_unique():
+    w = synth.WORKLOADS["qwen3_0p6b_grpo"]
+    r = bench.sample_rows(w, 512)
+    assert r.size == 512 and r[0] == 0 and r[-1] == w.R - 1 and np.all(np.diff(r) > 0)
+
+
+def test_reference_arm_non_zero_rank_exits_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "3", "--warmup", "3"], env=env, capture_output=True,
+                         text=True, timeout=120)
+    assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_traffic_record_ignored_when_kernel_changed(tmp_path, monkeypatch):
+    f = tmp_path / "t.txt"
+    f.write_text("kernel_sha: 0000\ndram_bytes_per_launch: 123\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic() is None
+    f.write_text(f"kernel_sha: {bench.kernel_sha()}\ndram_bytes_per_launch: 123\n")
+    assert bench.recorded_traffic() == 123.0

@@ -199,6 +199,43 @@ rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * rl_policy_loss_fwd_bwd without a caller-provided workspace, for callers
+ * that cannot allocate device memory: for example a plug-in inside a host
+ * framework that owns the GPU allocator and forbids raw cudaMalloc, or a
+ * program that hands all device memory to its own pool at start-up and has
+ * no allocation to spare on its update path.  The RL.cu pages have no
+ * counterpart to this entry point.
+ *
+ * Same arguments, meaning and results as rl_policy_loss_fwd_bwd, minus
+ * `workspace` and `workspace_bytes`.  The scratch is a file-scope device
+ * array of 131,328 bytes inside the library (the workspace of a persistent
+ * grid of up to 2048 CTAs, which covers every row count of the current
+ * kernel); every GPU that loads the library holds it until the process
+ * exits.  A call needing more scratch than that returns RL_ERR_WORKSPACE.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Each call clears the array's 256-byte status header with
+ *     cudaMemsetAsync on `stream` before launching.  The array keeps the
+ *     last call's contents otherwise.
+ *   - Every call shares the one array: calls that overlap on the GPU (two
+ *     streams, or two host threads) race and give wrong results; serialise
+ *     them.  rl_read_device_status does not apply; read device errors from
+ *     stats_dev->device_error.
+ *   - An argument rejected by rl_policy_loss_fwd_bwd's checks may be reported
+ *     after the header was cleared (only the library's own array is written).
+ */
+rl_status rl_policy_loss_fwd_bwd_noalloc(const void* logits, rl_dtype dtype,
+                                         long long B, long long T, long long V, long long ld,
+                                         const long long* ids, const float* logp_old,
+                                         const float* ref_logp, const unsigned char* mask,
+                                         const float* adv, rl_adv_layout adv_layout,
+                                         float eps, float beta, float c_ent, float grad_scale,
+                                         void* dlogits, float* logp_out, float* entropy_out,
+                                         rl_loss_stats* stats_dev, void* stream);
+
+/*
  * The launch shape rl_policy_loss_fwd_bwd would use on the current device for
  * this row shape: CTAs per cluster (one vocabulary slice each), clusters in
  * the persistent grid and dynamic shared memory per CTA.  Host-only query.

@@ -27,7 +27,8 @@ DTYPES = {"f32": RL_F32, "bf16": RL_BF16, "f16": RL_F16}
 
 __all__ = [
     "rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_workspace_size",
-    "rl_policy_loss_fwd_bwd", "rl_policy_loss_launch_shape", "rl_read_device_status",
+    "rl_policy_loss_fwd_bwd", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
+    "rl_read_device_status",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -67,13 +68,16 @@ def load(path: str | None = None):
     lib.rl_policy_loss_workspace_size.restype = SZ
     lib.rl_policy_loss_fwd_bwd.argtypes = [P, I, LL, LL, LL, LL, P, P, P, P, P, I, F, F, F, F,
                                            P, P, P, P, P, SZ, P]
+    lib.rl_policy_loss_fwd_bwd_noalloc.argtypes = [P, I, LL, LL, LL, LL, P, P, P, P, P, I, F, F,
+                                                   F, F, P, P, P, P, P]
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
     lib.rl_read_device_status.argtypes = [P, P]
     lib.rl_status_string.argtypes = [I]
     lib.rl_status_string.restype = ctypes.c_char_p
     for fn in ("rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_fwd_bwd",
-               "rl_policy_loss_launch_shape", "rl_read_device_status"):
+               "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
+               "rl_read_device_status"):
         getattr(lib, fn).restype = I
     _lib = lib
     return lib
@@ -133,6 +137,19 @@ def rl_policy_loss_fwd_bwd(logits, dtype, B, T, V, ld, ids, logp_old, ref_logp, 
         _ptr(mask), _ptr(adv), adv_layout, eps, beta, c_ent, grad_scale, _ptr(dlogits),
         _ptr(logp_out), _ptr(entropy_out), _ptr(stats_dev), _ptr(workspace), workspace_bytes,
         _stream(stream)), "rl_policy_loss_fwd_bwd")
+
+
+def rl_policy_loss_fwd_bwd_noalloc(logits, dtype, B, T, V, ld, ids, logp_old, ref_logp, mask,
+                                   adv, adv_layout, eps, beta, c_ent, grad_scale, dlogits,
+                                   logp_out, entropy_out, stats_dev, stream=None):
+    """rl_policy_loss_fwd_bwd with the library's own static scratch instead of a
+    caller workspace, for callers that cannot allocate device memory.  Calls
+    share that scratch: do not let two of them overlap on the GPU."""
+    _check(load().rl_policy_loss_fwd_bwd_noalloc(
+        _ptr(logits), _dtype(dtype), B, T, V, ld, _ptr(ids), _ptr(logp_old), _ptr(ref_logp),
+        _ptr(mask), _ptr(adv), adv_layout, eps, beta, c_ent, grad_scale, _ptr(dlogits),
+        _ptr(logp_out), _ptr(entropy_out), _ptr(stats_dev), _stream(stream)),
+        "rl_policy_loss_fwd_bwd_noalloc")
 
 
 def rl_policy_loss_launch_shape(dtype, V, n_rows):

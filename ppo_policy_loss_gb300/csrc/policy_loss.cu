@@ -634,6 +634,38 @@ bool finite(float x) { return std::isfinite(x); }
 
 using namespace rl;
 
+// ------------------------------------------------------------------ no-allocation variant
+// Scratch for rl_policy_loss_fwd_bwd_noalloc: the workspace a caller would
+// otherwise allocate (status header + one partial per CTA, kWorkspaceBytes =
+// 131,328 bytes), held in a file-scope device array instead.  Every GPU that
+// loads the library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_loss_scratch[kWorkspaceBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+std::map<int, void*> g_scratch_addr;  // device ordinal -> device address of g_loss_scratch
+
+// In host code g_loss_scratch names a host-side stand-in, not device memory:
+// the device address must come from cudaGetSymbolAddress, once per device,
+// with that device current.
+rl_status loss_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  auto found = g_scratch_addr.find(dev);
+  if (found != g_scratch_addr.end()) {
+    *out = found->second;
+    return RL_OK;
+  }
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_loss_scratch) != cudaSuccess || ptr == nullptr)
+    return RL_ERR_CUDA;
+  g_scratch_addr[dev] = ptr;
+  *out = ptr;
+  return RL_OK;
+}
+}  // namespace
+
 extern "C" size_t rl_policy_loss_workspace_size(long long n_rows) {
   (void)n_rows;
   return kWorkspaceBytes;
@@ -733,4 +765,25 @@ extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, 
     case RL_F16: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16>, args); break;
   }
   return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+extern "C" rl_status rl_policy_loss_fwd_bwd_noalloc(
+    const void* logits, rl_dtype dtype, long long B, long long T, long long V, long long ld,
+    const long long* ids, const float* logp_old, const float* ref_logp, const unsigned char* mask,
+    const float* adv, rl_adv_layout adv_layout, float eps, float beta, float c_ent,
+    float grad_scale, void* dlogits, float* logp_out, float* entropy_out,
+    rl_loss_stats* stats_dev, void* stream) {
+  if (B < 0 || T < 0) return RL_ERR_SHAPE;
+  if (B > 0 && T > (1LL << 40) / B) return RL_ERR_SHAPE;
+  if (rl_policy_loss_workspace_size(B * T) > sizeof(g_loss_scratch)) return RL_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const rl_status st = loss_scratch_address(&scratch);
+  if (st != RL_OK) return st;
+  // The status word and the last-CTA ticket must start at zero; the array
+  // keeps whatever the previous call left, so clear the header on the stream.
+  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return RL_ERR_CUDA;
+  return rl_policy_loss_fwd_bwd(logits, dtype, B, T, V, ld, ids, logp_old, ref_logp, mask, adv,
+                                adv_layout, eps, beta, c_ent, grad_scale, dlogits, logp_out,
+                                entropy_out, stats_dev, scratch, sizeof(g_loss_scratch), stream);
 }

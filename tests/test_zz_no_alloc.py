@@ -1,0 +1,74 @@
+"""rl_policy_loss_fwd_bwd_noalloc: the loss entry point for callers that cannot
+allocate device memory (a plug-in whose host framework owns the GPU allocator,
+or a program that hands all device memory to its own pool up front).  It uses
+the library's static scratch array instead of a caller workspace.
+
+Checked through the C ABI: two calls in a row must agree with the allocating
+entry point, within the tolerances of the parity tests.  This file is
+collected last so that a run stopping at the first failure has already run
+every other test; it also passes on its own in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import ppo_policy_loss_gb300 as rl
+from ppo_policy_loss_gb300 import STATS_BYTES, synth, torch_api
+from _parity import (LOGP_ATOL, assert_dlogits_close, assert_scalar_close, storage_np, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs():
+    w = synth.WORKLOADS["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=16,
+                                                  lengths=("uniform", 4, 16), c_ent=0.01)
+    small = synth.small_inputs(w)
+    logits = synth.logits(w, device="cuda")
+    rows = w.R
+    lo = to_dev((small["noise_old"] - 12.0).astype(np.float32))
+    rf = to_dev((small["noise_ref"] - 12.0).astype(np.float32))
+    adv = torch_api.group_advantages(to_dev(small["rewards"]), w.group)
+    return w, logits, to_dev(small["ids"]), to_dev(small["mask"]), adv, lo, rf, rows
+
+
+def _outputs(w, logits):
+    return (torch.empty_like(logits), torch.empty(w.R, device="cuda"),
+            torch.empty(w.R, device="cuda"), torch.zeros(STATS_BYTES, dtype=torch.uint8,
+                                                         device="cuda"))
+
+
+def test_noalloc_matches_allocating_entry_point_twice():
+    rl.build()
+    lib = rl.load()
+    w, logits, ids, mask, adv, lo, rf, R = _inputs()
+    stream = torch.cuda.current_stream().cuda_stream
+    common = (logits.data_ptr(), rl.RL_BF16, w.B, w.T, w.V, w.V, ids.data_ptr(), lo.data_ptr(),
+              rf.data_ptr(), mask.data_ptr(), adv.data_ptr(), rl.RL_ADV_PER_SEQ,
+              ctypes.c_float(w.eps), ctypes.c_float(w.beta), ctypes.c_float(w.c_ent),
+              ctypes.c_float(float(int(mask.sum()))))
+
+    # the allocating entry point, with a caller workspace
+    d_ref, lp_ref, h_ref, st_ref = _outputs(w, logits)
+    ws = torch.zeros(rl.rl_policy_loss_workspace_size(R), dtype=torch.uint8, device="cuda")
+    assert lib.rl_policy_loss_fwd_bwd(*common, d_ref.data_ptr(), lp_ref.data_ptr(),
+                                      h_ref.data_ptr(), st_ref.data_ptr(), ws.data_ptr(),
+                                      ws.numel(), stream) == rl.RL_OK
+    torch.cuda.synchronize()
+    ref = torch_api.read_stats(st_ref)
+    assert ref["device_error"] == 0 and ref["n_tokens"] > 0
+
+    for call in range(2):  # the second call finds the first call's contents in the scratch
+        d, lp, h, st = _outputs(w, logits)
+        assert lib.rl_policy_loss_fwd_bwd_noalloc(*common, d.data_ptr(), lp.data_ptr(),
+                                                  h.data_ptr(), st.data_ptr(), stream) == rl.RL_OK
+        torch.cuda.synchronize()
+        got = torch_api.read_stats(st)
+        assert got["device_error"] == 0, (call, got)
+        assert got["n_tokens"] == ref["n_tokens"] and got["n_clipped"] == ref["n_clipped"]
+        for k in ("loss", "pg_term", "kl_term", "ent_term"):
+            assert_scalar_close(k, got[k], ref[k])
+        assert float((lp - lp_ref).abs().max()) <= LOGP_ATOL
+        assert float((h - h_ref).abs().max()) <= LOGP_ATOL
+        assert_dlogits_close(storage_np(d), storage_np(d_ref), "bf16", where=f"noalloc call {call}")

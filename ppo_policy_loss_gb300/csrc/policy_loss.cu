@@ -42,10 +42,30 @@
 namespace rl {
 namespace {
 
+// Tuning knobs (compile-time; the defaults are the shipped configuration).
+#ifndef RL_CONSUMER_WARPS
+#define RL_CONSUMER_WARPS 16
+#endif
+#ifndef RL_RING_SLOTS
+#define RL_RING_SLOTS 13
+#endif
+#ifndef RL_LOOKAHEAD_CHUNKS
+#define RL_LOOKAHEAD_CHUNKS 3
+#endif
+#ifndef RL_MIN_CTAS_PER_SM
+#define RL_MIN_CTAS_PER_SM 1
+#endif
+#ifndef RL_SLICES_IN_RING
+#define RL_SLICES_IN_RING 1
+#endif
+#ifndef RL_MIN_CLUSTER
+#define RL_MIN_CLUSTER 1
+#endif
+
 constexpr int kChunkBytes = 16384;
-constexpr int kSlots = 13;
-constexpr int kLookaheadChunks = 3;
-constexpr int kConsumerWarps = 16;
+constexpr int kSlots = RL_RING_SLOTS;
+constexpr int kLookaheadChunks = RL_LOOKAHEAD_CHUNKS;
+constexpr int kConsumerWarps = RL_CONSUMER_WARPS;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kMaxCluster = 8;
@@ -89,12 +109,28 @@ struct LossArgs {
 };
 
 // ------------------------------------------------------------------ element formats
+// Each format reads 16-byte vectors from shared memory.  clamp() floors every
+// element at a large negative finite value (keeping NaN), so that a -inf
+// logit contributes exp = 0 and 0 * x = 0 instead of 0 * inf = NaN; vmax() is
+// the NaN-propagating maximum of a full vector; unpack() widens to fp32.
+constexpr float kFloor = -1.0e30f;
+
 template <int DT>
 struct Elem;
 
 template <>
 struct Elem<RL_F32> {
   static constexpr int kBytes = 4, kVec = 4;
+  __device__ static void clamp(uint4& w) {
+    w.x = __float_as_uint(max_nan(__uint_as_float(w.x), kFloor));
+    w.y = __float_as_uint(max_nan(__uint_as_float(w.y), kFloor));
+    w.z = __float_as_uint(max_nan(__uint_as_float(w.z), kFloor));
+    w.w = __float_as_uint(max_nan(__uint_as_float(w.w), kFloor));
+  }
+  __device__ static float vmax(const uint4& w) {
+    return max_nan(max_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                   max_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+  }
   __device__ static void unpack(const uint4& w, float (&z)[kVec]) {
     z[0] = __uint_as_float(w.x);
     z[1] = __uint_as_float(w.y);
@@ -108,9 +144,32 @@ struct Elem<RL_F32> {
   __device__ static void store1(unsigned char* p, float v) { *reinterpret_cast<float*>(p) = v; }
 };
 
+// Packed two-element NaN-propagating max of bf16 / fp16 pairs.
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t max_nan_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 template <>
 struct Elem<RL_BF16> {
   static constexpr int kBytes = 2, kVec = 8;
+  static constexpr uint32_t kFloor2 = 0xF149F149u;  // (-9.98e29, -9.98e29) in bf16
+  __device__ static void clamp(uint4& w) {
+    w.x = max_nan_bf16x2(w.x, kFloor2);
+    w.y = max_nan_bf16x2(w.y, kFloor2);
+    w.z = max_nan_bf16x2(w.z, kFloor2);
+    w.w = max_nan_bf16x2(w.w, kFloor2);
+  }
+  __device__ static float vmax(const uint4& w) {
+    const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(w.x, w.y), max_nan_bf16x2(w.z, w.w));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
   __device__ static void unpack(const uint4& w, float (&z)[kVec]) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -136,6 +195,18 @@ struct Elem<RL_BF16> {
 template <>
 struct Elem<RL_F16> {
   static constexpr int kBytes = 2, kVec = 8;
+  static constexpr uint32_t kFloor2 = 0xFBFFFBFFu;  // (-65504, -65504) in fp16
+  __device__ static void clamp(uint4& w) {
+    w.x = max_nan_f16x2(w.x, kFloor2);
+    w.y = max_nan_f16x2(w.y, kFloor2);
+    w.z = max_nan_f16x2(w.z, kFloor2);
+    w.w = max_nan_f16x2(w.w, kFloor2);
+  }
+  __device__ static float vmax(const uint4& w) {
+    const uint32_t m = max_nan_f16x2(max_nan_f16x2(w.x, w.y), max_nan_f16x2(w.z, w.w));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&m));
+    return max_nan(f.x, f.y);
+  }
   __device__ static void unpack(const uint4& w, float (&z)[kVec]) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -162,7 +233,8 @@ struct Elem<RL_F16> {
 // ------------------------------------------------------------------ online statistics
 // A partial (m, s, t) over a set of logits z: m = max z, s = sum 2^x,
 // t = sum 2^x * x with x = (z - m) * log2(e).  Then for the full row
-// lse = m + ln s and H = ln 2 * (log2 s - t / s).
+// lse = m + ln s and H = ln 2 * (log2 s - t / s).  Threads keep s and t as
+// two-lane sums (packed fp32x2 arithmetic, two independent chains).
 __device__ __forceinline__ void merge_stats(float& m, float& s, float& t, float m2, float s2,
                                             float t2) {
   if (m2 > m) {
@@ -177,35 +249,85 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, float& t, float 
   t = fmaf(f, t2 - d * s2, t);
 }
 
-template <int NV>
-__device__ __forceinline__ void accumulate(const float (&z)[NV], int nv, float& m, float& s,
-                                           float& t) {
-  float vm = z[0];
-#pragma unroll
-  for (int i = 1; i < NV; ++i)
-    if (i < nv) vm = max_nan(vm, z[i]);
+// Raise the running max to vm, rescaling the two-lane sums.  Returns false
+// while nothing finite has been seen (then only a NaN is remembered).
+__device__ __forceinline__ bool raise_max(float vm, float& m, float2& s, float2& t) {
   if (vm > m) {
     if (m != -INFINITY) {
       const float d = (vm - m) * kLog2e;
       const float f = ex2_approx(-d);
-      t = f * fmaf(-d, s, t);
-      s = f * s;
+      const float2 f2 = make_float2(f, f);
+      t = __fmul2_rn(f2, __ffma2_rn(make_float2(-d, -d), s, t));
+      s = __fmul2_rn(f2, s);
     }
     m = vm;
   }
-  if (m == -INFINITY) {  // nothing finite yet: only a NaN must be remembered
-    if (vm != vm) s = vm;
-    return;
+  if (m == -INFINITY) {
+    if (vm != vm) s.x = vm;
+    return false;
   }
+  return true;
+}
+
+// Pass-1 update with one full 16-byte vector.
+template <class E>
+__device__ __forceinline__ void accumulate_full(uint4 w, float& m, float2& s, float2& t) {
+  E::clamp(w);
+  if (!raise_max(E::vmax(w), m, s, t)) return;
+  float z[E::kVec];
+  E::unpack(w, z);
+  const float2 L2 = make_float2(kLog2e, kLog2e);
+  const float2 nmL = make_float2(-m * kLog2e, -m * kLog2e);
+#pragma unroll
+  for (int i = 0; i < E::kVec; i += 2) {
+    const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, nmL);
+    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    s = __fadd2_rn(s, e);
+    t = __ffma2_rn(e, x, t);
+  }
+}
+
+// Pass-1 update with the first nv (< kVec) elements of a vector (row tail).
+template <class E>
+__device__ __forceinline__ void accumulate_tail(uint4 w, int nv, float& m, float2& s, float2& t) {
+  E::clamp(w);
+  float z[E::kVec];
+  E::unpack(w, z);
+  float vm = z[0];
+#pragma unroll
+  for (int i = 1; i < E::kVec; ++i)
+    if (i < nv) vm = max_nan(vm, z[i]);
+  if (!raise_max(vm, m, s, t)) return;
   const float mL = m * kLog2e;
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
+  for (int i = 0; i < E::kVec; ++i) {
     if (i < nv) {
-      const float x = max_nan(fmaf(z[i], kLog2e, -mL), -250.f);
+      const float x = fmaf(z[i], kLog2e, -mL);
       const float e = ex2_approx(x);
-      s += e;
-      t = fmaf(e, x, t);
+      s.x += e;
+      t.x = fmaf(e, x, t.x);
     }
+  }
+}
+
+// Pass-2 gradient of one vector: d_v = 2^x (a0 + a1 x), x = z log2(e) - cL.
+// Without the entropy term (a1 = 0) no clamp is needed: a -inf logit gives
+// 2^x = 0 and 0 * a0 = 0.
+template <class E, bool kEntropy>
+__device__ __forceinline__ void grad_vec(uint4 w, float cL, float a0, float a1, float (&d)[E::kVec]) {
+  if (kEntropy) E::clamp(w);
+  float z[E::kVec];
+  E::unpack(w, z);
+  const float2 L2 = make_float2(kLog2e, kLog2e);
+  const float2 ncL = make_float2(-cL, -cL);
+  const float2 A0 = make_float2(a0, a0);
+#pragma unroll
+  for (int i = 0; i < E::kVec; i += 2) {
+    const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, ncL);
+    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    const float2 r = kEntropy ? __fmul2_rn(p, __ffma2_rn(make_float2(a1, a1), x, A0)) : __fmul2_rn(p, A0);
+    d[i] = r.x;
+    d[i + 1] = r.y;
   }
 }
 
@@ -226,9 +348,31 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Per-row scalars, loaded one row ahead of their use.
+struct RowScalars {
+  long long y;
+  float A, lpo, rf;
+  bool valid;
+};
+
+__device__ __forceinline__ RowScalars load_row(const LossArgs& a, long long row) {
+  RowScalars r;
+  r.valid = false;
+  r.y = 0;
+  r.A = r.lpo = r.rf = 0.f;
+  if (row < a.R) {
+    r.valid = a.mask[row] != 0;
+    r.y = a.ids[row];
+    r.A = a.adv[a.adv_per_token ? row : row / a.T];
+    r.lpo = a.logp_old ? a.logp_old[row] : 0.f;
+    r.rf = a.ref_logp ? a.ref_logp[row] : 0.f;
+  }
+  return r;
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs a) {
+__global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kernel(const LossArgs a) {
   using E = Elem<DT>;
   constexpr int kVec = E::kVec;
   constexpr int kChunkElems = kChunkBytes / E::kBytes;
@@ -268,8 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
       bool stop = false;
+      bool valid_next = cid < a.R ? a.mask[cid] != 0 : false;
       for (long long row = cid; row < a.R && !stop; row += ncl) {
-        if (!a.mask[row] || nchunks == 0) continue;
+        const bool valid = valid_next;
+        valid_next = row + ncl < a.R ? a.mask[row + ncl] != 0 : false;  // one row ahead
+        if (!valid || nchunks == 0) continue;
         const unsigned char* src = a.logits + row * a.row_bytes + lo * E::kBytes;
         for (int c = 0; c < nchunks; ++c, ++it) {
           const uint32_t slot = it % kSlots, round = it / kSlots;
@@ -297,6 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
     }
   } else {
     // ---------------------------------------------------------------- consumers
+    RowScalars cur = load_row(a, cid);  // in flight while the mask is counted
+
     // N = number of valid tokens; every CTA counts the whole mask.
     long long cnt = 0;
     {
@@ -321,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
     }
     const long long N = cnt;
     const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
+    const bool with_entropy = a.c_ent != 0.f;
 
     double acc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // J, pg, kl, H, clipped (rank 0, thread 0)
     unsigned int err = 0;
@@ -328,9 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
     bool aborted = false;
 
     for (long long row = cid; row < a.R; row += ncl) {
-      const bool valid = a.mask[row] != 0;  // the same for every CTA of the cluster
+      const RowScalars rs = cur;
+      cur = load_row(a, row + ncl);  // next row's scalars, in flight during this row
       unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes + lo * E::kBytes : nullptr;
-      if (!valid) {
+      if (!rs.valid) {
         if (drow) zero_slice<E>(drow, nelem, tid);
         if (rank == 0 && tid == 0) {
           if (a.logp_out) a.logp_out[row] = 0.f;
@@ -338,14 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
         }
         continue;
       }
-      const long long y = a.ids[row];
-      const float A = a.adv[a.adv_per_token ? row : row / a.T];
-      const float lpo = a.logp_old ? a.logp_old[row] : 0.f;
-      const float rf = a.ref_logp ? a.ref_logp[row] : 0.f;
+      const long long y = rs.y;
       const bool y_here = (y >= lo) && (y < hi);
 
       // ---- pass 1: online statistics of this thread's share of the slice
-      float m = -INFINITY, s = 0.f, t = 0.f;
+      float m = -INFINITY;
+      float2 s2 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
       for (int c = 0; c < nchunks; ++c) {
         const uint32_t k = it + c, slot = k % kSlots;
         wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
@@ -356,24 +505,28 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
           const int j = tid + q * kConsumerThreads;
           const long long e0 = c0 + static_cast<long long>(j) * kVec;
           if (e0 < hi) {
-            float z[kVec];
-            E::unpack(ld_shared_v4(buf + j * 16), z);
-            const int nv = (hi - e0 >= kVec) ? kVec : static_cast<int>(hi - e0);
+            const uint4 w = ld_shared_v4(buf + j * 16);
             if (y_here && static_cast<unsigned long long>(y - e0) < static_cast<unsigned long long>(kVec)) {
+              float z[kVec];
+              E::unpack(w, z);
 #pragma unroll
               for (int i = 0; i < kVec; ++i)
                 if (i == y - e0) sm.zy = z[i];
             }
-            accumulate<kVec>(z, nv, m, s, t);
+            if (hi - e0 >= kVec)
+              accumulate_full<E>(w, m, s2, t2);
+            else
+              accumulate_tail<E>(w, static_cast<int>(hi - e0), m, s2, t2);
           }
         }
       }
+      float s = s2.x + s2.y, t = t2.x + t2.y;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
-        merge_stats(m, s, t, m2, s2, t2);
+        const float sx = __shfl_xor_sync(0xffffffffu, s, o);
+        const float tx = __shfl_xor_sync(0xffffffffu, t, o);
+        merge_stats(m, s, t, m2, sx, tx);
       }
       if (lane == 0) sm.wpart[warp] = make_float4(m, s, t, 0.f);
       if (named_barrier_or(kConsumerBarrier, kConsumerThreads, *abort_flag != 0)) {
@@ -408,14 +561,15 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
       const float logp = zy - lse;
 
       // ---- per-token objective and its derivative with respect to logp
-      const float r = a.logp_old ? expf(logp - lpo) : 1.f;
+      const float A = rs.A;
+      const float r = a.logp_old ? expf(logp - rs.lpo) : 1.f;
       const float rA = r * A;
       const float pg = fminf(rA, fminf(fmaxf(r, 1.f - a.eps), 1.f + a.eps) * A);
       const bool clipped = (A > 0.f && r > 1.f + a.eps) || (A < 0.f && r < 1.f - a.eps);
       const float dpg = clipped ? 0.f : rA;
       float kl = 0.f, dkl = 0.f;
       if (a.ref_logp) {
-        const float d = rf - logp;
+        const float d = rs.rf - logp;
         dkl = expm1f(d);
         kl = dkl - d;
       }
@@ -452,13 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1) policy_loss_kernel(const LossArgs
             const int j = tid + q * kConsumerThreads;
             const long long e0 = c0 + static_cast<long long>(j) * kVec;
             if (e0 < hi) {
-              float z[kVec], d[kVec];
-              E::unpack(ld_shared_v4(buf + j * 16), z);
-#pragma unroll
-              for (int i = 0; i < kVec; ++i) {
-                const float x = max_nan(fmaf(z[i], kLog2e, -cL), -250.f);
-                d[i] = ex2_approx(x) * fmaf(a1, x, a0);
-              }
+              float d[kVec];
+              const uint4 w = ld_shared_v4(buf + j * 16);
+              if (with_entropy)
+                grad_vec<E, true>(w, cL, a0, a1, d);
+              else
+                grad_vec<E, false>(w, cL, a0, a1, d);
               if (y_here && static_cast<unsigned long long>(y - e0) < static_cast<unsigned long long>(kVec)) {
 #pragma unroll
                 for (int i = 0; i < kVec; ++i)
@@ -544,12 +697,13 @@ int elem_bytes(rl_dtype dt) {
 int choose_cluster(int es, long long V, long long* slice_out) {
   const long long align = 16 / es;
   for (int pass = 0; pass < 2; ++pass) {
-    const long long budget = pass == 0 ? kSlots - kLookaheadChunks : kSlots;
-    for (int c = 1; c <= kMaxCluster; ++c) {
+    for (int c = RL_MIN_CLUSTER; c <= kMaxCluster; ++c) {
       long long s = (V + c - 1) / c;
       s = (s + align - 1) / align * align;
       const long long chunks = (s * es + kChunkBytes - 1) / kChunkBytes;
-      if (chunks <= budget) {
+      const bool fits = pass == 0 ? chunks * RL_SLICES_IN_RING + kLookaheadChunks <= kSlots
+                                  : chunks <= kSlots;
+      if (fits) {
         *slice_out = s;
         return c;
       }

@@ -295,49 +295,89 @@ def run_gpu(args):
 
 
 def run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, ws, ld):
-    """Same step through the public C-ABI calls, with every input copied from
-    pinned host memory and the gradient and statistics copied back, inside the
-    timed region."""
+    """The same step through the public C-ABI calls with HOST buffers: every
+    step copies all its inputs from pinned host memory to the device and the
+    gradient and statistics back, inside the timed region.  Steps are
+    pipelined like a training loop that prefetches its next batch: two device
+    buffer sets, one stream per direction, so the upload of step i+1 runs
+    beside the download of step i (the link is full duplex) while events keep
+    every buffer from being reused before its last reader is done."""
     import torch
 
     import ppo_policy_loss_gb300 as rl
     from ppo_policy_loss_gb300 import STATS_BYTES
 
     steps = max(1, min(args.steps, args.e2e_steps))
+    keys = ("logits", "ids", "mask", "rewards", "logp_old", "ref")
     h = {}
-    for k in ("logits", "ids", "mask", "rewards", "logp_old", "ref"):
+    for k in keys:
         h[k] = torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
         h[k].copy_(inp[k])
     h_dlogits = torch.empty(dlogits.shape, dtype=dlogits.dtype, pin_memory=True)
     h_stats = torch.empty(STATS_BYTES, dtype=torch.uint8, pin_memory=True)
-    d = {k: torch.empty_like(inp[k]) for k in h}
+    sets = [dict(d={k: torch.empty_like(inp[k]) for k in keys}, dlogits=dlogits, stats=stats,
+                 ws=ws, adv=adv, logp=logp_out, ent=ent_out)]
+    sets.append(dict(d={k: torch.empty_like(inp[k]) for k in keys},
+                     dlogits=torch.empty_like(dlogits),
+                     stats=torch.zeros_like(stats), ws=torch.zeros_like(ws),
+                     adv=torch.empty_like(adv), logp=torch.empty_like(logp_out),
+                     ent=torch.empty_like(ent_out)))
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = h_dlogits.numel() * h_dlogits.element_size() + STATS_BYTES
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_cmp = stream
+    ev = lambda: torch.cuda.Event()
+    comp_done = [ev(), ev()]   # compute of the last step on set b finished
+    out_done = [ev(), ev()]    # download of the last step on set b finished
+    for e in comp_done + out_done:
+        e.record(s_cmp)
 
-    def one():
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
-        rl.rl_group_advantages(d["rewards"], w.B // w.group, w.group, 1e-4, 1, adv, stream)
-        rl.rl_policy_loss_fwd_bwd(d["logits"], "bf16", w.B, w.T, w.V, ld, d["ids"], d["logp_old"],
-                                  d["ref"], d["mask"], adv, rl.RL_ADV_PER_SEQ, w.eps, w.beta,
-                                  w.c_ent, 1.0, dlogits, logp_out, ent_out, stats, ws, ws.numel(),
-                                  stream)
-        h_dlogits.copy_(dlogits, non_blocking=True)
-        h_stats.copy_(stats, non_blocking=True)
+    def one(i):
+        b = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[i % 2])          # set b's inputs no longer read
+            for k in keys:
+                b["d"][k].copy_(h[k], non_blocking=True)
+            in_done = ev()
+            in_done.record(s_in)
+        s_cmp.wait_event(in_done)
+        s_cmp.wait_event(out_done[i % 2])              # set b's gradient already downloaded
+        rl.rl_group_advantages(b["d"]["rewards"], w.B // w.group, w.group, 1e-4, 1, b["adv"], s_cmp)
+        rl.rl_policy_loss_fwd_bwd(b["d"]["logits"], "bf16", w.B, w.T, w.V, ld, b["d"]["ids"],
+                                  b["d"]["logp_old"], b["d"]["ref"], b["d"]["mask"], b["adv"],
+                                  rl.RL_ADV_PER_SEQ, w.eps, w.beta, w.c_ent, 1.0, b["dlogits"],
+                                  b["logp"], b["ent"], b["stats"], b["ws"], b["ws"].numel(), s_cmp)
+        comp_done[i % 2].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[i % 2])
+            h_dlogits.copy_(b["dlogits"], non_blocking=True)
+            h_stats.copy_(b["stats"], non_blocking=True)
+            out_done[i % 2].record(s_out)
 
-    one()
+    one(0)
+    one(1)
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        one()
-    t1.record(stream)
+    t0.record(s_cmp)
+    s_in.wait_event(t0)
+    for i in range(steps):
+        one(i)
+    s_cmp.wait_stream(s_out)
+    t1.record(s_cmp)
     torch.cuda.synchronize(dev)
     ms = t0.elapsed_time(t1) / steps
     world = dist_env()[0]
-    del d, h, h_dlogits
+    st = torch_api_read(h_stats)
+    del sets, h, h_dlogits
     return {"value": world * w.R / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "pipeline": "double-buffered: upload of step i+1 beside download of step i",
+            "loss_last_step": st["loss"]}
+
+
+def torch_api_read(h_stats):
+    from ppo_policy_loss_gb300 import stats_from_bytes
+    return stats_from_bytes(h_stats.numpy().tobytes())
 
 
 # ----------------------------------------------------------------------------- CPU oracle

@@ -7,20 +7,29 @@
 // paragraph after its benchmark table, in one launch to avoid global-memory
 // round trips.  This kernel is that step for GB300, designed around HBM:
 //
-//   * Persistent grid of thread-block clusters; cluster q takes rows
-//     q, q + Q, q + 2Q, ...  Each of the C CTAs of a cluster owns one slice of
-//     the vocabulary, so that a whole row sits in the cluster's shared memory
-//     (C = 2 for a 151936-wide bf16 row): logits are read from HBM once and
-//     the gradient is written once.
-//   * One producer warp streams slices with 1-D bulk copies (cp.async.bulk,
-//     L2 evict-first) into a ring of 16 KB chunks guarded by mbarriers, and
-//     runs ahead into the next rows while the consumers work.
-//   * Sixteen consumer warps: pass 1 computes per-thread online (max, sum of
-//     exp, sum of exp * x) statistics from shared memory; warp shuffles and a
-//     named barrier combine them per CTA; the CTAs of the cluster exchange
-//     their partials through distributed shared memory with remote mbarrier
-//     arrives; pass 2 re-reads the chunks from shared memory, writes the
-//     gradient with 16-byte streaming stores and frees each chunk.
+//   * Persistent grid, one CTA per SM; CTA q takes rows q, q + Q, ...
+//   * One producer warp streams the valid rows with 1-D bulk copies
+//     (cp.async.bulk) into a ring of 13 x 16 KB shared-memory chunks guarded
+//     by full/empty mbarriers.  It runs ahead of the consumers by up to the
+//     whole ring.
+//   * Two row modes:
+//       - resident: a row that fits the ring twice over (at most 6 chunks,
+//         e.g. 32000 fp16 logits) is loaded once and kept in shared memory
+//         for both passes;
+//       - streaming: a longer row (151936 bf16 logits = 19 chunks) is streamed
+//         twice: the first load keeps its L2 lines (evict-last), the second
+//         pass re-reads them from L2 (evict-first).  Logits still cross the
+//         HBM bus once, and the ring is always free to prefetch.
+//     A cluster layout (each CTA of a 2..8-CTA cluster holding one slice of a
+//     resident row, statistics exchanged through distributed shared memory)
+//     is kept for comparison builds; it costs a cluster-wide exchange per row
+//     and loses to streaming on GB300.
+//   * Sixteen consumer warps.  Pass 1: per-thread online (max, sum 2^x,
+//     sum 2^x * x) in packed fp32x2 with independent accumulator chains.
+//     Each warp shuffle-merges its lanes and publishes one partial; the
+//     partials meet through one mbarrier (no CTA-wide barrier per row), and
+//     every warp merges them with shuffles.  Pass 2: the gradient, written
+//     with 16-byte streaming stores.
 //   * Masked rows: all-zero gradient stores only, their logits are not read.
 //   * N (valid tokens) is counted by every CTA at start (R bytes from L2);
 //     the loss is reduced in fp64: per-CTA partials in a fixed row order,
@@ -49,22 +58,21 @@ namespace {
 #ifndef RL_RING_SLOTS
 #define RL_RING_SLOTS 13
 #endif
-#ifndef RL_LOOKAHEAD_CHUNKS
-#define RL_LOOKAHEAD_CHUNKS 3
-#endif
 #ifndef RL_MIN_CTAS_PER_SM
 #define RL_MIN_CTAS_PER_SM 1
 #endif
-#ifndef RL_SLICES_IN_RING
-#define RL_SLICES_IN_RING 1
+// 0: rows that do not fit the ring twice are streamed (re-read from L2);
+// 1: such rows are split across a cluster and held on chip (comparison).
+#ifndef RL_CLUSTER_RESIDENT
+#define RL_CLUSTER_RESIDENT 0
 #endif
-#ifndef RL_MIN_CLUSTER
-#define RL_MIN_CLUSTER 1
+// L2 policy of the first load of a streamed row: 1 evict-last, 0 normal.
+#ifndef RL_STREAM_KEEP_L2
+#define RL_STREAM_KEEP_L2 1
 #endif
 
 constexpr int kChunkBytes = 16384;
 constexpr int kSlots = RL_RING_SLOTS;
-constexpr int kLookaheadChunks = RL_LOOKAHEAD_CHUNKS;
 constexpr int kConsumerWarps = RL_CONSUMER_WARPS;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
@@ -72,6 +80,8 @@ constexpr int kMaxCluster = 8;
 constexpr int kVecsPerChunk = kChunkBytes / 16;
 constexpr int kVecsPerThread = kVecsPerChunk / kConsumerThreads;
 static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly over consumers");
+static_assert(kConsumerWarps * kMaxCluster <= 128, "partials of one row fit 4 per lane");
+constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kConsumerBarrier = 1;  // named barrier id (0 is __syncthreads)
 
 struct LossSmem {
@@ -79,11 +89,9 @@ struct LossSmem {
   unsigned long long full[kSlots];
   unsigned long long empty[kSlots];
   unsigned long long xbar[2];
-  float4 xpart[2][kMaxCluster];
-  float4 wpart[kConsumerWarps];
+  float4 xpart[2][kMaxCluster * kConsumerWarps];  // (m, s, t, z_y or -inf) per warp
   long long wcount[kConsumerWarps];
   double wred[kConsumerWarps][5];
-  float zy;
   int abort;
   int is_last;
 };
@@ -103,7 +111,7 @@ struct LossArgs {
   WsPartial* partials;
   long long R, T, V;
   long long row_bytes;  // ld * element bytes
-  long long slice;      // vocabulary elements per cluster rank
+  long long slice;      // vocabulary elements per cluster rank (V when not clustered)
   int adv_per_token;
   float eps, beta, c_ent, grad_scale;
 };
@@ -233,8 +241,8 @@ struct Elem<RL_F16> {
 // ------------------------------------------------------------------ online statistics
 // A partial (m, s, t) over a set of logits z: m = max z, s = sum 2^x,
 // t = sum 2^x * x with x = (z - m) * log2(e).  Then for the full row
-// lse = m + ln s and H = ln 2 * (log2 s - t / s).  Threads keep s and t as
-// two-lane sums (packed fp32x2 arithmetic, two independent chains).
+// lse = m + ln s and H = ln 2 * (log2 s - t / s).  Each thread keeps one
+// two-lane (s, t) pair per vector position of a chunk: independent chains.
 __device__ __forceinline__ void merge_stats(float& m, float& s, float& t, float m2, float s2,
                                             float t2) {
   if (m2 > m) {
@@ -249,35 +257,51 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, float& t, float 
   t = fmaf(f, t2 - d * s2, t);
 }
 
-// Raise the running max to vm, rescaling the two-lane sums.  Returns false
-// while nothing finite has been seen (then only a NaN is remembered).
-__device__ __forceinline__ bool raise_max(float vm, float& m, float2& s, float2& t) {
-  if (vm > m) {
-    if (m != -INFINITY) {
-      const float d = (vm - m) * kLog2e;
+struct ThreadStats {
+  float m;
+  float2 s[kVecsPerThread];
+  float2 t[kVecsPerThread];
+};
+
+__device__ __forceinline__ void stats_init(ThreadStats& a) {
+  a.m = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kVecsPerThread; ++q) a.s[q] = a.t[q] = make_float2(0.f, 0.f);
+}
+
+// Raise the running max to vm, rescaling every chain.  Returns false while
+// nothing finite has been seen (then only a NaN is remembered).
+__device__ __forceinline__ bool raise_max(float vm, ThreadStats& a) {
+  if (vm > a.m) {
+    if (a.m != -INFINITY) {
+      const float d = (vm - a.m) * kLog2e;
       const float f = ex2_approx(-d);
-      const float2 f2 = make_float2(f, f);
-      t = __fmul2_rn(f2, __ffma2_rn(make_float2(-d, -d), s, t));
-      s = __fmul2_rn(f2, s);
+      const float2 f2 = make_float2(f, f), nd2 = make_float2(-d, -d);
+#pragma unroll
+      for (int q = 0; q < kVecsPerThread; ++q) {
+        a.t[q] = __fmul2_rn(f2, __ffma2_rn(nd2, a.s[q], a.t[q]));
+        a.s[q] = __fmul2_rn(f2, a.s[q]);
+      }
     }
-    m = vm;
+    a.m = vm;
   }
-  if (m == -INFINITY) {
-    if (vm != vm) s.x = vm;
+  if (a.m == -INFINITY) {
+    if (vm != vm) a.s[0].x = vm;
     return false;
   }
   return true;
 }
 
-// Pass-1 update with one full 16-byte vector.
+// Pass-1 update with one full 16-byte vector into chain q.
 template <class E>
-__device__ __forceinline__ void accumulate_full(uint4 w, float& m, float2& s, float2& t) {
+__device__ __forceinline__ void accumulate_full(uint4 w, ThreadStats& a, int q) {
   E::clamp(w);
-  if (!raise_max(E::vmax(w), m, s, t)) return;
+  if (!raise_max(E::vmax(w), a)) return;
   float z[E::kVec];
   E::unpack(w, z);
   const float2 L2 = make_float2(kLog2e, kLog2e);
-  const float2 nmL = make_float2(-m * kLog2e, -m * kLog2e);
+  const float2 nmL = make_float2(-a.m * kLog2e, -a.m * kLog2e);
+  float2 s = a.s[q], t = a.t[q];
 #pragma unroll
   for (int i = 0; i < E::kVec; i += 2) {
     const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, nmL);
@@ -285,11 +309,13 @@ __device__ __forceinline__ void accumulate_full(uint4 w, float& m, float2& s, fl
     s = __fadd2_rn(s, e);
     t = __ffma2_rn(e, x, t);
   }
+  a.s[q] = s;
+  a.t[q] = t;
 }
 
 // Pass-1 update with the first nv (< kVec) elements of a vector (row tail).
 template <class E>
-__device__ __forceinline__ void accumulate_tail(uint4 w, int nv, float& m, float2& s, float2& t) {
+__device__ __forceinline__ void accumulate_tail(uint4 w, int nv, ThreadStats& a, int q) {
   E::clamp(w);
   float z[E::kVec];
   E::unpack(w, z);
@@ -297,15 +323,15 @@ __device__ __forceinline__ void accumulate_tail(uint4 w, int nv, float& m, float
 #pragma unroll
   for (int i = 1; i < E::kVec; ++i)
     if (i < nv) vm = max_nan(vm, z[i]);
-  if (!raise_max(vm, m, s, t)) return;
-  const float mL = m * kLog2e;
+  if (!raise_max(vm, a)) return;
+  const float mL = a.m * kLog2e;
 #pragma unroll
   for (int i = 0; i < E::kVec; ++i) {
     if (i < nv) {
       const float x = fmaf(z[i], kLog2e, -mL);
       const float e = ex2_approx(x);
-      s.x += e;
-      t.x = fmaf(e, x, t.x);
+      a.s[q].x += e;
+      a.t[q].x = fmaf(e, x, a.t[q].x);
     }
   }
 }
@@ -348,6 +374,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Per-row scalars, loaded one row ahead of their use.
 struct RowScalars {
   long long y;
@@ -371,7 +408,9 @@ __device__ __forceinline__ RowScalars load_row(const LossArgs& a, long long row)
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int DT>
+// kStream: rows are streamed twice through the ring (second pass from L2);
+// otherwise each CTA's slice of a row stays in the ring for both passes.
+template <int DT, bool kStream>
 __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kernel(const LossArgs a) {
   using E = Elem<DT>;
   constexpr int kVec = E::kVec;
@@ -385,14 +424,15 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank(), csize = cluster_size();
   const uint32_t cid = cluster_id(), ncl = cluster_count();
+  const int n_parts = static_cast<int>(csize) * kConsumerWarps;  // partials per row
 
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_addr(&sm.full[s]), 1);
       mbar_init(smem_addr(&sm.empty[s]), kConsumerWarps);
     }
-    mbar_init(smem_addr(&sm.xbar[0]), csize);
-    mbar_init(smem_addr(&sm.xbar[1]), csize);
+    mbar_init(smem_addr(&sm.xbar[0]), n_parts);
+    mbar_init(smem_addr(&sm.xbar[1]), n_parts);
     sm.abort = 0;
     sm.is_last = 0;
     fence_mbar_init();
@@ -402,14 +442,15 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
 
   const long long lo = static_cast<long long>(rank) * a.slice;
   const long long hi = min(a.V, lo + a.slice);
-  const long long nelem = hi > lo ? hi - lo : 0;
-  const long long slice_bytes = (nelem * E::kBytes + 15) & ~15LL;
+  const int nelem = hi > lo ? static_cast<int>(hi - lo) : 0;
+  const long long slice_bytes = (static_cast<long long>(nelem) * E::kBytes + 15) & ~15LL;
   const int nchunks = static_cast<int>((slice_bytes + kChunkBytes - 1) / kChunkBytes);
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      const uint64_t pol_last = RL_STREAM_KEEP_L2 ? policy_evict_last() : policy_evict_normal();
+      const uint64_t pol_first = policy_evict_first();
       uint32_t it = 0;
       bool stop = false;
       bool valid_next = cid < a.R ? a.mask[cid] != 0 : false;
@@ -418,23 +459,26 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         valid_next = row + ncl < a.R ? a.mask[row + ncl] != 0 : false;  // one row ahead
         if (!valid || nchunks == 0) continue;
         const unsigned char* src = a.logits + row * a.row_bytes + lo * E::kBytes;
-        for (int c = 0; c < nchunks; ++c, ++it) {
-          const uint32_t slot = it % kSlots, round = it / kSlots;
-          if (round > 0 &&
-              !wait_bounded<false>(smem_addr(&sm.empty[slot]), (round - 1) & 1, abort_flag)) {
-            stop = true;
-            break;
+        for (int pass = 0; pass < (kStream ? 2 : 1) && !stop; ++pass) {
+          const uint64_t pol = (kStream && pass == 0) ? pol_last : pol_first;
+          for (int c = 0; c < nchunks; ++c, ++it) {
+            const uint32_t slot = it % kSlots, round = it / kSlots;
+            if (round > 0 &&
+                !wait_bounded<false>(smem_addr(&sm.empty[slot]), (round - 1) & 1, abort_flag)) {
+              stop = true;
+              break;
+            }
+            if (*abort_flag) {
+              stop = true;
+              break;
+            }
+            const uint32_t bytes = static_cast<uint32_t>(
+                min(static_cast<long long>(kChunkBytes), slice_bytes - static_cast<long long>(c) * kChunkBytes));
+            const uint32_t fb = smem_addr(&sm.full[slot]);
+            mbar_arrive_expect_tx(fb, bytes);
+            bulk_load(smem_addr(sm.ring[slot]), src + static_cast<long long>(c) * kChunkBytes, bytes,
+                      fb, pol);
           }
-          if (*abort_flag) {
-            stop = true;
-            break;
-          }
-          const uint32_t bytes = static_cast<uint32_t>(
-              min(static_cast<long long>(kChunkBytes), slice_bytes - static_cast<long long>(c) * kChunkBytes));
-          const uint32_t fb = smem_addr(&sm.full[slot]);
-          mbar_arrive_expect_tx(fb, bytes);
-          bulk_load(smem_addr(sm.ring[slot]), src + static_cast<long long>(c) * kChunkBytes, bytes, fb,
-                    pol);
         }
       }
       if (stop) {  // let every copy already issued land before this CTA can exit
@@ -489,76 +533,106 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         }
         continue;
       }
+      if (*abort_flag) {
+        aborted = true;
+        break;
+      }
       const long long y = rs.y;
-      const bool y_here = (y >= lo) && (y < hi);
+      // Where the sampled id sits in this CTA's slice: chunk cy, vector jy, element iy.
+      int cy = -1, jy = -1, iy = 0;
+      if (y >= lo && y < hi) {
+        const int off = static_cast<int>(y - lo);
+        cy = off / kChunkElems;
+        jy = (off % kChunkElems) / kVec;
+        iy = off % kVec;
+      }
 
       // ---- pass 1: online statistics of this thread's share of the slice
-      float m = -INFINITY;
-      float2 s2 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
+      ThreadStats st;
+      stats_init(st);
+      float zy = -INFINITY;
+      const uint32_t base = it;
       for (int c = 0; c < nchunks; ++c) {
-        const uint32_t k = it + c, slot = k % kSlots;
+        const uint32_t k = it++, slot = k % kSlots;
         wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
         const uint32_t buf = smem_addr(sm.ring[slot]);
-        const long long c0 = lo + static_cast<long long>(c) * kChunkElems;
+        const int c0 = c * kChunkElems;
+        const bool full_chunk = c0 + kChunkElems <= nelem;
 #pragma unroll
         for (int q = 0; q < kVecsPerThread; ++q) {
           const int j = tid + q * kConsumerThreads;
-          const long long e0 = c0 + static_cast<long long>(j) * kVec;
-          if (e0 < hi) {
+          const int e0 = c0 + j * kVec;
+          if (full_chunk || e0 < nelem) {
             const uint4 w = ld_shared_v4(buf + j * 16);
-            if (y_here && static_cast<unsigned long long>(y - e0) < static_cast<unsigned long long>(kVec)) {
+            if (c == cy && j == jy) {
               float z[kVec];
               E::unpack(w, z);
 #pragma unroll
               for (int i = 0; i < kVec; ++i)
-                if (i == y - e0) sm.zy = z[i];
+                if (i == iy) zy = z[i];
             }
-            if (hi - e0 >= kVec)
-              accumulate_full<E>(w, m, s2, t2);
+            if (full_chunk || nelem - e0 >= kVec)
+              accumulate_full<E>(w, st, q);
             else
-              accumulate_tail<E>(w, static_cast<int>(hi - e0), m, s2, t2);
+              accumulate_tail<E>(w, nelem - e0, st, q);
           }
         }
+        if (kStream) {  // this chunk is re-read from L2 in pass 2: free it now
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+        }
       }
-      float s = s2.x + s2.y, t = t2.x + t2.y;
+
+      // ---- one partial per warp; the C * 16 partials meet through xbar[b]
+      float m = st.m, s = 0.f, t = 0.f;
+#pragma unroll
+      for (int q = 0; q < kVecsPerThread; ++q) {
+        s += st.s[q].x + st.s[q].y;
+        t += st.t[q].x + st.t[q].y;
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float sx = __shfl_xor_sync(0xffffffffu, s, o);
-        const float tx = __shfl_xor_sync(0xffffffffu, t, o);
-        merge_stats(m, s, t, m2, sx, tx);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
+        merge_stats(m, s, t, m2, s2, t2);
+        zy = max_nan(zy, __shfl_xor_sync(0xffffffffu, zy, o));
       }
-      if (lane == 0) sm.wpart[warp] = make_float4(m, s, t, 0.f);
-      if (named_barrier_or(kConsumerBarrier, kConsumerThreads, *abort_flag != 0)) {
-        aborted = true;
-        break;
-      }
-
-      // ---- exchange the CTA partials across the cluster (DSMEM + remote arrive)
       const uint32_t b = vrow & 1;
-      if (tid == 0) {
-        float M = sm.wpart[0].x, S = sm.wpart[0].y, Tt = sm.wpart[0].z;
-        for (int w = 1; w < kConsumerWarps; ++w)
-          merge_stats(M, S, Tt, sm.wpart[w].x, sm.wpart[w].y, sm.wpart[w].z);
-        const float4 P = make_float4(M, S, Tt, y_here ? sm.zy : 0.f);
-        const uint32_t xa = smem_addr(&sm.xpart[b][rank]);
+      if (lane == 0) {
+        const float4 P = make_float4(m, s, t, zy);
+        const uint32_t xa = smem_addr(&sm.xpart[b][rank * kConsumerWarps + warp]);
         const uint32_t ba = smem_addr(&sm.xbar[b]);
         for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
         for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
       }
       wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
-
-      float M = -INFINITY, S = 0.f, Tt = 0.f;
-      for (uint32_t q = 0; q < csize; ++q) {
-        const float4 P = sm.xpart[b][q];
+      float M = -INFINITY, S = 0.f, Tt = 0.f, zyr = -INFINITY;
+      for (int p = lane; p < n_parts; p += 32) {
+        const float4 P = sm.xpart[b][p];
         merge_stats(M, S, Tt, P.x, P.y, P.z);
+        zyr = max_nan(zyr, P.w);
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+        const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
+        merge_stats(M, S, Tt, m2, s2, t2);
+        zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
+      }
+      // every lane of every warp uses lane 0's bits
+      M = __shfl_sync(0xffffffffu, M, 0);
+      S = __shfl_sync(0xffffffffu, S, 0);
+      Tt = __shfl_sync(0xffffffffu, Tt, 0);
+      zyr = __shfl_sync(0xffffffffu, zyr, 0);
+
       const bool y_ok = (y >= 0) && (y < a.V);
-      const float zy = y_ok ? sm.xpart[b][static_cast<uint32_t>(y / a.slice)].w : __int_as_float(0x7fc00000);
+      const float zv = y_ok ? zyr : __int_as_float(0x7fc00000);
       const float log2S = log2f(S);
       const float lse = fmaf(log2S, kLn2, M);
       const float H = kLn2 * (log2S - Tt / S);
-      const float logp = zy - lse;
+      const float logp = zv - lse;
 
       // ---- per-token objective and its derivative with respect to logp
       const float A = rs.A;
@@ -597,33 +671,41 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       const float a1 = sc * a.c_ent * kLn2;
       const float gy = sc * g;
       for (int c = 0; c < nchunks; ++c) {
-        const uint32_t slot = (it + c) % kSlots;
+        uint32_t slot;
+        if (kStream) {
+          const uint32_t k = it++;
+          slot = k % kSlots;
+          wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
+        } else {
+          slot = (base + c) % kSlots;
+        }
         if (drow) {
           const uint32_t buf = smem_addr(sm.ring[slot]);
-          const long long c0 = lo + static_cast<long long>(c) * kChunkElems;
+          const int c0 = c * kChunkElems;
+          const bool full_chunk = c0 + kChunkElems <= nelem;
 #pragma unroll
           for (int q = 0; q < kVecsPerThread; ++q) {
             const int j = tid + q * kConsumerThreads;
-            const long long e0 = c0 + static_cast<long long>(j) * kVec;
-            if (e0 < hi) {
+            const int e0 = c0 + j * kVec;
+            if (full_chunk || e0 < nelem) {
               float d[kVec];
               const uint4 w = ld_shared_v4(buf + j * 16);
               if (with_entropy)
                 grad_vec<E, true>(w, cL, a0, a1, d);
               else
                 grad_vec<E, false>(w, cL, a0, a1, d);
-              if (y_here && static_cast<unsigned long long>(y - e0) < static_cast<unsigned long long>(kVec)) {
+              if (c == cy && j == jy) {
 #pragma unroll
                 for (int i = 0; i < kVec; ++i)
-                  if (i == y - e0) d[i] -= gy;
+                  if (i == iy) d[i] -= gy;
               }
-              unsigned char* dst = drow + (e0 - lo) * E::kBytes;
-              if (hi - e0 >= kVec) {
+              unsigned char* dst = drow + static_cast<long long>(e0) * E::kBytes;
+              if (full_chunk || nelem - e0 >= kVec) {
                 st_global_cs_v4(dst, E::pack(d));
               } else {
 #pragma unroll
                 for (int i = 0; i < kVec; ++i)
-                  if (i < hi - e0) E::store1(dst + i * E::kBytes, d[i]);
+                  if (i < nelem - e0) E::store1(dst + i * E::kBytes, d[i]);
               }
             }
           }
@@ -631,7 +713,6 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
       }
-      it += nchunks;
       ++vrow;
     }
 
@@ -662,8 +743,8 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         double tot[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
         for (int w = 0; w < kConsumerWarps; ++w)
           for (int k = 0; k < 5; ++k) tot[k] += sm.wred[w][k];
-        const unsigned int st = atomicExch(&a.ws->status, 0u);
-        a.ws->last_status = st;
+        const unsigned int stw = atomicExch(&a.ws->status, 0u);
+        a.ws->last_status = stw;
         rl_loss_stats out;
         const double inv = N > 0 ? 1.0 / static_cast<double>(N) : 0.0;
         out.loss = -tot[0] * inv;
@@ -673,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         out.clip_frac = tot[4] * inv;
         out.n_tokens = N;
         out.n_clipped = static_cast<long long>(tot[4]);
-        out.device_error = static_cast<int>(st);
+        out.device_error = static_cast<int>(stw);
         out.reserved = 0;
         *a.stats = out;
       }
@@ -692,56 +773,70 @@ int elem_bytes(rl_dtype dt) {
   return 0;
 }
 
-// Smallest cluster whose per-CTA slice fits the ring with room to prefetch
-// the next row (else without that room).  Returns 0 if no cluster fits.
-int choose_cluster(int es, long long V, long long* slice_out) {
+struct Plan {
+  int cluster;      // CTAs per row
+  int n_clusters;   // clusters (rows in flight) in the persistent grid
+  long long slice;  // vocabulary elements per CTA
+  bool stream;      // rows streamed twice (second pass from L2)
+};
+
+// Row layout: a row that fits the ring twice over stays on chip in one CTA;
+// a longer one is streamed (or, in comparison builds, split over the
+// smallest cluster whose slices fit the ring with room to prefetch).
+bool choose_layout(int es, long long V, Plan* p) {
+  if (V > (1LL << 30)) return false;  // element offsets within a row are 32-bit
+  const long long row_chunks = ((V * es + 15) / 16 * 16 + kChunkBytes - 1) / kChunkBytes;
+  p->cluster = 1;
+  p->slice = V;
+  p->stream = false;
+  if (row_chunks <= kMaxResidentChunks) return true;
+  if (!RL_CLUSTER_RESIDENT) {
+    p->stream = true;
+    return true;
+  }
   const long long align = 16 / es;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int c = RL_MIN_CLUSTER; c <= kMaxCluster; ++c) {
-      long long s = (V + c - 1) / c;
-      s = (s + align - 1) / align * align;
-      const long long chunks = (s * es + kChunkBytes - 1) / kChunkBytes;
-      const bool fits = pass == 0 ? chunks * RL_SLICES_IN_RING + kLookaheadChunks <= kSlots
-                                  : chunks <= kSlots;
-      if (fits) {
-        *slice_out = s;
-        return c;
-      }
+  for (int c = 2; c <= kMaxCluster; ++c) {
+    long long s = (V + c - 1) / c;
+    s = (s + align - 1) / align * align;
+    if ((s * es + kChunkBytes - 1) / kChunkBytes <= kSlots - 3) {
+      p->cluster = c;
+      p->slice = s;
+      return true;
     }
   }
-  return 0;
+  return false;
 }
 
-template <int DT>
+template <int DT, bool S>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&policy_loss_kernel<DT>);
+  return reinterpret_cast<void*>(&policy_loss_kernel<DT, S>);
 }
 
-void* kernel_for(rl_dtype dt) {
+void* kernel_for(rl_dtype dt, bool stream) {
   switch (dt) {
-    case RL_F32: return kernel_ptr<RL_F32>();
-    case RL_BF16: return kernel_ptr<RL_BF16>();
-    case RL_F16: return kernel_ptr<RL_F16>();
+    case RL_F32: return stream ? kernel_ptr<RL_F32, true>() : kernel_ptr<RL_F32, false>();
+    case RL_BF16: return stream ? kernel_ptr<RL_BF16, true>() : kernel_ptr<RL_BF16, false>();
+    case RL_F16: return stream ? kernel_ptr<RL_F16, true>() : kernel_ptr<RL_F16, false>();
   }
   return nullptr;
 }
 
-// Per (device, dtype, cluster size): attributes set once and the number of
+// Per (device, kernel, cluster size): attributes set once and the number of
 // co-resident clusters.
 std::mutex g_occ_mu;
-std::map<std::tuple<int, int, int>, int> g_occ;
+std::map<std::tuple<int, int, int, int>, int> g_occ;
 
-rl_status max_clusters(rl_dtype dt, int cluster, int* out) {
+rl_status max_clusters(rl_dtype dt, bool stream, int cluster, int* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
-  const auto key = std::make_tuple(dev, static_cast<int>(dt), cluster);
+  const auto key = std::make_tuple(dev, static_cast<int>(dt), static_cast<int>(stream), cluster);
   std::lock_guard<std::mutex> lock(g_occ_mu);
   auto found = g_occ.find(key);
   if (found != g_occ.end()) {
     *out = found->second;
     return RL_OK;
   }
-  void* fn = kernel_for(dt);
+  void* fn = kernel_for(dt, stream);
   const int smem = static_cast<int>(sizeof(LossSmem));
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return RL_ERR_CUDA;
@@ -763,21 +858,18 @@ rl_status max_clusters(rl_dtype dt, int cluster, int* out) {
   return RL_OK;
 }
 
-rl_status plan(rl_dtype dt, long long V, long long R, int* cluster, int* n_clusters,
-               long long* slice) {
+rl_status plan(rl_dtype dt, long long V, long long R, Plan* p) {
   const int es = elem_bytes(dt);
   if (es == 0) return RL_ERR_DTYPE;
   if (V < 1 || R < 0) return RL_ERR_SHAPE;
-  const int c = choose_cluster(es, V, slice);
-  if (c == 0) return RL_ERR_SHAPE;
+  if (!choose_layout(es, V, p)) return RL_ERR_SHAPE;
   int occ = 0;
-  const rl_status st = max_clusters(dt, c, &occ);
+  const rl_status st = max_clusters(dt, p->stream, p->cluster, &occ);
   if (st != RL_OK) return st;
   long long n = occ;
   if (n > R) n = R > 0 ? R : 1;
-  if (n * c > kMaxGrid) n = kMaxGrid / c;
-  *cluster = c;
-  *n_clusters = static_cast<int>(n);
+  if (n * p->cluster > kMaxGrid) n = kMaxGrid / p->cluster;
+  p->n_clusters = static_cast<int>(n);
   return RL_OK;
 }
 
@@ -829,12 +921,11 @@ extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, lo
                                                  int* cluster_size, int* n_clusters,
                                                  int* smem_bytes) {
   if (!cluster_size || !n_clusters || !smem_bytes) return RL_ERR_NULL;
-  long long slice = 0;
-  int c = 0, n = 0;
-  const rl_status st = plan(dtype, V, n_rows, &c, &n, &slice);
+  Plan p;
+  const rl_status st = plan(dtype, V, n_rows, &p);
   if (st != RL_OK) return st;
-  *cluster_size = c;
-  *n_clusters = n;
+  *cluster_size = p.cluster;
+  *n_clusters = p.n_clusters;
   *smem_bytes = static_cast<int>(sizeof(LossSmem));
   return RL_OK;
 }
@@ -871,10 +962,11 @@ extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, 
     if (l0 < d0 + n && d0 < l0 + n) return RL_ERR_ALIAS;
   }
 
-  int cluster = 0, n_clusters = 0;
-  long long slice = 0;
-  const rl_status st = plan(dtype, V, R, &cluster, &n_clusters, &slice);
+  Plan pl;
+  const rl_status st = plan(dtype, V, R, &pl);
   if (st != RL_OK) return st;
+  const int cluster = pl.cluster, n_clusters = pl.n_clusters;
+  const long long slice = pl.slice;
 
   LossArgs args;
   args.logits = static_cast<const unsigned char*>(logits);
@@ -914,9 +1006,18 @@ extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, 
   cfg.numAttrs = 1;
   cudaError_t e = cudaErrorInvalidValue;
   switch (dtype) {
-    case RL_F32: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32>, args); break;
-    case RL_BF16: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_BF16>, args); break;
-    case RL_F16: e = cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16>, args); break;
+    case RL_F32:
+      e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32, true>, args)
+                    : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32, false>, args);
+      break;
+    case RL_BF16:
+      e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_BF16, true>, args)
+                    : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_BF16, false>, args);
+      break;
+    case RL_F16:
+      e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16, true>, args)
+                    : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16, false>, args);
+      break;
   }
   return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }

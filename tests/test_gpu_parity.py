@@ -2,8 +2,9 @@
 
 Small cases compare every output element by element (loss and statistics,
 per-token logp and entropy, every dlogits element at grad_scale 1 and N);
-they are sized to span several 16 KB chunks, every cluster size the planner
-picks (1 to 4 CTAs per row), ragged vocabulary tails and padded rows.  The
+they are sized to span several 16 KB chunks, both row layouts (rows held
+on chip for both passes, and rows streamed twice through the ring, up to
+256 chunks per row), ragged vocabulary tails and padded rows.  The
 full-size workloads run in the launch configuration the benchmark times and
 are compared on the scalar loss and statistics (all rows), on logp/entropy
 (all rows), on sampled dlogits rows, and on properties that hold at any size
@@ -93,8 +94,15 @@ SMALL = {
                                              lengths=("uniform", 1, 8), beta=0.1),
     "bf16_single_chunk": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=8192,
                                                      lengths=("uniform", 1, 8)),
+    "f32_v1M_stream": W["tiny_grpo"].scaled(n_prompts=1, group=2, T=4, V=1 << 20,
+                                            lengths=("uniform", 1, 4)),
+    "bf16_v300001_stream": W["large_grpo"].scaled(n_prompts=1, group=4, T=4, V=300001,
+                                                  lengths=("uniform", 1, 4), c_ent=0.01),
+    "f16_v49152_resident": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=49152,
+                                                     lengths=("uniform", 2, 8)),
 }
-PADDED_LD = {"f32_v12345_ragged": 12348, "bf16_v1001_ragged": 1008, "f16_v7_tiny": 8}
+PADDED_LD = {"f32_v12345_ragged": 12348, "bf16_v1001_ragged": 1008, "f16_v7_tiny": 8,
+             "bf16_v300001_stream": 300008}
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
@@ -103,15 +111,16 @@ def test_small_parity(name):
     _run_both(w, ld=PADDED_LD.get(name))
 
 
-def test_launch_shape_cluster_sizes():
-    assert rl.rl_policy_loss_launch_shape("bf16", 151936, 32768)[0] == 2
-    assert rl.rl_policy_loss_launch_shape("f32", 151936, 100)[0] == 4
-    assert rl.rl_policy_loss_launch_shape("bf16", 200000, 100)[0] == 3
-    assert rl.rl_policy_loss_launch_shape("f16", 32000, 100)[0] == 1
-    c, n, smem = rl.rl_policy_loss_launch_shape("bf16", 151936, 32768)
-    assert n >= 1 and smem <= 227 * 1024
+def test_launch_shape():
+    # rows that fit the ring twice stay on chip in one CTA; longer rows are
+    # streamed by one CTA; the persistent grid fills the device
+    for dt, V in (("bf16", 151936), ("f32", 151936), ("bf16", 200000), ("f16", 32000),
+                  ("f32", 1024), ("f32", 1 << 20)):
+        c, n, smem = rl.rl_policy_loss_launch_shape(dt, V, 32768)
+        assert c == 1 and 1 <= n <= 2048 and smem <= 227 * 1024, (dt, V, c, n, smem)
+    assert rl.rl_policy_loss_launch_shape("bf16", 151936, 5)[1] == 5  # no more CTAs than rows
     with pytest.raises(rl.RlLossError):
-        rl.rl_policy_loss_launch_shape("f32", 1 << 20, 10)  # 4 MB rows do not fit on chip
+        rl.rl_policy_loss_launch_shape("bf16", (1 << 30) + 8, 10)  # beyond 32-bit row offsets
 
 
 def test_in_place_matches():

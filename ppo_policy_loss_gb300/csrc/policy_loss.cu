@@ -258,49 +258,48 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, float& t, float 
 }
 
 struct ThreadStats {
-  float m;
+  float m;    // running max, starting at the clamp floor (finite: no -inf cases)
+  float nmL;  // -m * log2(e)
   float2 s[kVecsPerThread];
   float2 t[kVecsPerThread];
 };
 
 __device__ __forceinline__ void stats_init(ThreadStats& a) {
-  a.m = -INFINITY;
+  a.m = kFloor;
+  a.nmL = -kFloor * kLog2e;
 #pragma unroll
   for (int q = 0; q < kVecsPerThread; ++q) a.s[q] = a.t[q] = make_float2(0.f, 0.f);
 }
 
-// Raise the running max to vm, rescaling every chain.  Returns false while
-// nothing finite has been seen (then only a NaN is remembered).
-__device__ __forceinline__ bool raise_max(float vm, ThreadStats& a) {
-  if (vm > a.m) {
-    if (a.m != -INFINITY) {
-      const float d = (vm - a.m) * kLog2e;
-      const float f = ex2_approx(-d);
-      const float2 f2 = make_float2(f, f), nd2 = make_float2(-d, -d);
+// Raise each lane's running max to vm, rescaling its chains.  The decision
+// is taken per warp (all lanes rescale when any lane needs to; for the others
+// the factor is exactly 1), so the branch never diverges.  Must be called by
+// the whole warp.  A NaN vm never raises the max: its NaN enters through x.
+__device__ __forceinline__ void raise_max(float vm, ThreadStats& a) {
+  if (__any_sync(0xffffffffu, vm > a.m)) {
+    const float nm = fmaxf(a.m, vm);
+    const float d = (nm - a.m) * kLog2e;  // >= 0 and finite: both are >= the floor
+    const float f = ex2_approx(-d);
+    const float2 f2 = make_float2(f, f), nd2 = make_float2(-d, -d);
 #pragma unroll
-      for (int q = 0; q < kVecsPerThread; ++q) {
-        a.t[q] = __fmul2_rn(f2, __ffma2_rn(nd2, a.s[q], a.t[q]));
-        a.s[q] = __fmul2_rn(f2, a.s[q]);
-      }
+    for (int q = 0; q < kVecsPerThread; ++q) {
+      a.t[q] = __fmul2_rn(f2, __ffma2_rn(nd2, a.s[q], a.t[q]));
+      a.s[q] = __fmul2_rn(f2, a.s[q]);
     }
-    a.m = vm;
+    a.m = nm;
+    a.nmL = -nm * kLog2e;
   }
-  if (a.m == -INFINITY) {
-    if (vm != vm) a.s[0].x = vm;
-    return false;
-  }
-  return true;
 }
 
-// Pass-1 update with one full 16-byte vector into chain q.
+// Pass-1 update with one full 16-byte vector into chain q (whole warp).
 template <class E>
 __device__ __forceinline__ void accumulate_full(uint4 w, ThreadStats& a, int q) {
   E::clamp(w);
-  if (!raise_max(E::vmax(w), a)) return;
+  raise_max(E::vmax(w), a);
   float z[E::kVec];
   E::unpack(w, z);
   const float2 L2 = make_float2(kLog2e, kLog2e);
-  const float2 nmL = make_float2(-a.m * kLog2e, -a.m * kLog2e);
+  const float2 nmL = make_float2(a.nmL, a.nmL);
   float2 s = a.s[q], t = a.t[q];
 #pragma unroll
   for (int i = 0; i < E::kVec; i += 2) {
@@ -313,27 +312,38 @@ __device__ __forceinline__ void accumulate_full(uint4 w, ThreadStats& a, int q) 
   a.t[q] = t;
 }
 
-// Pass-1 update with the first nv (< kVec) elements of a vector (row tail).
+// Pass-1 update with the first nv (0..kVec) elements of a vector (row tail;
+// whole warp, lanes past the end pass nv = 0).
 template <class E>
 __device__ __forceinline__ void accumulate_tail(uint4 w, int nv, ThreadStats& a, int q) {
   E::clamp(w);
   float z[E::kVec];
   E::unpack(w, z);
-  float vm = z[0];
+  float vm = kFloor;
 #pragma unroll
-  for (int i = 1; i < E::kVec; ++i)
+  for (int i = 0; i < E::kVec; ++i)
     if (i < nv) vm = max_nan(vm, z[i]);
-  if (!raise_max(vm, a)) return;
-  const float mL = a.m * kLog2e;
+  raise_max(vm, a);
 #pragma unroll
   for (int i = 0; i < E::kVec; ++i) {
     if (i < nv) {
-      const float x = fmaf(z[i], kLog2e, -mL);
+      const float x = fmaf(z[i], kLog2e, a.nmL);
       const float e = ex2_approx(x);
       a.s[q].x += e;
       a.t[q].x = fmaf(e, x, a.t[q].x);
     }
   }
+}
+
+template <class E>
+__device__ __forceinline__ float element_of(uint4 w, int i) {
+  float z[E::kVec];
+  E::unpack(w, z);
+  float r = z[0];
+#pragma unroll
+  for (int k = 1; k < E::kVec; ++k)
+    if (k == i) r = z[k];
+  return r;
 }
 
 // Pass-2 gradient of one vector: d_v = 2^x (a0 + a1 x), x = z log2(e) - cL.
@@ -538,13 +548,15 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         break;
       }
       const long long y = rs.y;
-      // Where the sampled id sits in this CTA's slice: chunk cy, vector jy, element iy.
-      int cy = -1, jy = -1, iy = 0;
+      // Where the sampled id sits in this CTA's slice: chunk cy, vector jy of
+      // the chunk (owned by thread ty as its vector qy), element iy.
+      int cy = -1, jy = 0, iy = 0, ty = -1;
       if (y >= lo && y < hi) {
         const int off = static_cast<int>(y - lo);
         cy = off / kChunkElems;
         jy = (off % kChunkElems) / kVec;
         iy = off % kVec;
+        ty = jy % kConsumerThreads;
       }
 
       // ---- pass 1: online statistics of this thread's share of the slice
@@ -555,28 +567,22 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       for (int c = 0; c < nchunks; ++c) {
         const uint32_t k = it++, slot = k % kSlots;
         wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
-        const uint32_t buf = smem_addr(sm.ring[slot]);
+        const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
         const int c0 = c * kChunkElems;
-        const bool full_chunk = c0 + kChunkElems <= nelem;
+        if (c0 + kChunkElems <= nelem) {
 #pragma unroll
-        for (int q = 0; q < kVecsPerThread; ++q) {
-          const int j = tid + q * kConsumerThreads;
-          const int e0 = c0 + j * kVec;
-          if (full_chunk || e0 < nelem) {
-            const uint4 w = ld_shared_v4(buf + j * 16);
-            if (c == cy && j == jy) {
-              float z[kVec];
-              E::unpack(w, z);
+          for (int q = 0; q < kVecsPerThread; ++q)
+            accumulate_full<E>(ld_shared_v4(buf + q * kConsumerThreads * 16), st, q);
+        } else {
 #pragma unroll
-              for (int i = 0; i < kVec; ++i)
-                if (i == iy) zy = z[i];
-            }
-            if (full_chunk || nelem - e0 >= kVec)
-              accumulate_full<E>(w, st, q);
-            else
-              accumulate_tail<E>(w, nelem - e0, st, q);
+          for (int q = 0; q < kVecsPerThread; ++q) {
+            const int e0 = c0 + (tid + q * kConsumerThreads) * kVec;
+            const int nv = max(0, min(kVec, nelem - e0));
+            const uint4 w = nv > 0 ? ld_shared_v4(buf + q * kConsumerThreads * 16) : make_uint4(0u, 0u, 0u, 0u);
+            accumulate_tail<E>(w, nv, st, q);
           }
         }
+        if (c == cy && tid == ty) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + jy * 16), iy);
         if (kStream) {  // this chunk is re-read from L2 in pass 2: free it now
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
@@ -599,14 +605,22 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         zy = max_nan(zy, __shfl_xor_sync(0xffffffffu, zy, o));
       }
       const uint32_t b = vrow & 1;
-      if (lane == 0) {
-        const float4 P = make_float4(m, s, t, zy);
-        const uint32_t xa = smem_addr(&sm.xpart[b][rank * kConsumerWarps + warp]);
-        const uint32_t ba = smem_addr(&sm.xbar[b]);
-        for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
-        for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
+      if (csize == 1) {  // one CTA per row: CTA-scope publish and wait
+        if (lane == 0) {
+          sm.xpart[b][warp] = make_float4(m, s, t, zy);
+          mbar_arrive(smem_addr(&sm.xbar[b]));
+        }
+        wait_bounded<false>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
+      } else {  // cluster: every rank gets every warp's partial through DSMEM
+        if (lane == 0) {
+          const float4 P = make_float4(m, s, t, zy);
+          const uint32_t xa = smem_addr(&sm.xpart[b][rank * kConsumerWarps + warp]);
+          const uint32_t ba = smem_addr(&sm.xbar[b]);
+          for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
+          for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
+        }
+        wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
       }
-      wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
       float M = -INFINITY, S = 0.f, Tt = 0.f, zyr = -INFINITY;
       for (int p = lane; p < n_parts; p += 32) {
         const float4 P = sm.xpart[b][p];
@@ -682,31 +696,60 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         if (drow) {
           const uint32_t buf = smem_addr(sm.ring[slot]);
           const int c0 = c * kChunkElems;
-          const bool full_chunk = c0 + kChunkElems <= nelem;
+          unsigned char* dst = drow + static_cast<long long>(c0 + tid * kVec) * E::kBytes;
+          if (c0 + kChunkElems <= nelem) {
 #pragma unroll
-          for (int q = 0; q < kVecsPerThread; ++q) {
-            const int j = tid + q * kConsumerThreads;
-            const int e0 = c0 + j * kVec;
-            if (full_chunk || e0 < nelem) {
+            for (int q = 0; q < kVecsPerThread; ++q) {
               float d[kVec];
-              const uint4 w = ld_shared_v4(buf + j * 16);
+              const uint4 w = ld_shared_v4(buf + (tid + q * kConsumerThreads) * 16);
               if (with_entropy)
                 grad_vec<E, true>(w, cL, a0, a1, d);
               else
                 grad_vec<E, false>(w, cL, a0, a1, d);
-              if (c == cy && j == jy) {
+              st_global_cs_v4(dst + q * kConsumerThreads * 16, E::pack(d));
+            }
+          } else {
 #pragma unroll
-                for (int i = 0; i < kVec; ++i)
-                  if (i == iy) d[i] -= gy;
-              }
-              unsigned char* dst = drow + static_cast<long long>(e0) * E::kBytes;
-              if (full_chunk || nelem - e0 >= kVec) {
-                st_global_cs_v4(dst, E::pack(d));
-              } else {
+            for (int q = 0; q < kVecsPerThread; ++q) {
+              const int e0 = c0 + (tid + q * kConsumerThreads) * kVec;
+              if (e0 < nelem) {
+                float d[kVec];
+                const uint4 w = ld_shared_v4(buf + (tid + q * kConsumerThreads) * 16);
+                if (with_entropy)
+                  grad_vec<E, true>(w, cL, a0, a1, d);
+                else
+                  grad_vec<E, false>(w, cL, a0, a1, d);
+                unsigned char* o = dst + q * kConsumerThreads * 16;
+                if (nelem - e0 >= kVec) {
+                  st_global_cs_v4(o, E::pack(d));
+                } else {
 #pragma unroll
-                for (int i = 0; i < kVec; ++i)
-                  if (i < nelem - e0) E::store1(dst + i * E::kBytes, d[i]);
+                  for (int i = 0; i < kVec; ++i)
+                    if (i < nelem - e0) E::store1(o + i * E::kBytes, d[i]);
+                }
               }
+            }
+          }
+          if (c == cy && tid == ty) {
+            // the owner of the sampled id rewrites its vector with the -g term
+            // (after its own store of that vector, so program order settles it)
+            float d[kVec];
+            const uint4 w = ld_shared_v4(buf + jy * 16);
+            if (with_entropy)
+              grad_vec<E, true>(w, cL, a0, a1, d);
+            else
+              grad_vec<E, false>(w, cL, a0, a1, d);
+#pragma unroll
+            for (int i = 0; i < kVec; ++i)
+              if (i == iy) d[i] -= gy;
+            const int e0 = c0 + jy * kVec;
+            unsigned char* o = drow + static_cast<long long>(e0) * E::kBytes;
+            if (nelem - e0 >= kVec) {
+              st_global_cs_v4(o, E::pack(d));
+            } else {
+#pragma unroll
+              for (int i = 0; i < kVec; ++i)
+                if (i < nelem - e0) E::store1(o + i * E::kBytes, d[i]);
             }
           }
         }

@@ -1,14 +1,18 @@
-"""Benchmark of the fused GRPO policy-loss step on GB300.
+"""Benchmark of the fused RL policy-loss step on GB300.
 
-One step = the whole hot path over one batch: rl_group_advantages (reward
-normalisation) then rl_policy_loss_fwd_bwd (log-softmax, clipped surrogate,
-k3 KL, entropy bonus, masked-mean loss and the bf16 logits gradient in one
-launch).  Workload: Qwen3-0.6B-shaped GRPO, 4 prompts x group 8 = 32
-sequences x T=1024 positions x V=151936 bf16 logits ~N(0, 3), ragged lengths
-U{256..1024}; synthetic inputs (seeded), 10 GB of logits, far larger than L2,
-so no flush is needed between steps.
+One step = the whole hot path over one batch: the advantages (GRPO reward
+normalisation with rl_group_advantages, or PPO-GAE with rl_gae_reverse_scan)
+then rl_policy_loss_fwd_bwd (log-softmax, clipped surrogate, k3 KL, entropy
+bonus, masked-mean loss and the logits gradient in one launch).
+
+Default workload (the headline): Qwen3-0.6B-shaped GRPO, 4 prompts x group 8
+= 32 sequences x T=1024 positions x V=151936 bf16 logits ~N(0, 3), ragged
+lengths U{256..1024}; synthetic seeded inputs; 10 GB of logits, far larger
+than L2, so no flush is needed between steps.  ``--workload`` selects one of
+the other configurations (see ppo_policy_loss_gb300/synth.py).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME]
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own
 replica of the workload on its GPU (the path has no cross-rank exchange
@@ -35,8 +39,21 @@ sys.path.insert(0, ROOT)
 METRIC = "fused GRPO loss+dlogits tokens/s at V=151936 bf16; % of HBM roofline"
 WORKLOAD = "qwen3_0p6b_grpo"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "policy_loss_qwen3_0p6b_grpo_traffic.txt")
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
+DESCRIBE = {
+    "tiny_grpo": "tiny GRPO: 2 prompts x group 4 = 8 seqs, T=16, V=1024 fp32",
+    "qwen3_0p6b_grpo": "Qwen3-0.6B GRPO: 4 prompts x group 8 = 32 seqs, T=1024, V=151936 bf16, "
+                       "lengths U{256..1024}, eps=0.2 beta=0.04 c_ent=0",
+    "long_seq_grpo": "long-sequence GRPO: 2 prompts x group 8 = 16 seqs, T=4096, V=32000 fp16, "
+                     "geometric lengths (mean 1500, cap 4096), beta=0 c_ent=0.01",
+    "ppo_gae": "PPO-GAE: 64 seqs, T=512, V=151936 bf16, gamma=1 lambda=0.95, c_ent=0.01",
+    "large_grpo": "large GRPO: 8 prompts x group 8 = 64 seqs, T=2048, V=151936 bf16, "
+                  "lengths U{128..2048}, eps=0.2 beta=0.04",
+}
+
+
+def traffic_file(workload):
+    return os.path.join(ROOT, "profiles", f"policy_loss_{workload}_traffic.txt")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -61,12 +78,12 @@ def kernel_sha() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(workload=WORKLOAD, path=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
     try:
         kv = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(path or traffic_file(workload)) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
@@ -76,6 +93,22 @@ def recorded_traffic():
         return float(kv["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Positions per second over all ranks: every rank runs its own replica."""
+    return world * rows_per_rank / (ms_per_step / 1e3)
 
 
 class ClockSampler:
@@ -127,22 +160,6 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def max_over_ranks(x: float, device) -> float:
-    """Max of a per-rank scalar over all ranks (identity when not distributed)."""
-    import torch
-    import torch.distributed as dist
-    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
-        return x
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
-    """Positions per second over all ranks: every rank runs its own replica."""
-    return world * rows_per_rank / (ms_per_step / 1e3)
-
-
 # ----------------------------------------------------------------------------- inputs
 def make_inputs(w, dev):
     """Device inputs of the workload.  logp_old / ref_logp are composed from the
@@ -153,29 +170,90 @@ def make_inputs(w, dev):
 
     small = synth.small_inputs(w)
     logits = synth.logits(w, device=dev)
-    ids = torch.from_numpy(small["ids"]).to(dev)
-    mask = torch.from_numpy(small["mask"]).to(dev)
-    rewards = torch.from_numpy(small["rewards"]).to(dev)
+
+    def t(x, dt=None):
+        a = torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        return a if dt is None else a.to(dt)
+
+    inp = dict(small=small, logits=logits, ids=t(small["ids"]), mask=t(small["mask"]),
+               rewards=t(small["rewards"]))
+    if w.advantage == "gae":
+        inp["values"] = t(small["values"])
+        inp["lengths"] = t(small["lengths"])
     logp = torch.empty(w.R, dtype=torch.float32, device=dev)
     for r0 in range(0, w.R, 1024):  # torch log_softmax, chunked (input preparation only)
         blk = logits[r0:r0 + 1024].float()
         lse = torch.logsumexp(blk, dim=1)
-        logp[r0:r0 + 1024] = blk.gather(1, ids[r0:r0 + 1024, None])[:, 0] - lse
+        logp[r0:r0 + 1024] = blk.gather(1, inp["ids"][r0:r0 + 1024, None])[:, 0] - lse
         del blk
-    m = mask.bool()
-    logp_old = torch.where(m, logp + torch.from_numpy(small["noise_old"]).to(dev).float(), 0.0)
-    ref = torch.where(m, logp + torch.from_numpy(small["noise_ref"]).to(dev).float(), 0.0)
-    return dict(small=small, logits=logits, ids=ids, mask=mask, rewards=rewards,
-                logp_old=logp_old.contiguous(), ref=ref.contiguous())
+    m = inp["mask"].bool()
+    inp["logp_old"] = torch.where(m, logp + t(small["noise_old"], torch.float32), 0.0).contiguous()
+    inp["ref"] = torch.where(m, logp + t(small["noise_ref"], torch.float32), 0.0).contiguous()
+    return inp
 
 
 def alg_bytes(w, n_valid):
     """Algorithmic bytes of one rl_policy_loss_fwd_bwd launch: one read of each
     valid logits row, one write of every dlogits row, plus the per-row arrays
-    (ids 8, logp_old 4, ref 4, mask 1, logp_out 4, entropy_out 4) and the
-    per-sequence advantages."""
+    (ids 8, logp_old 4, ref 4 when the KL term is on, mask 1, logp_out 4,
+    entropy_out 4) and the advantages (per sequence, or per token for PPO-GAE)."""
     es = w.elem_bytes
-    return n_valid * w.V * es + w.R * w.V * es + w.R * (8 + 4 + 4 + 1 + 4 + 4) + w.B * 4
+    adv = w.R * 4 if w.advantage == "gae" else w.B * 4
+    ref = 4 if w.beta != 0 else 0
+    return n_valid * w.V * es + w.R * w.V * es + w.R * (8 + 4 + ref + 1 + 4 + 4) + adv
+
+
+class Step:
+    """Device buffers of one step and the launches of the whole path on them."""
+
+    KEYS = ("logits", "ids", "mask", "rewards", "logp_old", "ref", "values", "lengths")
+
+    def __init__(self, w, inp, dev, own_inputs=False):
+        import torch
+        from ppo_policy_loss_gb300 import torch_api
+
+        self.w = w
+        self.keys = [k for k in self.KEYS if k in inp]
+        self.d = {k: (torch.empty_like(inp[k]) if own_inputs else inp[k]) for k in self.keys}
+        self.adv = torch.empty(w.R if w.advantage == "gae" else w.B, dtype=torch.float32,
+                               device=dev)
+        self.dlogits = torch.empty_like(inp["logits"])
+        self.logp = torch.empty(w.R, dtype=torch.float32, device=dev)
+        self.ent = torch.empty(w.R, dtype=torch.float32, device=dev)
+        self.ws = torch_api.new_workspace(w.R, dev)
+        self.stats = torch_api.new_stats(dev)
+        self.ld = inp["logits"].stride(0)
+
+    def launch(self, stream, ev=None):
+        """2 launches: the advantages, then the fused loss (bracketed by ev)."""
+        import ppo_policy_loss_gb300 as rl
+        w, d = self.w, self.d
+        if w.advantage == "gae":
+            rl.rl_gae_reverse_scan(d["rewards"], d["values"], d["lengths"], w.B, w.T, w.gamma,
+                                   w.lam, self.adv, None, stream)
+            layout = rl.RL_ADV_PER_TOKEN
+        else:
+            rl.rl_group_advantages(d["rewards"], w.B // w.group, w.group, 1e-4, 1, self.adv,
+                                   stream)
+            layout = rl.RL_ADV_PER_SEQ
+        if ev is not None:
+            ev[0].record(stream)
+        rl.rl_policy_loss_fwd_bwd(d["logits"], w.dtype, w.B, w.T, w.V, self.ld, d["ids"],
+                                  d["logp_old"], d["ref"] if w.beta != 0 else None, d["mask"],
+                                  self.adv, layout, w.eps, w.beta, w.c_ent, 1.0, self.dlogits,
+                                  self.logp, self.ent, self.stats, self.ws, self.ws.numel(),
+                                  stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+
+def workload_for(args):
+    from ppo_policy_loss_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.seqs:  # a slice of the workload (profiling captures): same T, V and distributions
+        w = (w.scaled(n_prompts=max(1, args.seqs // w.group)) if args.seqs >= w.group
+             else w.scaled(n_prompts=1, group=max(2, args.seqs)))
+    return w
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -183,7 +261,7 @@ def run_gpu(args):
     import torch
 
     import ppo_policy_loss_gb300 as rl
-    from ppo_policy_loss_gb300 import STATS_BYTES, synth, torch_api
+    from ppo_policy_loss_gb300 import torch_api
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -193,31 +271,11 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
     rl.build()
     rl.load()
-    w = synth.WORKLOADS[WORKLOAD]
-    if args.seqs:  # a slice of the workload (profiling captures): same T, V and distributions
-        w = (w.scaled(n_prompts=max(1, args.seqs // w.group)) if args.seqs >= w.group
-             else w.scaled(n_prompts=1, group=max(2, args.seqs)))
+    w = workload_for(args)
     inp = make_inputs(w, dev)
     n_valid = int(inp["small"]["mask"].sum())
     stream = torch.cuda.current_stream(dev)
-    adv = torch.empty(w.B, dtype=torch.float32, device=dev)
-    dlogits = torch.empty_like(inp["logits"])
-    logp_out = torch.empty(w.R, dtype=torch.float32, device=dev)
-    ent_out = torch.empty(w.R, dtype=torch.float32, device=dev)
-    ws = torch_api.new_workspace(w.R, dev)
-    stats = torch_api.new_stats(dev)
-    ld = inp["logits"].stride(0)
-
-    def step(ev=None):
-        rl.rl_group_advantages(inp["rewards"], w.B // w.group, w.group, 1e-4, 1, adv, stream)
-        if ev is not None:
-            ev[0].record(stream)
-        rl.rl_policy_loss_fwd_bwd(inp["logits"], "bf16", w.B, w.T, w.V, ld, inp["ids"],
-                                  inp["logp_old"], inp["ref"], inp["mask"], adv,
-                                  rl.RL_ADV_PER_SEQ, w.eps, w.beta, w.c_ent, 1.0, dlogits,
-                                  logp_out, ent_out, stats, ws, ws.numel(), stream)
-        if ev is not None:
-            ev[1].record(stream)
+    step = Step(w, inp, dev)
 
     def barrier():
         if world > 1:
@@ -226,29 +284,28 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step()
+        step.launch(stream)
     barrier()
-    st = torch_api.read_stats(stats)
+    st = torch_api.read_stats(step.stats)
     assert st["device_error"] == 0 and st["n_tokens"] == n_valid, st
 
     # ---- timed region: K steps, inputs resident in HBM
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(int(vis.split(",")[local]) if vis else local)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     sampler.start()
     time.sleep(0.3)
     t0.record(stream)
     for i in range(args.steps):
-        step(kev[i])
+        step.launch(stream, kev[i])
     t1.record(stream)
     barrier()
     clocks = sampler.stop()
-    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dev)
     k_ms = [a.elapsed_time(b) for a, b in kev]
-    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     value = whole_job_rate(w.R, world, ms_step)
 
@@ -257,25 +314,25 @@ def run_gpu(args):
     bytes_launch = alg_bytes(w, n_valid)
     peak, peak_kind = hbm_peak()
     achieved = bytes_launch / (kern_ms / 1e3) / 1e9
-    traffic = recorded_traffic()
+    traffic = recorded_traffic(args.workload) if not args.seqs else None
 
     # ---- end to end through the C ABI with pinned host buffers
-    e2e = run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, ws, ld)
-
+    e2e = run_e2e(args, w, inp, dev, stream, step) if args.e2e_steps > 0 else None
+    shape = rl.rl_policy_loss_launch_shape(w.dtype, w.V, w.R)
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; shapes and distributions of the Qwen3-0.6B GRPO workload)",
-        "config": {"workload": f"{WORKLOAD}: 4 prompts x group 8 = 32 seqs, T=1024, V=151936 bf16, "
-                               "lengths U{256..1024}, eps=0.2 beta=0.04 c_ent=0",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": f"{args.workload}: {DESCRIBE.get(args.workload, '')}",
                    "B": w.B, "T": w.T, "V": w.V, "rows": w.R, "valid_tokens": n_valid,
                    "slice": (f"profiling slice: first {w.B} sequences" if args.seqs else None),
                    "valid_tokens_per_s": world * n_valid / (ms_step / 1e3),
-                   "l2": "inputs (10 GB logits) far larger than the 129 MB L2; no flush",
+                   "l2": (f"inputs ({w.R * w.V * w.elem_bytes / 1e9:.1f} GB logits) vs 129 MB "
+                          "L2; no flush"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch_shape": dict(zip(("cluster", "clusters", "smem"),
-                                            rl.rl_policy_loss_launch_shape("bf16", w.V, w.R)))},
+                   "launch_shape": {"cluster": shape[0], "clusters": shape[1],
+                                    "smem": shape[2]}},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "traffic": traffic, "alg_bytes_per_launch": bytes_launch,
@@ -294,7 +351,7 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
 
 
-def run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, ws, ld):
+def run_e2e(args, w, inp, dev, stream, step0):
     """The same step through the public C-ABI calls with HOST buffers: every
     step copies all its inputs from pinned host memory to the device and the
     gradient and statistics back, inside the timed region.  Steps are
@@ -304,31 +361,22 @@ def run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, w
     every buffer from being reused before its last reader is done."""
     import torch
 
-    import ppo_policy_loss_gb300 as rl
-    from ppo_policy_loss_gb300 import STATS_BYTES
+    from ppo_policy_loss_gb300 import STATS_BYTES, stats_from_bytes
 
     steps = max(1, min(args.steps, args.e2e_steps))
-    keys = ("logits", "ids", "mask", "rewards", "logp_old", "ref")
     h = {}
-    for k in keys:
+    for k in step0.keys:
         h[k] = torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
         h[k].copy_(inp[k])
-    h_dlogits = torch.empty(dlogits.shape, dtype=dlogits.dtype, pin_memory=True)
+    h_dlogits = torch.empty(step0.dlogits.shape, dtype=step0.dlogits.dtype, pin_memory=True)
     h_stats = torch.empty(STATS_BYTES, dtype=torch.uint8, pin_memory=True)
-    sets = [dict(d={k: torch.empty_like(inp[k]) for k in keys}, dlogits=dlogits, stats=stats,
-                 ws=ws, adv=adv, logp=logp_out, ent=ent_out)]
-    sets.append(dict(d={k: torch.empty_like(inp[k]) for k in keys},
-                     dlogits=torch.empty_like(dlogits),
-                     stats=torch.zeros_like(stats), ws=torch.zeros_like(ws),
-                     adv=torch.empty_like(adv), logp=torch.empty_like(logp_out),
-                     ent=torch.empty_like(ent_out)))
+    sets = [Step(w, inp, dev, own_inputs=True), Step(w, inp, dev, own_inputs=True)]
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = h_dlogits.numel() * h_dlogits.element_size() + STATS_BYTES
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     s_cmp = stream
-    ev = lambda: torch.cuda.Event()
-    comp_done = [ev(), ev()]   # compute of the last step on set b finished
-    out_done = [ev(), ev()]    # download of the last step on set b finished
+    comp_done = [torch.cuda.Event(), torch.cuda.Event()]  # last compute on set b finished
+    out_done = [torch.cuda.Event(), torch.cuda.Event()]   # last download from set b finished
     for e in comp_done + out_done:
         e.record(s_cmp)
 
@@ -336,22 +384,18 @@ def run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, w
         b = sets[i % 2]
         with torch.cuda.stream(s_in):
             s_in.wait_event(comp_done[i % 2])          # set b's inputs no longer read
-            for k in keys:
-                b["d"][k].copy_(h[k], non_blocking=True)
-            in_done = ev()
+            for k in b.keys:
+                b.d[k].copy_(h[k], non_blocking=True)
+            in_done = torch.cuda.Event()
             in_done.record(s_in)
         s_cmp.wait_event(in_done)
         s_cmp.wait_event(out_done[i % 2])              # set b's gradient already downloaded
-        rl.rl_group_advantages(b["d"]["rewards"], w.B // w.group, w.group, 1e-4, 1, b["adv"], s_cmp)
-        rl.rl_policy_loss_fwd_bwd(b["d"]["logits"], "bf16", w.B, w.T, w.V, ld, b["d"]["ids"],
-                                  b["d"]["logp_old"], b["d"]["ref"], b["d"]["mask"], b["adv"],
-                                  rl.RL_ADV_PER_SEQ, w.eps, w.beta, w.c_ent, 1.0, b["dlogits"],
-                                  b["logp"], b["ent"], b["stats"], b["ws"], b["ws"].numel(), s_cmp)
+        b.launch(s_cmp)
         comp_done[i % 2].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i % 2])
-            h_dlogits.copy_(b["dlogits"], non_blocking=True)
-            h_stats.copy_(b["stats"], non_blocking=True)
+            h_dlogits.copy_(b.dlogits, non_blocking=True)
+            h_stats.copy_(b.stats, non_blocking=True)
             out_done[i % 2].record(s_out)
 
     one(0)
@@ -365,19 +409,15 @@ def run_e2e(args, w, inp, dev, stream, adv, dlogits, logp_out, ent_out, stats, w
     s_cmp.wait_stream(s_out)
     t1.record(s_cmp)
     torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1) / steps
+    ms = max_over_ranks(t0.elapsed_time(t1), dev) / steps
     world = dist_env()[0]
-    st = torch_api_read(h_stats)
+    st = stats_from_bytes(h_stats.numpy().tobytes())
     del sets, h, h_dlogits
-    return {"value": world * w.R / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+    return {"value": whole_job_rate(w.R, world, ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": steps,
             "pipeline": "double-buffered: upload of step i+1 beside download of step i",
             "loss_last_step": st["loss"]}
-
-
-def torch_api_read(h_stats):
-    from ppo_policy_loss_gb300 import stats_from_bytes
-    return stats_from_bytes(h_stats.numpy().tobytes())
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -386,8 +426,15 @@ def sample_rows(w, n):
     return np.unique(np.linspace(0, w.R - 1, max(1, n)).round().astype(np.int64))
 
 
+def _storage(t):
+    import torch
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
 def sample_logits(w, rows, dev_logits=None):
-    """Host copy (uint16 storage) of the given rows of the workload's logits."""
+    """Host copy (element storage) of the given rows of the workload's logits."""
     import torch
     from ppo_policy_loss_gb300 import synth
 
@@ -401,7 +448,7 @@ def sample_logits(w, rows, dev_logits=None):
             sel = rows[(rows // synth.ROW_BLOCK) == b] - b * synth.ROW_BLOCK
             parts.append(blk[torch.from_numpy(sel).to(blk.device)].cpu())
         t = torch.cat(parts)
-    return t.view(torch.int16).numpy().view(np.uint16)
+    return _storage(t)
 
 
 def cpu_sample(w, rows, dev_logits=None):
@@ -416,25 +463,30 @@ def cpu_sample(w, rows, dev_logits=None):
     _, logp, _ = oracle.row_stats(host, w.dtype, w.V, ids, mask)
     lo = np.where(mask != 0, logp + small["noise_old"][rows], 0.0).astype(np.float32)
     rf = np.where(mask != 0, logp + small["noise_ref"][rows], 0.0).astype(np.float32)
-    return dict(host=host, mask=mask, ids=ids, rewards=small["rewards"], rows=rows, lo=lo, rf=rf)
+    return dict(host=host, mask=mask, ids=ids, small=small, rows=rows, lo=lo, rf=rf)
 
 
 def oracle_step(w, s, threads):
-    """One oracle pass of the whole step over the sample: group advantages of
-    the batch, then loss, statistics and the bf16 gradient of every sample row."""
+    """One oracle pass of the whole step over the sample: the batch's
+    advantages, then loss, statistics and the gradient of every sample row."""
     import oracle
 
-    A = oracle.group_advantages(s["rewards"], w.group)
-    arow = np.repeat(A, w.T)[s["rows"]]
+    sm = s["small"]
+    if w.advantage == "gae":
+        A, _ = oracle.gae(sm["rewards"], sm["values"], sm["lengths"], w.gamma, w.lam)
+        arow = A.reshape(-1)[s["rows"]]
+    else:
+        arow = np.repeat(oracle.group_advantages(sm["rewards"], w.group), w.T)[s["rows"]]
     return oracle.policy_loss(s["host"], w.dtype, w.V, s["ids"], s["mask"], arow,
-                              logp_old=s["lo"], ref_logp=s["rf"], eps=w.eps, beta=w.beta,
-                              c_ent=w.c_ent, grad_scale=1.0, threads=threads)
+                              logp_old=s["lo"], ref_logp=s["rf"] if w.beta != 0 else None,
+                              eps=w.eps, beta=w.beta, c_ent=w.c_ent, grad_scale=1.0,
+                              threads=threads)
 
 
 def _sample_text(w, s, threads, extra=""):
     n, nv = s["rows"].size, int(s["mask"].sum())
-    return (f"{n} rows spread evenly over the {w.R}-row batch ({nv} valid, V={w.V} bf16){extra}; "
-            f"fp64 C oracle on {threads} host threads")
+    return (f"{n} rows spread evenly over the {w.R}-row batch ({nv} valid, V={w.V} {w.dtype})"
+            f"{extra}; fp64 C oracle on {threads} host threads")
 
 
 def cpu_baseline(w, dev_logits=None, budget_s=15.0, n_rows=512):
@@ -461,9 +513,8 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    from ppo_policy_loss_gb300 import synth
 
-    w = synth.WORKLOADS[WORKLOAD]
+    w = workload_for(args)
     threads = oracle.default_threads()
     # size each step so that warm-up + timed steps take about args.ref_seconds
     probe = cpu_sample(w, sample_rows(w, 64))
@@ -483,8 +534,8 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": WORKLOAD, "B": w.B, "T": w.T, "V": w.V,
-                      "step_sample_rows": int(s["rows"].size)},
+           "config": {"workload": f"{args.workload}: {DESCRIBE.get(args.workload, '')}",
+                      "B": w.B, "T": w.T, "V": w.V, "step_sample_rows": int(s["rows"].size)},
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                             "sample": "each step: " + _sample_text(w, s, threads)},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -498,12 +549,15 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["tiny_grpo", "qwen3_0p6b_grpo", "long_seq_grpo", "ppo_gae",
+                             "large_grpo"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seqs", type=int, default=0,
-                    help="profiling only: keep the first SEQS sequences (whole groups)")
+                    help="profiling only: keep the first SEQS sequences")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -74,10 +74,14 @@ def test_reference_arm_non_zero_rank_exits_quietly():
     assert out.returncode == 0 and out.stdout.strip() == ""
 
 
-def test_traffic_record_ignored_when_kernel_changed(tmp_path, monkeypatch):
+def test_traffic_record_ignored_when_kernel_changed(tmp_path):
     f = tmp_path / "t.txt"
     f.write_text("kernel_sha: 0000\ndram_bytes_per_launch: 123\n")
-    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    assert bench.recorded_traffic() is None
+    assert bench.recorded_traffic(path=str(f)) is None
     f.write_text(f"kernel_sha: {bench.kernel_sha()}\ndram_bytes_per_launch: 123\n")
-    assert bench.recorded_traffic() == 123.0
+    assert bench.recorded_traffic(path=str(f)) == 123.0
+
+
+def test_alg_bytes_ppo_counts_per_token_advantages_and_no_reference():
+    w = synth.WORKLOADS["ppo_gae"]
+    assert bench.alg_bytes(w, w.R) == 2 * w.R * w.V * 2 + w.R * 21 + w.R * 4

@@ -212,27 +212,31 @@ def row_stats(logits: np.ndarray, dtype, V: int, ids: np.ndarray, mask: np.ndarr
     return lse, logp, ent
 
 
-def surrogate(r, A, eps):
-    """Clipped surrogate pg = min(r A, clip(r, 1 - eps, 1 + eps) A) and its
+def surrogate(r, A, eps, eps_high=None):
+    """Clipped surrogate pg = min(r A, clip(r, 1 - eps, 1 + eps_high) A) and its
     derivative with respect to logp (r = exp(logp - logp_old), dr/dlogp = r).
 
     Page: ainews.cool RL.cu article, "PPO 更新内核" bullet (clipped surrogate
-    objective).  Where the two branches differ, the smaller is the clipped one
-    exactly when (A > 0 and r > 1 + eps) or (A < 0 and r < 1 - eps); its
-    derivative is 0 there and r A elsewhere (ties, including r = 1 +/- eps,
-    take r A).  Returns (pg, dpg, clipped).
+    objective).  eps_high (default eps) is the upper clip offset; a larger
+    upper than lower offset is the asymmetric ("clip-higher") variant.  Where
+    the two branches differ, the smaller is the clipped one exactly when
+    (A > 0 and r > 1 + eps_high) or (A < 0 and r < 1 - eps); its derivative
+    is 0 there and r A elsewhere (ties, including r on a boundary, take r A).
+    Returns (pg, dpg, clipped).
     """
+    hi = 1.0 + (eps if eps_high is None else eps_high)
+    lo = 1.0 - eps
     r = np.asarray(r, np.float64)
     A = np.asarray(A, np.float64)
     s1 = r * A
-    s2 = np.clip(r, 1.0 - eps, 1.0 + eps) * A
+    s2 = np.clip(r, lo, hi) * A
     pg = np.minimum(s1, s2)
-    clipped = ((A > 0) & (r > 1.0 + eps)) | ((A < 0) & (r < 1.0 - eps))
+    clipped = ((A > 0) & (r > hi)) | ((A < 0) & (r < lo))
     dpg = np.where(clipped, 0.0, r * A)
     return pg, dpg, clipped
 
 
-def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent):
+def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent, eps_high=None):
     """Per-token PPO/GRPO objective J_t and its derivative g_t = dJ_t/dlogp_t.
 
     Page: ainews.cool RL.cu article, "PPO 更新内核" bullet (clipped surrogate,
@@ -251,7 +255,7 @@ def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent):
     A = np.where(m, np.asarray(adv, np.float64), 0.0)
     r = np.exp(logp - np.where(m, logp_old, 0.0)) if logp_old is not None else np.ones_like(logp)
     r = np.where(m, r, 1.0)
-    pg, dpg, clipped = surrogate(r, A, eps)
+    pg, dpg, clipped = surrogate(r, A, eps, eps_high)
     if ref_logp is not None:
         d = np.where(m, np.asarray(ref_logp, np.float64) - logp, 0.0)
         kl = np.exp(d) - d - 1.0
@@ -266,20 +270,65 @@ def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent):
     return dict(r=z(r), pg=z(pg), kl=z(kl), H=H, J=z(J), g=z(g), clipped=m & clipped)
 
 
+AGGREGATIONS = ("token_mean", "seq_mean_token_mean", "seq_mean_token_sum", "token_sum_norm")
+
+
+def loss_weights(mask, T, agg="token_mean", agg_norm=None):
+    """Weight w_t of each token in loss = -sum_t w_t J_t (0 on masked tokens).
+
+    The pages name the masked loss only as the PPO/GRPO objective; the four
+    aggregations in use for it are:
+      token_mean          w = 1 / N                  (one mean over all tokens)
+      seq_mean_token_mean w = 1 / (B' L_b)           (mean over sequences of
+                                                      each sequence's token mean)
+      seq_mean_token_sum  w = 1 / B'                 (mean over sequences of
+                                                      each sequence's token sum)
+      token_sum_norm      w = 1 / agg_norm           (token sum over a fixed
+                                                      normaliser, e.g. B * T_max)
+    L_b = valid tokens of sequence b (row b*T + t); B' = sequences with L_b > 0.
+    """
+    m = np.asarray(mask, dtype=np.uint8).reshape(-1) != 0
+    w = np.zeros(m.size)
+    if agg == "token_mean":
+        N = int(m.sum())
+        w[m] = 1.0 / N if N else 0.0
+    elif agg in ("seq_mean_token_mean", "seq_mean_token_sum"):
+        L = m.reshape(-1, T).sum(axis=1)
+        Bp = int((L > 0).sum())
+        Lrow = np.repeat(L, T)
+        if agg == "seq_mean_token_mean":
+            w[m] = 1.0 / (Bp * Lrow[m])
+        else:
+            w[m] = 1.0 / Bp
+    elif agg == "token_sum_norm":
+        w[m] = 1.0 / float(agg_norm)
+    else:
+        raise ValueError(agg)
+    return w
+
+
 def loss_from_stats(logp, ent, mask, adv_row, logp_old=None, ref_logp=None, eps=0.2,
-                    beta=0.0, c_ent=0.0):
+                    beta=0.0, c_ent=0.0, eps_high=None, agg="token_mean", T=None,
+                    agg_norm=None):
     """Loss and monitoring statistics from per-row (logp, H) (fp64, math.fsum sums).
 
-    loss = -(1/N) sum_t m_t J_t; pg_term, kl_term, ent_term the masked means of
-    pg, kl and H; n_clipped the tokens whose surrogate gradient the clip cuts.
-    N = 0 gives zeros.  Also returns the per-token arrays of token_objective.
+    loss = -sum_t w_t J_t with the weights of ``loss_weights`` (token_mean:
+    -(1/N) sum_t m_t J_t); pg_term, kl_term, ent_term are the token means of
+    pg, kl and H whatever the aggregation; n_clipped the tokens whose
+    surrogate gradient the clip cuts.  N = 0 gives zeros.  Also returns the
+    per-token arrays of token_objective and the weights.
     """
     m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
     N = count(m)
-    obj = token_objective(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent)
+    obj = token_objective(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent, eps_high)
     mb = m.astype(bool)
+    T = m.size if T is None else T
+    w = loss_weights(m, T, agg, agg_norm) if N else np.zeros(m.size)
     if N > 0:
-        loss = -math.fsum(obj["J"][mb]) / N
+        if agg == "token_mean":
+            loss = -math.fsum(obj["J"][mb]) / N
+        else:
+            loss = -math.fsum((w * obj["J"])[mb])
         pg_term = math.fsum(obj["pg"][mb]) / N
         kl_term = math.fsum(obj["kl"][mb]) / N
         ent_term = math.fsum(obj["H"][mb]) / N
@@ -288,12 +337,13 @@ def loss_from_stats(logp, ent, mask, adv_row, logp_old=None, ref_logp=None, eps=
     n_clipped = int(obj["clipped"].sum())
     return dict(loss=loss, pg_term=pg_term, kl_term=kl_term, ent_term=ent_term, n_tokens=N,
                 n_clipped=n_clipped, clip_frac=(n_clipped / N if N else 0.0),
-                logp=np.where(mb, logp, 0.0), entropy=np.where(mb, ent, 0.0), **obj)
+                logp=np.where(mb, logp, 0.0), entropy=np.where(mb, ent, 0.0), weights=w, **obj)
 
 
 def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=None,
                 eps=0.2, beta=0.0, c_ent=0.0, grad_scale=1.0, grad_rows=None,
-                out_dtype=None, threads=None):
+                out_dtype=None, threads=None, eps_high=None, agg="token_mean", T=None,
+                agg_norm=None):
     """The whole fused step on CPU: loss, statistics, per-row outputs and dlogits.
 
     ``adv_row`` is the advantage of each row (a per-sequence advantage already
@@ -302,8 +352,9 @@ def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=No
     is returned in ``out_dtype`` (default: the logits' format) as rows
     [len(grad_rows), V].
 
-    Loss = -(1/N) sum_t m_t J_t; N = 0 gives loss 0 and zero gradients.
-    dz_v = grad_scale (m_t / N) [ g_t (p_v - [v = y_t]) + c_ent p_v (ln p_v + H_t) ]
+    Loss = -sum_t w_t J_t (token_mean: w_t = m_t / N); N = 0 gives loss 0 and
+    zero gradients.
+    dz_v = grad_scale w_t [ g_t (p_v - [v = y_t]) + c_ent p_v (ln p_v + H_t) ]
     (d logp / dz_v = [v = y] - p_v and dH / dz_v = -p_v (ln p_v + H)).
     """
     lg = np.ascontiguousarray(logits)
@@ -311,13 +362,13 @@ def policy_loss(logits, dtype, V, ids, mask, adv_row, logp_old=None, ref_logp=No
     m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
     ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
     lse, logp, ent = row_stats(lg, dtype, V, ids, m, threads)
-    out = loss_from_stats(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent)
+    out = loss_from_stats(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent,
+                          eps_high, agg, T, agg_norm)
     out["lse"] = lse
     if grad_rows is not False:
-        N = out["n_tokens"]
         rows = np.arange(n_rows, dtype=np.int64) if grad_rows is None else \
             np.ascontiguousarray(grad_rows, dtype=np.int64)
-        scale = np.where(m[rows] != 0, grad_scale / N if N else 0.0, 0.0)
+        scale = np.where(m[rows] != 0, grad_scale * out["weights"][rows], 0.0)
         out["grad_rows"] = rows
         out["dlogits"] = dlogits_rows(lg, dtype, V, ids, rows, lse[rows], ent[rows],
                                       out["g"][rows], scale, c_ent,

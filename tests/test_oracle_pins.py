@@ -256,9 +256,9 @@ def test_gae_constant_delta_geometric():
 
 
 # ----------------------------------------------------------------------------- objective
-def _golden_clip():
+def _golden_clip(name="clip_cases.txt"):
     rows = []
-    with open(os.path.join(GOLDEN, "clip_cases.txt")) as f:
+    with open(os.path.join(GOLDEN, name)) as f:
         for line in f:
             line = line.strip()
             if line and not line.startswith("#"):
@@ -270,6 +270,14 @@ def test_surrogate_hand_table():
     tab = _golden_clip()
     A, r, pg, dpg, clipped = tab.T
     got_pg, got_dpg, got_clipped = oracle.surrogate(r, A, 0.2)
+    np.testing.assert_allclose(got_pg, pg, atol=1e-15)
+    np.testing.assert_allclose(got_dpg, dpg, atol=1e-15)
+    assert np.array_equal(got_clipped, clipped.astype(bool))
+
+
+def test_surrogate_clip_higher_hand_table():
+    A, r, pg, dpg, clipped = _golden_clip("clip_higher_cases.txt").T
+    got_pg, got_dpg, got_clipped = oracle.surrogate(r, A, 0.2, 0.28)
     np.testing.assert_allclose(got_pg, pg, atol=1e-15)
     np.testing.assert_allclose(got_dpg, dpg, atol=1e-15)
     assert np.array_equal(got_clipped, clipped.astype(bool))
@@ -407,3 +415,73 @@ def test_dlogits_rounding_to_bf16_is_single_rounding():
     d64 = oracle.policy_loss(z, "f64", 64, ids, mask, adv, out_dtype="f64", **kw)["dlogits"]
     d16 = oracle.policy_loss(z, "f64", 64, ids, mask, adv, out_dtype="bf16", **kw)["dlogits"]
     assert np.array_equal(d16, oracle.encode(d64, "bf16"))
+
+
+# ----------------------------------------------------------------------------- aggregations
+def _seq_problem(seed, B=6, T=7, V=11, lengths=None):
+    rng = np.random.default_rng(seed)
+    z = rng.normal(0, 1.5, (B * T, V))
+    ids = rng.integers(0, V, B * T)
+    L = rng.integers(0, T + 1, B) if lengths is None else np.asarray(lengths)
+    mask = (np.arange(T)[None, :] < L[:, None]).astype(np.uint8).reshape(-1)
+    adv = np.repeat(rng.normal(0, 1, B), T)
+    _, logp0, _ = oracle.row_stats(z, "f64", V, ids, mask, threads=1)
+    lo = logp0 + rng.normal(0, 0.1, B * T)
+    rf = logp0 + rng.normal(0, 0.2, B * T)
+    return z, ids, mask, adv, lo, rf, L
+
+
+def _loss(z, ids, mask, adv, lo, rf, T, agg, agg_norm=None, **kw):
+    return oracle.policy_loss(z, "f64", z.shape[1], ids, mask, adv, logp_old=lo, ref_logp=rf,
+                              eps=0.2, beta=0.05, c_ent=0.02, agg=agg, T=T, agg_norm=agg_norm,
+                              grad_rows=False, **kw)["loss"]
+
+
+def test_token_sum_over_N_is_token_mean():
+    z, ids, mask, adv, lo, rf, L = _seq_problem(40)
+    N = int(mask.sum())
+    a = _loss(z, ids, mask, adv, lo, rf, 7, "token_mean")
+    b = _loss(z, ids, mask, adv, lo, rf, 7, "token_sum_norm", agg_norm=N)
+    assert abs(a - b) < 1e-13
+
+
+def test_sequence_means_with_equal_lengths_reduce_to_token_mean():
+    z, ids, mask, adv, lo, rf, L = _seq_problem(41, lengths=[5, 5, 5, 5, 5, 5])
+    a = _loss(z, ids, mask, adv, lo, rf, 7, "token_mean")
+    b = _loss(z, ids, mask, adv, lo, rf, 7, "seq_mean_token_mean")
+    c = _loss(z, ids, mask, adv, lo, rf, 7, "seq_mean_token_sum")
+    assert abs(a - b) < 1e-13
+    assert abs(c - 5 * a) < 1e-12
+
+
+def test_sequence_mean_ignores_empty_sequences_and_weights_each_sequence_equally():
+    # one sequence alone gives its own token mean; adding an empty sequence changes nothing;
+    # two sequences give the plain average of their two token means
+    z, ids, mask, adv, lo, rf, L = _seq_problem(42, B=3, lengths=[3, 0, 6])
+    only0 = mask.copy().reshape(3, 7)
+    only0[2] = 0
+    only2 = mask.copy().reshape(3, 7)
+    only2[0] = 0
+    m0 = _loss(z, ids, only0.reshape(-1), adv, lo, rf, 7, "token_mean")
+    m2 = _loss(z, ids, only2.reshape(-1), adv, lo, rf, 7, "token_mean")
+    both = _loss(z, ids, mask, adv, lo, rf, 7, "seq_mean_token_mean")
+    assert abs(both - (m0 + m2) / 2) < 1e-13
+    assert abs(_loss(z, ids, only0.reshape(-1), adv, lo, rf, 7, "seq_mean_token_mean") - m0) < 1e-13
+
+
+@pytest.mark.parametrize("agg", oracle.AGGREGATIONS)
+def test_dlogits_central_differences_every_aggregation(agg):
+    z, ids, mask, adv, lo, rf, L = _seq_problem(43, B=4, T=3, V=5, lengths=[3, 1, 0, 2])
+    kw = dict(eps=0.2, eps_high=0.3, beta=0.07, c_ent=0.03, logp_old=lo, ref_logp=rf, agg=agg,
+              T=3, agg_norm=9.0)
+    out = oracle.policy_loss(z, "f64", 5, ids, mask, adv, grad_scale=1.0, out_dtype="f64", **kw)
+    h = 1e-6
+    fd = np.zeros_like(z)
+    for i in range(z.shape[0]):
+        for v in range(5):
+            zp, zm = z.copy(), z.copy()
+            zp[i, v] += h
+            zm[i, v] -= h
+            fd[i, v] = (oracle.policy_loss(zp, "f64", 5, ids, mask, adv, grad_rows=False, **kw)["loss"]
+                        - oracle.policy_loss(zm, "f64", 5, ids, mask, adv, grad_rows=False, **kw)["loss"]) / (2 * h)
+    np.testing.assert_allclose(out["dlogits"], fd, rtol=1e-6, atol=1e-9)

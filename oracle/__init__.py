@@ -406,3 +406,47 @@ def dlogits_rows(logits, dtype, V, ids, rows, lse, ent, g, scale, c_ent, out_dty
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(work, range(0, rows.size, step)))
     return out
+
+
+# --------------------------------------------------------------------------- critic
+def value_loss(values, values_old, returns, mask, clip_eps=None, grad_scale=1.0):
+    """PPO clipped value (critic) loss and its gradient with respect to the values.
+
+    Page: ainews.cool RL.cu article, section "技术深度解析": the policy (actor)
+    and value (critic) networks of the PPO loop; the value loss itself is not
+    written there, so this is the standard clipped form:
+        vc  = v_old + clip(v - v_old, -clip_eps, clip_eps)
+        L_t = 1/2 max((v - ret)^2, (vc - ret)^2)          (unclipped if no v_old
+                                                           or clip_eps is None)
+        loss = (1/N) sum_t m_t L_t
+    dL/dv_t = grad_scale (m_t / N) * ((v - ret) where the unclipped square is
+    the larger or equal, else (vc - ret) [|v - v_old| <= clip_eps]); the clip
+    is inclusive at the boundary.  N = 0 gives zeros.
+    Returns dict(loss, dvalues, n_tokens, n_clipped, clip_frac, mean_abs_err);
+    n_clipped counts tokens where the clipped square is strictly larger.
+    """
+    v = np.asarray(values, np.float64).reshape(-1)
+    ret = np.asarray(returns, np.float64).reshape(-1)
+    m = np.asarray(mask).reshape(-1) != 0
+    N = int(m.sum())
+    u = (v - ret) ** 2
+    if values_old is not None and clip_eps is not None:
+        vo = np.asarray(values_old, np.float64).reshape(-1)
+        vc = vo + np.clip(v - vo, -clip_eps, clip_eps)
+        c = (vc - ret) ** 2
+        inside = np.abs(v - vo) <= clip_eps
+        use_c = c > u
+        grad = np.where(use_c, (vc - ret) * inside, v - ret)
+        L = 0.5 * np.maximum(u, c)
+    else:
+        use_c = np.zeros(v.size, bool)
+        grad = v - ret
+        L = 0.5 * u
+    if N == 0:
+        return dict(loss=0.0, dvalues=np.zeros(v.size), n_tokens=0, n_clipped=0, clip_frac=0.0,
+                    mean_abs_err=0.0)
+    loss = math.fsum(L[m]) / N
+    dvalues = np.where(m, grad_scale * grad / N, 0.0)
+    n_clipped = int((use_c & m).sum())
+    return dict(loss=loss, dvalues=dvalues, n_tokens=N, n_clipped=n_clipped,
+                clip_frac=n_clipped / N, mean_abs_err=math.fsum(np.abs(v - ret)[m]) / N)

@@ -485,3 +485,40 @@ def test_dlogits_central_differences_every_aggregation(agg):
             fd[i, v] = (oracle.policy_loss(zp, "f64", 5, ids, mask, adv, grad_rows=False, **kw)["loss"]
                         - oracle.policy_loss(zm, "f64", 5, ids, mask, adv, grad_rows=False, **kw)["loss"]) / (2 * h)
     np.testing.assert_allclose(out["dlogits"], fd, rtol=1e-6, atol=1e-9)
+
+
+# ----------------------------------------------------------------------------- critic
+def test_value_loss_hand_table():
+    v, vo, ret, L, dv = _golden_clip("value_clip_cases.txt").T
+    n = v.size
+    o = oracle.value_loss(v, vo, ret, np.ones(n), clip_eps=0.2, grad_scale=n)
+    assert abs(o["loss"] - L.mean()) < 1e-15
+    np.testing.assert_allclose(o["dvalues"], dv, atol=1e-15)
+    assert o["n_clipped"] == 1
+
+
+def test_value_loss_unclipped_is_half_mse():
+    rng = np.random.default_rng(50)
+    v, ret = rng.normal(0, 1, 300), rng.normal(0, 1, 300)
+    m = (rng.random(300) < 0.7).astype(np.uint8)
+    o = oracle.value_loss(v, None, ret, m)
+    assert abs(o["loss"] - 0.5 * np.mean((v - ret)[m == 1] ** 2)) < 1e-14
+    # a clip range wider than every step changes nothing
+    o2 = oracle.value_loss(v, v + 0.01, ret, m, clip_eps=10.0)
+    assert abs(o2["loss"] - o["loss"]) < 1e-15 and o2["n_clipped"] == 0
+
+
+def test_value_loss_central_differences():
+    rng = np.random.default_rng(51)
+    v, vo, ret = rng.normal(0, 1, 40), rng.normal(0, 1, 40), rng.normal(0, 1, 40)
+    m = (rng.random(40) < 0.8).astype(np.uint8)
+    keep = (np.abs(np.abs(v - vo) - 0.3) > 1e-3)  # away from the clip kinks
+    v, vo, ret, m = v[keep], vo[keep], ret[keep], m[keep]
+    o = oracle.value_loss(v, vo, ret, m, clip_eps=0.3)
+    h = 1e-6
+    for i in range(v.size):
+        vp, vm = v.copy(), v.copy()
+        vp[i] += h
+        vm[i] -= h
+        fd = (oracle.value_loss(vp, vo, ret, m, 0.3)["loss"] - oracle.value_loss(vm, vo, ret, m, 0.3)["loss"]) / (2 * h)
+        assert abs(fd - o["dvalues"][i]) < 1e-7

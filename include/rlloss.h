@@ -64,9 +64,20 @@ typedef enum {
 typedef enum { RL_F32 = 0, RL_BF16 = 1, RL_F16 = 2 } rl_dtype;
 
 typedef enum {
-  RL_ADV_PER_SEQ = 0,    /* adv[B]: one advantage per sequence (GRPO) */
-  RL_ADV_PER_TOKEN = 1   /* adv[B*T]: one advantage per token (PPO-GAE) */
+  RL_ADV_PER_SEQ = 0,      /* adv[B]: one advantage per sequence (GRPO) */
+  RL_ADV_PER_TOKEN = 1,    /* adv[B*T]: one advantage per token (PPO-GAE) */
+  RL_ADV_GROUP_REWARDS = 2 /* adv[B] holds the sequences' REWARDS; the loss launch
+                              computes the group-relative advantages itself
+                              (rl_policy_loss_fwd_bwd_ex only) */
 } rl_adv_layout;
+
+/* How token objectives are averaged into the loss (loss = -sum_t w_t J_t). */
+typedef enum {
+  RL_AGG_TOKEN_MEAN = 0,          /* w = 1/N: one mean over all valid tokens */
+  RL_AGG_SEQ_MEAN_TOKEN_MEAN = 1, /* w = 1/(B' L_b): mean over sequences of their token means */
+  RL_AGG_SEQ_MEAN_TOKEN_SUM = 2,  /* w = 1/B': mean over sequences of their token sums */
+  RL_AGG_TOKEN_SUM_NORM = 3       /* w = 1/agg_norm: token sum over a fixed normaliser */
+} rl_loss_agg;
 
 /* Device-error bits of rl_loss_stats.device_error and of the workspace word. */
 #define RL_DEVERR_ID_RANGE 1u
@@ -199,6 +210,70 @@ rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Every option of the fused loss, for rl_policy_loss_fwd_bwd_ex.  Fields not
+ * listed here mean what they mean for rl_policy_loss_fwd_bwd.  Start from
+ * rl_policy_loss_desc_init() so that new fields keep their defaults.
+ *
+ * Advantages (adv, adv_layout): with RL_ADV_GROUP_REWARDS, adv[B] holds each
+ * sequence's reward and the kernel computes, per row, the group-relative
+ * advantage A_b = (R_b - mean_g) / (std_g + std_eps) of its group of
+ * group_size consecutive sequences (ddof 0 or 1), in fp64 exactly as
+ * rl_group_advantages does: reward normalisation and the loss in one launch,
+ * as the pages' PPO update kernel fuses advantage estimation into the update
+ * (ainews.cool RL.cu article, "PPO 更新内核" bullet).
+ *
+ * Clip (eps, eps_high): pg = min(r A, clamp(r, 1 - eps, 1 + eps_high) A);
+ * eps_high < 0 means eps_high = eps.  A larger eps_high is the asymmetric
+ * ("clip-higher") variant.
+ *
+ * Aggregation (agg, agg_norm): loss = -sum_t w_t J_t and dz scales by
+ * grad_scale * w_t, with w_t from rl_loss_agg; L_b = valid tokens of sequence
+ * b, B' = sequences with L_b > 0; agg_norm (> 0) is used by
+ * RL_AGG_TOKEN_SUM_NORM only.  The statistics pg_term, kl_term, ent_term and
+ * clip_frac stay token means (over N) whatever the aggregation.
+ */
+typedef struct {
+  const void* logits;
+  rl_dtype dtype;
+  long long B, T, V, ld;
+  const long long* ids;
+  const float* logp_old;         /* nullable */
+  const float* ref_logp;         /* nullable iff beta == 0 */
+  const unsigned char* mask;
+  const float* adv;
+  rl_adv_layout adv_layout;
+  int group_size;                /* RL_ADV_GROUP_REWARDS: G, B % G == 0, G > ddof */
+  int ddof;                      /* RL_ADV_GROUP_REWARDS: 0 or 1 (default 1) */
+  double std_eps;                /* RL_ADV_GROUP_REWARDS: default 1e-4 */
+  float eps;                     /* default 0.2 */
+  float eps_high;                /* default -1 (= eps) */
+  float beta, c_ent;             /* default 0 */
+  float grad_scale;              /* default 1 */
+  rl_loss_agg agg;               /* default RL_AGG_TOKEN_MEAN */
+  double agg_norm;               /* RL_AGG_TOKEN_SUM_NORM only */
+  void* dlogits;                 /* nullable: forward only */
+  float* logp_out;               /* nullable */
+  float* entropy_out;            /* nullable */
+  rl_loss_stats* stats_dev;
+  void* workspace;
+  size_t workspace_bytes;
+} rl_policy_loss_desc;
+
+/* Fill *desc with the defaults above (all pointers NULL, sizes 0). */
+void rl_policy_loss_desc_init(rl_policy_loss_desc* desc);
+
+/*
+ * The fused loss with every option of rl_policy_loss_desc, in one launch.
+ * rl_policy_loss_fwd_bwd is this call with the defaults (token mean,
+ * symmetric clip, advantages given).  Errors as rl_policy_loss_fwd_bwd, plus
+ * RL_ERR_NULL for a NULL desc, RL_ERR_DTYPE for an unknown aggregation or
+ * layout, RL_ERR_SHAPE for a group size that does not divide B (or is not
+ * above ddof), RL_ERR_ARG for ddof not 0/1, a negative/NaN std_eps, a NaN
+ * eps_high or a non-positive agg_norm with RL_AGG_TOKEN_SUM_NORM.
+ */
+rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* desc, void* stream);
+
+/*
  * rl_policy_loss_fwd_bwd without a caller-provided workspace, for callers
  * that cannot allocate device memory: for example a plug-in inside a host
  * framework that owns the GPU allocator and forbids raw cudaMalloc, or a
@@ -234,6 +309,44 @@ rl_status rl_policy_loss_fwd_bwd_noalloc(const void* logits, rl_dtype dtype,
                                          float eps, float beta, float c_ent, float grad_scale,
                                          void* dlogits, float* logp_out, float* entropy_out,
                                          rl_loss_stats* stats_dev, void* stream);
+
+/*
+ * Scalar results of rl_value_loss_fwd_bwd (device memory, written at the end).
+ *   loss = (1/N) sum_t m_t L_t;  clip_frac = n_clipped / N;
+ *   mean_abs_err = (1/N) sum_t m_t |v_t - ret_t|.
+ */
+typedef struct {
+  double loss;
+  double clip_frac;
+  double mean_abs_err;
+  long long n_tokens;
+  long long n_clipped;   /* tokens where the clipped square is strictly larger */
+} rl_value_stats;
+
+/*
+ * PPO clipped value (critic) loss and its gradient with respect to the values.
+ * The pages give the PPO loop a critic (ainews.cool RL.cu article, section
+ * "技术深度解析", actor/critic bullet); this is the standard clipped form:
+ *   vc  = v_old + clamp(v - v_old, -clip_eps, clip_eps)
+ *   L_t = 1/2 max((v - ret)^2, (vc - ret)^2)     (1/2 (v - ret)^2 unclipped)
+ *   loss = (1/N) sum_t m_t L_t,  N = number of nonzero mask bytes
+ *   dvalues_t = grad_scale (m_t / N) * (v - ret)        where the unclipped
+ *               square is the larger or equal, else (vc - ret) when
+ *               |v - v_old| <= clip_eps, else 0          (inclusive clip)
+ *   values, returns : float[n], device, read only (returns from
+ *                     rl_gae_reverse_scan);
+ *   values_old      : float[n] or NULL; NULL or clip_eps < 0 means unclipped;
+ *   mask            : uint8[n], nonzero = valid token;
+ *   dvalues         : float[n] written (0 on masked tokens), or NULL;
+ *   stats_dev       : one rl_value_stats in device memory.
+ * fp32 per token, fp64 fixed-order reduction; one launch of one CTA.
+ * Errors: RL_ERR_SHAPE (n < 0), RL_ERR_NULL, RL_ERR_ARG (NaN clip_eps,
+ * non-finite grad_scale).  N = 0 gives zeros.
+ */
+rl_status rl_value_loss_fwd_bwd(const float* values, const float* values_old,
+                                const float* returns, const unsigned char* mask, long long n,
+                                float clip_eps, float grad_scale, float* dvalues,
+                                rl_value_stats* stats_dev, void* stream);
 
 /*
  * The launch shape rl_policy_loss_fwd_bwd would use on the current device for

@@ -20,15 +20,20 @@ from ._build import LIB_PATH, build
 RL_OK, RL_ERR_NULL, RL_ERR_SHAPE, RL_ERR_DTYPE, RL_ERR_ALIGN, RL_ERR_ALIAS, \
     RL_ERR_WORKSPACE, RL_ERR_ID_RANGE, RL_ERR_TIMEOUT, RL_ERR_CUDA, RL_ERR_ARG = range(11)
 RL_F32, RL_BF16, RL_F16 = 0, 1, 2
-RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN = 0, 1
+RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN, RL_ADV_GROUP_REWARDS = 0, 1, 2
+RL_AGG_TOKEN_MEAN, RL_AGG_SEQ_MEAN_TOKEN_MEAN, RL_AGG_SEQ_MEAN_TOKEN_SUM, RL_AGG_TOKEN_SUM_NORM = \
+    0, 1, 2, 3
+AGGREGATIONS = {"token_mean": 0, "seq_mean_token_mean": 1, "seq_mean_token_sum": 2,
+                "token_sum_norm": 3}
 RL_DEVERR_ID_RANGE, RL_DEVERR_TIMEOUT = 1, 2
 
 DTYPES = {"f32": RL_F32, "bf16": RL_BF16, "f16": RL_F16}
 
 __all__ = [
     "rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_workspace_size",
-    "rl_policy_loss_fwd_bwd", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
-    "rl_read_device_status",
+    "rl_policy_loss_fwd_bwd", "rl_policy_loss_fwd_bwd_ex", "rl_policy_loss_desc_init",
+    "rl_policy_loss_desc", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
+    "rl_read_device_status", "rl_value_loss_fwd_bwd", "rl_value_stats", "value_stats_from_bytes",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -47,7 +52,28 @@ class rl_loss_stats(ctypes.Structure):
                 ("reserved", ctypes.c_int)]
 
 
+class rl_policy_loss_desc(ctypes.Structure):
+    _fields_ = [("logits", ctypes.c_void_p), ("dtype", ctypes.c_int),
+                ("B", ctypes.c_longlong), ("T", ctypes.c_longlong), ("V", ctypes.c_longlong),
+                ("ld", ctypes.c_longlong), ("ids", ctypes.c_void_p), ("logp_old", ctypes.c_void_p),
+                ("ref_logp", ctypes.c_void_p), ("mask", ctypes.c_void_p), ("adv", ctypes.c_void_p),
+                ("adv_layout", ctypes.c_int), ("group_size", ctypes.c_int), ("ddof", ctypes.c_int),
+                ("std_eps", ctypes.c_double), ("eps", ctypes.c_float), ("eps_high", ctypes.c_float),
+                ("beta", ctypes.c_float), ("c_ent", ctypes.c_float), ("grad_scale", ctypes.c_float),
+                ("agg", ctypes.c_int), ("agg_norm", ctypes.c_double), ("dlogits", ctypes.c_void_p),
+                ("logp_out", ctypes.c_void_p), ("entropy_out", ctypes.c_void_p),
+                ("stats_dev", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class rl_value_stats(ctypes.Structure):
+    _fields_ = [("loss", ctypes.c_double), ("clip_frac", ctypes.c_double),
+                ("mean_abs_err", ctypes.c_double), ("n_tokens", ctypes.c_longlong),
+                ("n_clipped", ctypes.c_longlong)]
+
+
 STATS_BYTES = ctypes.sizeof(rl_loss_stats)
+VALUE_STATS_BYTES = ctypes.sizeof(rl_value_stats)
 _lib = None
 
 
@@ -70,13 +96,18 @@ def load(path: str | None = None):
                                            P, P, P, P, P, SZ, P]
     lib.rl_policy_loss_fwd_bwd_noalloc.argtypes = [P, I, LL, LL, LL, LL, P, P, P, P, P, I, F, F,
                                                    F, F, P, P, P, P, P]
+    lib.rl_policy_loss_desc_init.argtypes = [ctypes.POINTER(rl_policy_loss_desc)]
+    lib.rl_policy_loss_desc_init.restype = None
+    lib.rl_policy_loss_fwd_bwd_ex.argtypes = [ctypes.POINTER(rl_policy_loss_desc), P]
+    lib.rl_value_loss_fwd_bwd.argtypes = [P, P, P, P, LL, F, F, P, P, P]
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
     lib.rl_read_device_status.argtypes = [P, P]
     lib.rl_status_string.argtypes = [I]
     lib.rl_status_string.restype = ctypes.c_char_p
     for fn in ("rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_fwd_bwd",
-               "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
+               "rl_policy_loss_fwd_bwd_ex", "rl_policy_loss_fwd_bwd_noalloc", "rl_value_loss_fwd_bwd",
+               "rl_policy_loss_launch_shape",
                "rl_read_device_status"):
         getattr(lib, fn).restype = I
     _lib = lib
@@ -139,6 +170,18 @@ def rl_policy_loss_fwd_bwd(logits, dtype, B, T, V, ld, ids, logp_old, ref_logp, 
         _stream(stream)), "rl_policy_loss_fwd_bwd")
 
 
+def rl_policy_loss_desc_init() -> rl_policy_loss_desc:
+    """A descriptor holding the library's defaults (see rl_policy_loss_desc_init)."""
+    d = rl_policy_loss_desc()
+    load().rl_policy_loss_desc_init(ctypes.byref(d))
+    return d
+
+
+def rl_policy_loss_fwd_bwd_ex(desc: rl_policy_loss_desc, stream=None):
+    _check(load().rl_policy_loss_fwd_bwd_ex(ctypes.byref(desc), _stream(stream)),
+           "rl_policy_loss_fwd_bwd_ex")
+
+
 def rl_policy_loss_fwd_bwd_noalloc(logits, dtype, B, T, V, ld, ids, logp_old, ref_logp, mask,
                                    adv, adv_layout, eps, beta, c_ent, grad_scale, dlogits,
                                    logp_out, entropy_out, stats_dev, stream=None):
@@ -150,6 +193,19 @@ def rl_policy_loss_fwd_bwd_noalloc(logits, dtype, B, T, V, ld, ids, logp_old, re
         _ptr(mask), _ptr(adv), adv_layout, eps, beta, c_ent, grad_scale, _ptr(dlogits),
         _ptr(logp_out), _ptr(entropy_out), _ptr(stats_dev), _stream(stream)),
         "rl_policy_loss_fwd_bwd_noalloc")
+
+
+def rl_value_loss_fwd_bwd(values, values_old, returns, mask, n, clip_eps, grad_scale, dvalues,
+                          stats_dev, stream=None):
+    _check(load().rl_value_loss_fwd_bwd(_ptr(values), _ptr(values_old), _ptr(returns), _ptr(mask),
+                                        n, clip_eps, grad_scale, _ptr(dvalues), _ptr(stats_dev),
+                                        _stream(stream)), "rl_value_loss_fwd_bwd")
+
+
+def value_stats_from_bytes(raw: bytes) -> dict:
+    """Decode a host copy of one rl_value_stats record."""
+    st = rl_value_stats.from_buffer_copy(bytes(raw))
+    return {name: getattr(st, name) for name, _ in rl_value_stats._fields_}
 
 
 def rl_policy_loss_launch_shape(dtype, V, n_rows):

@@ -42,6 +42,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -91,6 +92,7 @@ struct LossSmem {
   unsigned long long xbar[2];
   float4 xpart[2][kMaxCluster * kConsumerWarps];  // (m, s, t, z_y or -inf) per warp
   long long wcount[kConsumerWarps];
+  long long wseq[kConsumerWarps];
   double wred[kConsumerWarps][5];
   int abort;
   int is_last;
@@ -112,8 +114,13 @@ struct LossArgs {
   long long R, T, V;
   long long row_bytes;  // ld * element bytes
   long long slice;      // vocabulary elements per cluster rank (V when not clustered)
-  int adv_per_token;
-  float eps, beta, c_ent, grad_scale;
+  int adv_mode;         // rl_adv_layout
+  int group_size, ddof; // RL_ADV_GROUP_REWARDS
+  double std_eps;       // RL_ADV_GROUP_REWARDS
+  float clip_lo, clip_hi;  // 1 - eps, 1 + eps_high
+  float beta, c_ent, grad_scale;
+  int agg;              // rl_loss_agg
+  double agg_w;         // RL_AGG_TOKEN_SUM_NORM: 1 / agg_norm
 };
 
 // ------------------------------------------------------------------ element formats
@@ -291,6 +298,38 @@ __device__ __forceinline__ void raise_max(float vm, ThreadStats& a) {
   }
 }
 
+// Pass-1 update with a full chunk: this thread's kVecsPerThread vectors,
+// one running-max check for all of them, then independent chains (whole warp).
+template <class E>
+__device__ __forceinline__ void accumulate_chunk(uint32_t buf, ThreadStats& a) {
+  uint4 w[kVecsPerThread];
+  float vm = kFloor;
+#pragma unroll
+  for (int q = 0; q < kVecsPerThread; ++q) {
+    w[q] = ld_shared_v4(buf + q * kConsumerThreads * 16);
+    E::clamp(w[q]);
+    vm = max_nan(vm, E::vmax(w[q]));
+  }
+  raise_max(vm, a);
+  const float2 L2 = make_float2(kLog2e, kLog2e);
+  const float2 nmL = make_float2(a.nmL, a.nmL);
+#pragma unroll
+  for (int q = 0; q < kVecsPerThread; ++q) {
+    float z[E::kVec];
+    E::unpack(w[q], z);
+    float2 s = a.s[q], t = a.t[q];
+#pragma unroll
+    for (int i = 0; i < E::kVec; i += 2) {
+      const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, nmL);
+      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      s = __fadd2_rn(s, e);
+      t = __ffma2_rn(e, x, t);
+    }
+    a.s[q] = s;
+    a.t[q] = t;
+  }
+}
+
 // Pass-1 update with one full 16-byte vector into chain q (whole warp).
 template <class E>
 __device__ __forceinline__ void accumulate_full(uint4 w, ThreadStats& a, int q) {
@@ -410,11 +449,56 @@ __device__ __forceinline__ RowScalars load_row(const LossArgs& a, long long row)
   if (row < a.R) {
     r.valid = a.mask[row] != 0;
     r.y = a.ids[row];
-    r.A = a.adv[a.adv_per_token ? row : row / a.T];
+    if (a.adv_mode != RL_ADV_GROUP_REWARDS) r.A = a.adv[a.adv_mode == RL_ADV_PER_TOKEN ? row : row / a.T];
     r.lpo = a.logp_old ? a.logp_old[row] : 0.f;
     r.rf = a.ref_logp ? a.ref_logp[row] : 0.f;
   }
   return r;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Nonzero bytes of mask[begin, begin + n), counted by one warp (every lane
+// gets the count).
+__device__ __forceinline__ int warp_count_mask(const unsigned char* m, long long n, int lane) {
+  int c = 0;
+  long long i0 = 0;
+  if (((reinterpret_cast<uintptr_t>(m)) & 15) == 0) {
+    const long long nv = n >> 4;
+    const uint4* mv = reinterpret_cast<const uint4*>(m);
+    for (long long i = lane; i < nv; i += 32) {
+      const uint4 w = __ldg(mv + i);
+      c += (__popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
+            __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u))) >> 3;
+    }
+    i0 = nv << 4;
+  }
+  for (long long i = i0 + lane; i < n; i += 32) c += m[i] != 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
+}
+
+// Group-relative advantage of sequence b from the rewards (one warp, fp64,
+// the same arithmetic as rl_group_advantages): (R_b - mean) / (std + eps).
+__device__ __forceinline__ float warp_group_advantage(const LossArgs& a, long long b, int lane) {
+  const int G = a.group_size;
+  const float* r = a.adv + (b / G) * G;
+  double sum = 0.0;
+  for (int j = lane; j < G; j += 32) sum += static_cast<double>(r[j]);
+  const double mean = warp_sum_d(sum) / G;
+  double sq = 0.0;
+  for (int j = lane; j < G; j += 32) {
+    const double d = static_cast<double>(r[j]) - mean;
+    sq += d * d;
+  }
+  const double std = sqrt(warp_sum_d(sq) / (G - a.ddof));
+  const double inv = 1.0 / (std + a.std_eps);
+  return static_cast<float>((static_cast<double>(a.adv[b]) - mean) * inv);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -525,6 +609,20 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     const long long N = cnt;
     const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
     const bool with_entropy = a.c_ent != 0.f;
+    const bool seq_agg = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN || a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM;
+    long long Bp = 0;  // sequences with at least one valid token
+    if (seq_agg) {
+      const long long nseq = a.R / a.T;
+      long long nb = 0;
+      for (long long b = warp; b < nseq; b += kConsumerWarps)
+        nb += warp_count_mask(a.mask + b * a.T, a.T, lane) > 0;
+      if (lane == 0) sm.wseq[warp] = nb;
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      for (int w = 0; w < kConsumerWarps; ++w) Bp += sm.wseq[w];
+    }
+    long long cache_b = -1;  // sequence whose length / advantage this warp holds
+    int cache_L = 0;
+    float cache_A = 0.f;
 
     double acc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // J, pg, kl, H, clipped (rank 0, thread 0)
     unsigned int err = 0;
@@ -546,6 +644,23 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       if (*abort_flag) {
         aborted = true;
         break;
+      }
+      // Per-sequence quantities, recomputed by each warp when the sequence changes.
+      const long long bseq = row / a.T;
+      if (bseq != cache_b) {
+        cache_b = bseq;
+        if (a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN)
+          cache_L = warp_count_mask(a.mask + bseq * a.T, a.T, lane);
+        if (a.adv_mode == RL_ADV_GROUP_REWARDS) cache_A = warp_group_advantage(a, bseq, lane);
+      }
+      // Loss weight of this token and the gradient scale of its row.
+      double w_row = 1.0;  // token mean: the 1/N is applied once, at the end
+      float sc_row = sc;
+      if (a.agg != RL_AGG_TOKEN_MEAN) {
+        w_row = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN ? 1.0 / (static_cast<double>(Bp) * cache_L)
+              : a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM  ? 1.0 / static_cast<double>(Bp)
+                                                     : a.agg_w;
+        sc_row = static_cast<float>(static_cast<double>(a.grad_scale) * w_row);
       }
       const long long y = rs.y;
       // Where the sampled id sits in this CTA's slice: chunk cy, vector jy of
@@ -570,9 +685,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
         const int c0 = c * kChunkElems;
         if (c0 + kChunkElems <= nelem) {
-#pragma unroll
-          for (int q = 0; q < kVecsPerThread; ++q)
-            accumulate_full<E>(ld_shared_v4(buf + q * kConsumerThreads * 16), st, q);
+          accumulate_chunk<E>(buf, st);
         } else {
 #pragma unroll
           for (int q = 0; q < kVecsPerThread; ++q) {
@@ -649,11 +762,11 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       const float logp = zv - lse;
 
       // ---- per-token objective and its derivative with respect to logp
-      const float A = rs.A;
+      const float A = a.adv_mode == RL_ADV_GROUP_REWARDS ? cache_A : rs.A;
       const float r = a.logp_old ? expf(logp - rs.lpo) : 1.f;
       const float rA = r * A;
-      const float pg = fminf(rA, fminf(fmaxf(r, 1.f - a.eps), 1.f + a.eps) * A);
-      const bool clipped = (A > 0.f && r > 1.f + a.eps) || (A < 0.f && r < 1.f - a.eps);
+      const float pg = fminf(rA, fminf(fmaxf(r, a.clip_lo), a.clip_hi) * A);
+      const bool clipped = (A > 0.f && r > a.clip_hi) || (A < 0.f && r < a.clip_lo);
       const float dpg = clipped ? 0.f : rA;
       float kl = 0.f, dkl = 0.f;
       if (a.ref_logp) {
@@ -668,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         g = logp;
       }
       if (rank == 0 && tid == 0) {
-        acc[0] += J;
+        acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(J) : w_row * J;
         acc[1] += pg;
         acc[2] += kl;
         acc[3] += H;
@@ -681,9 +794,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       // ---- pass 2: dz_v = sc [g (p_v - [v == y]) + c_ent p_v (ln p_v + H)]
       //      with x_v = z_v log2(e) - (M log2(e) + log2 S):  p_v = 2^x_v, ln p_v = x_v ln 2
       const float cL = fmaf(M, kLog2e, log2S);
-      const float a0 = sc * fmaf(a.c_ent, H, g);
-      const float a1 = sc * a.c_ent * kLn2;
-      const float gy = sc * g;
+      const float a0 = sc_row * fmaf(a.c_ent, H, g);
+      const float a1 = sc_row * a.c_ent * kLn2;
+      const float gy = sc_row * g;
       for (int c = 0; c < nchunks; ++c) {
         uint32_t slot;
         if (kStream) {
@@ -790,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         a.ws->last_status = stw;
         rl_loss_stats out;
         const double inv = N > 0 ? 1.0 / static_cast<double>(N) : 0.0;
-        out.loss = -tot[0] * inv;
+        out.loss = a.agg == RL_AGG_TOKEN_MEAN ? -tot[0] * inv : (N > 0 ? -tot[0] : 0.0);
         out.pg_term = tot[1] * inv;
         out.kl_term = tot[2] * inv;
         out.ent_term = tot[3] * inv;
@@ -973,82 +1086,110 @@ extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, lo
   return RL_OK;
 }
 
-extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, long long B,
-                                            long long T, long long V, long long ld,
-                                            const long long* ids, const float* logp_old,
-                                            const float* ref_logp, const unsigned char* mask,
-                                            const float* adv, rl_adv_layout adv_layout, float eps,
-                                            float beta, float c_ent, float grad_scale,
-                                            void* dlogits, float* logp_out, float* entropy_out,
-                                            rl_loss_stats* stats_dev, void* workspace,
-                                            size_t workspace_bytes, void* stream) {
-  const int es = elem_bytes(dtype);
+extern "C" void rl_policy_loss_desc_init(rl_policy_loss_desc* d) {
+  if (!d) return;
+  std::memset(d, 0, sizeof(*d));
+  d->dtype = RL_BF16;
+  d->adv_layout = RL_ADV_PER_SEQ;
+  d->group_size = 1;
+  d->ddof = 1;
+  d->std_eps = 1e-4;
+  d->eps = 0.2f;
+  d->eps_high = -1.f;
+  d->grad_scale = 1.f;
+  d->agg = RL_AGG_TOKEN_MEAN;
+  d->agg_norm = 1.0;
+}
+
+extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, void* stream) {
+  if (!d) return RL_ERR_NULL;
+  const int es = elem_bytes(d->dtype);
   if (es == 0) return RL_ERR_DTYPE;
-  if (adv_layout != RL_ADV_PER_SEQ && adv_layout != RL_ADV_PER_TOKEN) return RL_ERR_DTYPE;
+  if (d->adv_layout != RL_ADV_PER_SEQ && d->adv_layout != RL_ADV_PER_TOKEN &&
+      d->adv_layout != RL_ADV_GROUP_REWARDS)
+    return RL_ERR_DTYPE;
+  if (d->agg != RL_AGG_TOKEN_MEAN && d->agg != RL_AGG_SEQ_MEAN_TOKEN_MEAN &&
+      d->agg != RL_AGG_SEQ_MEAN_TOKEN_SUM && d->agg != RL_AGG_TOKEN_SUM_NORM)
+    return RL_ERR_DTYPE;
+  const long long B = d->B, T = d->T, V = d->V, ld = d->ld;
   if (B < 0 || T < 0 || V < 1 || ld < V) return RL_ERR_SHAPE;
   if (B > 0 && T > (1LL << 40) / B) return RL_ERR_SHAPE;
   const long long R = B * T;
-  if (!stats_dev) return RL_ERR_NULL;
-  if (!workspace || workspace_bytes < rl_policy_loss_workspace_size(R)) return RL_ERR_WORKSPACE;
-  if (R > 0 && (!logits || !ids || !mask || !adv)) return RL_ERR_NULL;
-  if (beta != 0.f && !ref_logp) return RL_ERR_NULL;
-  if (!finite(eps) || eps < 0.f || !finite(beta) || !finite(c_ent) || !finite(grad_scale))
+  if (!d->stats_dev) return RL_ERR_NULL;
+  if (!d->workspace || d->workspace_bytes < rl_policy_loss_workspace_size(R)) return RL_ERR_WORKSPACE;
+  if (R > 0 && (!d->logits || !d->ids || !d->mask || !d->adv)) return RL_ERR_NULL;
+  if (d->beta != 0.f && !d->ref_logp) return RL_ERR_NULL;
+  if (!finite(d->eps) || d->eps < 0.f || !finite(d->eps_high) || !finite(d->beta) ||
+      !finite(d->c_ent) || !finite(d->grad_scale))
+    return RL_ERR_ARG;
+  if (d->adv_layout == RL_ADV_GROUP_REWARDS) {
+    if (d->ddof != 0 && d->ddof != 1) return RL_ERR_ARG;
+    if (!(d->std_eps >= 0.0) || !std::isfinite(d->std_eps)) return RL_ERR_ARG;
+    if (d->group_size <= d->ddof || d->group_size < 1 || B % d->group_size != 0) return RL_ERR_SHAPE;
+  }
+  if (d->agg == RL_AGG_TOKEN_SUM_NORM && !(d->agg_norm > 0.0 && std::isfinite(d->agg_norm)))
     return RL_ERR_ARG;
   const long long row_bytes = ld * es;
   if ((row_bytes & 15) != 0) return RL_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(logits) & 15) != 0) return RL_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(dlogits) & 15) != 0) return RL_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return RL_ERR_ALIGN;
-  if (dlogits && dlogits != logits && R > 0) {
-    const uintptr_t l0 = reinterpret_cast<uintptr_t>(logits), d0 = reinterpret_cast<uintptr_t>(dlogits);
+  if ((reinterpret_cast<uintptr_t>(d->logits) & 15) != 0) return RL_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(d->dlogits) & 15) != 0) return RL_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(d->workspace) & 15) != 0) return RL_ERR_ALIGN;
+  if (d->dlogits && d->dlogits != d->logits && R > 0) {
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(d->logits);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d->dlogits);
     const uintptr_t n = static_cast<uintptr_t>(R) * static_cast<uintptr_t>(row_bytes);
     if (l0 < d0 + n && d0 < l0 + n) return RL_ERR_ALIAS;
   }
 
   Plan pl;
-  const rl_status st = plan(dtype, V, R, &pl);
+  const rl_status st = plan(d->dtype, V, R, &pl);
   if (st != RL_OK) return st;
-  const int cluster = pl.cluster, n_clusters = pl.n_clusters;
-  const long long slice = pl.slice;
 
   LossArgs args;
-  args.logits = static_cast<const unsigned char*>(logits);
-  args.dlogits = static_cast<unsigned char*>(dlogits);
-  args.ids = ids;
-  args.logp_old = logp_old;
-  args.ref_logp = ref_logp;
-  args.mask = mask;
-  args.adv = adv;
-  args.logp_out = logp_out;
-  args.entropy_out = entropy_out;
-  args.stats = stats_dev;
-  args.ws = static_cast<WsHeader*>(workspace);
-  args.partials = reinterpret_cast<WsPartial*>(static_cast<unsigned char*>(workspace) + sizeof(WsHeader));
+  args.logits = static_cast<const unsigned char*>(d->logits);
+  args.dlogits = static_cast<unsigned char*>(d->dlogits);
+  args.ids = d->ids;
+  args.logp_old = d->logp_old;
+  args.ref_logp = d->ref_logp;
+  args.mask = d->mask;
+  args.adv = d->adv;
+  args.logp_out = d->logp_out;
+  args.entropy_out = d->entropy_out;
+  args.stats = d->stats_dev;
+  args.ws = static_cast<WsHeader*>(d->workspace);
+  args.partials =
+      reinterpret_cast<WsPartial*>(static_cast<unsigned char*>(d->workspace) + sizeof(WsHeader));
   args.R = R;
   args.T = T > 0 ? T : 1;
   args.V = V;
   args.row_bytes = row_bytes;
-  args.slice = slice;
-  args.adv_per_token = adv_layout == RL_ADV_PER_TOKEN;
-  args.eps = eps;
-  args.beta = beta;
-  args.c_ent = c_ent;
-  args.grad_scale = grad_scale;
+  args.slice = pl.slice;
+  args.adv_mode = d->adv_layout;
+  args.group_size = d->group_size;
+  args.ddof = d->ddof;
+  args.std_eps = d->std_eps;
+  args.clip_lo = 1.f - d->eps;
+  args.clip_hi = 1.f + (d->eps_high < 0.f ? d->eps : d->eps_high);
+  args.beta = d->beta;
+  args.c_ent = d->c_ent;
+  args.grad_scale = d->grad_scale;
+  args.agg = d->agg;
+  args.agg_w = d->agg == RL_AGG_TOKEN_SUM_NORM ? 1.0 / d->agg_norm : 0.0;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.x = pl.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(cluster * n_clusters));
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.cluster * pl.n_clusters));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = sizeof(LossSmem);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaErrorInvalidValue;
-  switch (dtype) {
+  switch (d->dtype) {
     case RL_F32:
       e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32, true>, args)
                     : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32, false>, args);
@@ -1063,6 +1204,45 @@ extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, 
       break;
   }
   return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, long long B,
+                                            long long T, long long V, long long ld,
+                                            const long long* ids, const float* logp_old,
+                                            const float* ref_logp, const unsigned char* mask,
+                                            const float* adv, rl_adv_layout adv_layout, float eps,
+                                            float beta, float c_ent, float grad_scale,
+                                            void* dlogits, float* logp_out, float* entropy_out,
+                                            rl_loss_stats* stats_dev, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  // The fixed-argument form covers given advantages only.
+  if (adv_layout != RL_ADV_PER_SEQ && adv_layout != RL_ADV_PER_TOKEN) return RL_ERR_DTYPE;
+  rl_policy_loss_desc d;
+  rl_policy_loss_desc_init(&d);
+  d.logits = logits;
+  d.dtype = dtype;
+  d.B = B;
+  d.T = T;
+  d.V = V;
+  d.ld = ld;
+  d.ids = ids;
+  d.logp_old = logp_old;
+  d.ref_logp = ref_logp;
+  d.mask = mask;
+  d.adv = adv;
+  d.adv_layout = adv_layout;
+  d.eps = eps;
+  d.eps_high = eps;
+  d.beta = beta;
+  d.c_ent = c_ent;
+  d.grad_scale = grad_scale;
+  d.dlogits = dlogits;
+  d.logp_out = logp_out;
+  d.entropy_out = entropy_out;
+  d.stats_dev = stats_dev;
+  d.workspace = workspace;
+  d.workspace_bytes = workspace_bytes;
+  return rl_policy_loss_fwd_bwd_ex(&d, stream);
 }
 
 extern "C" rl_status rl_policy_loss_fwd_bwd_noalloc(

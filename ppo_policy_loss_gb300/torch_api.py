@@ -7,9 +7,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN, STATS_BYTES, rl_gae_reverse_scan,
-               rl_group_advantages, rl_policy_loss_fwd_bwd, rl_policy_loss_workspace_size,
-               stats_from_bytes)
+from . import (AGGREGATIONS, DTYPES, RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN,
+               STATS_BYTES, rl_gae_reverse_scan, rl_group_advantages, rl_policy_loss_desc_init,
+               VALUE_STATS_BYTES, rl_policy_loss_fwd_bwd_ex, rl_policy_loss_workspace_size,
+               rl_value_loss_fwd_bwd, stats_from_bytes, value_stats_from_bytes)
 
 _DT = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
 
@@ -52,12 +53,17 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
                 B: int, T: int, V: int | None = None, logp_old=None, ref_logp=None,
                 eps: float = 0.2, beta: float = 0.0, c_ent: float = 0.0, grad_scale: float = 1.0,
                 dlogits="new", logp_out="new", entropy_out="new", workspace=None, stats=None,
-                stream=None) -> dict:
-    """Run rl_policy_loss_fwd_bwd on [B*T, ld] logits.
+                stream=None, eps_high: float | None = None, agg: str = "token_mean",
+                agg_norm: float = 1.0, group_size: int | None = None, ddof: int = 1,
+                std_eps: float = 1e-4) -> dict:
+    """Run the fused loss on [B*T, ld] logits (rl_policy_loss_fwd_bwd_ex).
 
     ``dlogits`` / ``logp_out`` / ``entropy_out``: "new" allocates, None skips,
     a tensor is written in place (``dlogits=logits`` is the in-place form).
-    ``adv`` of B elements is per sequence, of B*T elements per token.
+    ``adv`` of B elements is per sequence, of B*T elements per token; with
+    ``group_size`` set, ``adv`` holds the B rewards and the launch computes the
+    group-relative advantages itself.  ``agg`` names the loss aggregation
+    (token_mean, seq_mean_token_mean, seq_mean_token_sum, token_sum_norm).
     Returns the output tensors and the (device) stats record; call
     ``read_stats`` for the scalars.
     """
@@ -73,9 +79,66 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
         entropy_out = torch.empty(R, dtype=torch.float32, device=dev)
     workspace = new_workspace(R, dev) if workspace is None else workspace
     stats = new_stats(dev) if stats is None else stats
-    layout = RL_ADV_PER_TOKEN if adv.numel() == R and R != B else RL_ADV_PER_SEQ
-    rl_policy_loss_fwd_bwd(logits, dtype_name(logits), B, T, V, ld, ids, logp_old, ref_logp, mask,
-                           adv, layout, eps, beta, c_ent, grad_scale, dlogits, logp_out,
-                           entropy_out, stats, workspace, workspace.numel(), stream)
+    if group_size is not None:
+        layout = RL_ADV_GROUP_REWARDS
+    else:
+        layout = RL_ADV_PER_TOKEN if adv.numel() == R and R != B else RL_ADV_PER_SEQ
+    d = rl_policy_loss_desc_init()
+    p = lambda t: t.data_ptr() if t is not None else None
+    d.logits, d.dtype, d.B, d.T, d.V, d.ld = p(logits), DTYPES[dtype_name(logits)], B, T, V, ld
+    d.ids, d.logp_old, d.ref_logp, d.mask, d.adv = p(ids), p(logp_old), p(ref_logp), p(mask), p(adv)
+    d.adv_layout = layout
+    if group_size is not None:
+        d.group_size, d.ddof, d.std_eps = group_size, ddof, std_eps
+    d.eps, d.eps_high = eps, (-1.0 if eps_high is None else eps_high)
+    d.beta, d.c_ent, d.grad_scale = beta, c_ent, grad_scale
+    d.agg, d.agg_norm = AGGREGATIONS[agg], agg_norm
+    d.dlogits, d.logp_out, d.entropy_out = p(dlogits), p(logp_out), p(entropy_out)
+    d.stats_dev, d.workspace, d.workspace_bytes = p(stats), p(workspace), workspace.numel()
+    rl_policy_loss_fwd_bwd_ex(d, stream)
     return dict(dlogits=dlogits, logp=logp_out, entropy=entropy_out, stats=stats,
                 workspace=workspace)
+
+
+def value_loss(values: torch.Tensor, returns: torch.Tensor, mask: torch.Tensor, values_old=None,
+               clip_eps: float = -1.0, grad_scale: float = 1.0, dvalues="new", stream=None):
+    """PPO clipped value loss (rl_value_loss_fwd_bwd); returns (dvalues, stats dict)."""
+    n = values.numel()
+    if isinstance(dvalues, str):
+        dvalues = torch.empty_like(values)
+    st = torch.zeros(VALUE_STATS_BYTES, dtype=torch.uint8, device=values.device)
+    rl_value_loss_fwd_bwd(values, values_old, returns, mask, n, clip_eps, grad_scale, dvalues, st,
+                          stream)
+    return dvalues, value_stats_from_bytes(st.cpu().numpy().tobytes())
+
+
+class FusedPolicyLoss(torch.autograd.Function):
+    """Autograd wrapper: forward runs the fused kernel once and keeps its
+    logits gradient; backward hands that gradient back, scaled by the
+    incoming gradient (a no-op when it is exactly 1, the usual case).
+
+    loss = FusedPolicyLoss.apply(logits, ids, mask, adv, B, T, options)
+    with ``options`` a dict of policy_loss keyword arguments (logp_old,
+    ref_logp, eps, beta, c_ent, eps_high, agg, agg_norm, group_size, ...).
+    ``options["inplace"] = True`` writes the gradient over the logits
+    (saves one logits-sized buffer; the logits are then gone).
+    """
+
+    @staticmethod
+    def forward(ctx, logits, ids, mask, adv, B, T, options=None):
+        opts = dict(options or {})
+        inplace = opts.pop("inplace", False)
+        out = policy_loss(logits.detach(), ids, mask, adv, B, T,
+                          dlogits=logits.detach() if inplace else "new", **opts)
+        ctx.save_for_backward(out["dlogits"])
+        ctx.stats = out["stats"]
+        ctx.mark_non_differentiable(out["logp"], out["entropy"])
+        loss = out["stats"][:8].view(torch.float64)[0].clone()
+        return loss, out["logp"], out["entropy"]
+
+    @staticmethod
+    def backward(ctx, grad_loss, _g_logp, _g_ent):
+        (dlogits,) = ctx.saved_tensors
+        if grad_loss is not None and float(grad_loss) != 1.0:
+            dlogits = dlogits * grad_loss.to(dlogits.dtype)
+        return dlogits, None, None, None, None, None, None

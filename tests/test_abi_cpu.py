@@ -138,3 +138,44 @@ def test_binding_raises_without_library(tmp_path):
             rl.load(str(tmp_path / "missing.so"))
         finally:
             rl._lib = saved
+
+
+def _desc(**over):
+    d = rl.rl_policy_loss_desc_init()
+    d.logits, d.dtype, d.B, d.T, d.V, d.ld = FAKE, rl.RL_BF16, 2, 4, 1024, 1024
+    d.ids, d.mask, d.adv = FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000
+    d.dlogits, d.stats_dev, d.workspace = FAKE + 0x400000, FAKE + 0x500000, FAKE + 0x600000
+    d.workspace_bytes = rl.rl_policy_loss_workspace_size(8)
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_desc_defaults(lib):
+    d = rl.rl_policy_loss_desc_init()
+    assert abs(d.eps - 0.2) < 1e-7 and d.eps_high == -1.0 and d.ddof == 1
+    assert d.std_eps == 1e-4 and d.grad_scale == 1.0 and d.agg == rl.RL_AGG_TOKEN_MEAN
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(agg=9), rl.RL_ERR_DTYPE),
+    (dict(adv_layout=5), rl.RL_ERR_DTYPE),
+    (dict(agg=rl.RL_AGG_TOKEN_SUM_NORM, agg_norm=0.0), rl.RL_ERR_ARG),
+    (dict(agg=rl.RL_AGG_TOKEN_SUM_NORM, agg_norm=float("nan")), rl.RL_ERR_ARG),
+    (dict(adv_layout=rl.RL_ADV_GROUP_REWARDS, group_size=3), rl.RL_ERR_SHAPE),  # 3 does not divide B=2
+    (dict(adv_layout=rl.RL_ADV_GROUP_REWARDS, group_size=1), rl.RL_ERR_SHAPE),  # G <= ddof
+    (dict(adv_layout=rl.RL_ADV_GROUP_REWARDS, group_size=2, ddof=2), rl.RL_ERR_ARG),
+    (dict(adv_layout=rl.RL_ADV_GROUP_REWARDS, group_size=2, std_eps=-1.0), rl.RL_ERR_ARG),
+    (dict(eps_high=float("inf")), rl.RL_ERR_ARG),
+    (dict(stats_dev=None), rl.RL_ERR_NULL),
+])
+def test_desc_argument_errors(lib, over, status):
+    assert lib.rl_policy_loss_fwd_bwd_ex(ctypes.byref(_desc(**over)), None) == status
+
+
+def test_desc_null(lib):
+    assert lib.rl_policy_loss_fwd_bwd_ex(None, None) == rl.RL_ERR_NULL
+
+
+def test_fixed_form_rejects_group_rewards_layout(lib):
+    assert call_loss(lib, adv_layout=rl.RL_ADV_GROUP_REWARDS) == rl.RL_ERR_DTYPE

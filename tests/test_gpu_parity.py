@@ -298,3 +298,162 @@ def test_full_size_workload(name):
     for r0 in range(0, R, 4096):
         blk = out["dlogits"][r0:r0 + 4096][dm[r0:r0 + 4096]]
         assert int(torch.count_nonzero(blk.view(torch.int16))) == 0
+
+
+# ----------------------------------------------------------------- loss options (descriptor API)
+def _options_case(seed=7, V=40000, dtype="bf16"):
+    w = W["qwen3_0p6b_grpo"].scaled(n_prompts=3, group=4, T=16, V=V, dtype=dtype,
+                                    lengths=("uniform", 0, 16), seed=seed, c_ent=0.01)
+    small, logits = build_case(w)
+    mask = small["mask"].copy()
+    mask.reshape(w.B, w.T)[1] = 0          # one empty sequence
+    mask.reshape(w.B, w.T)[2, :16] = 1     # one full sequence
+    host = storage_np(logits)
+    ids = small["ids"]
+    lse, logp, ent = oracle.row_stats(host, w.dtype, w.V, ids, mask)
+    lo, rf = composed_old_ref(logp, small, mask, w.R)
+    return w, small, logits, host, mask, ids, (lse, logp, ent), lo, rf
+
+
+@pytest.mark.parametrize("agg", ["token_mean", "seq_mean_token_mean", "seq_mean_token_sum",
+                                 "token_sum_norm"])
+@pytest.mark.parametrize("eps_high", [None, 0.28])
+def test_aggregation_and_clip_higher(agg, eps_high):
+    w, small, logits, host, mask, ids, (lse, logp, ent), lo, rf = _options_case()
+    A = oracle.group_advantages(small["rewards"], w.group)
+    arow = np.repeat(A, w.T)
+    kw = dict(eps_high=eps_high, agg=agg, T=w.T, agg_norm=100.0)
+    ref = oracle.loss_from_stats(logp, ent, mask, arow, lo, rf, w.eps, w.beta, w.c_ent, **kw)
+    band = band_mask(ref, w.eps) | (np.abs(ref["r"] - (1 + (eps_high or w.eps))) < CLIP_BAND)
+    band &= mask != 0
+    gs = 37.0
+    out = torch_api.policy_loss(logits, to_dev(ids), to_dev(mask), to_dev(A.astype(np.float32)),
+                                w.B, w.T, logp_old=to_dev(lo), ref_logp=to_dev(rf), eps=w.eps,
+                                beta=w.beta, c_ent=w.c_ent, grad_scale=gs, eps_high=eps_high,
+                                agg=agg, agg_norm=100.0)
+    torch.cuda.synchronize()
+    st = torch_api.read_stats(out["stats"])
+    assert_stats_match(st, ref, int(band.sum()))
+    rows = np.nonzero(~band)[0]
+    scale = gs * ref["weights"][rows]
+    d_ref = oracle.dlogits_rows(host, w.dtype, w.V, ids, rows, lse[rows], ent[rows],
+                                ref["g"][rows], scale, w.c_ent, w.dtype)
+    assert_dlogits_close(storage_np(out["dlogits"])[rows], d_ref, w.dtype, where=agg)
+
+
+@pytest.mark.parametrize("ddof", [1, 0])
+def test_group_rewards_fused_into_the_loss_launch(ddof):
+    w, small, logits, host, mask, ids, (lse, logp, ent), lo, rf = _options_case(seed=11, V=8200)
+    rewards = to_dev(small["rewards"])
+    common = dict(logp_old=to_dev(lo), ref_logp=to_dev(rf), eps=w.eps, beta=w.beta,
+                  c_ent=w.c_ent, grad_scale=5.0, agg="seq_mean_token_mean")
+    fused = torch_api.policy_loss(logits, to_dev(ids), to_dev(mask), rewards, w.B, w.T,
+                                  group_size=w.group, ddof=ddof, **common)
+    adv = torch_api.group_advantages(rewards, w.group, ddof=ddof)
+    split = torch_api.policy_loss(logits, to_dev(ids), to_dev(mask), adv, w.B, w.T, **common)
+    torch.cuda.synchronize()
+    # same fp64 arithmetic for the advantages: the two paths agree bit for bit
+    assert torch.equal(fused["stats"], split["stats"])
+    assert torch.equal(fused["dlogits"].view(torch.int16), split["dlogits"].view(torch.int16))
+    # and both match the oracle
+    A = oracle.group_advantages(small["rewards"], w.group, ddof=ddof)
+    ref = oracle.loss_from_stats(logp, ent, mask, np.repeat(A, w.T), lo, rf, w.eps, w.beta,
+                                 w.c_ent, agg="seq_mean_token_mean", T=w.T)
+    band = band_mask(ref, w.eps) & (mask != 0)
+    assert_stats_match(torch_api.read_stats(fused["stats"]), ref, int(band.sum()))
+
+
+# ----------------------------------------------------------------- critic
+@pytest.mark.parametrize("clip", [None, 0.2])
+def test_value_loss_ppo_workload(clip):
+    w = W["ppo_gae"]
+    small = synth.small_inputs(w)
+    _, ret = oracle.gae(small["rewards"], small["values"], small["lengths"], w.gamma, w.lam)
+    ret = ret.astype(np.float32).reshape(-1)
+    rng = np.random.default_rng(12)
+    v = (small["values"].reshape(-1) + rng.normal(0, 0.4, w.R)).astype(np.float32)
+    v_old = (small["values"].reshape(-1) + rng.normal(0, 0.4, w.R)).astype(np.float32)
+    L = rng.integers(1, w.T + 1, w.B)
+    mask = (np.arange(w.T)[None, :] < L[:, None]).astype(np.uint8).reshape(-1)
+    N = int(mask.sum())
+    ref = oracle.value_loss(v, v_old if clip else None, ret, mask, clip, grad_scale=N)
+    dv, st = torch_api.value_loss(to_dev(v), to_dev(ret), to_dev(mask),
+                                  values_old=to_dev(v_old) if clip else None,
+                                  clip_eps=clip if clip else -1.0, grad_scale=float(N))
+    dv = dv.cpu().numpy()
+    # tokens at a kink (clip boundary or equal squares) may take either branch
+    vd, vo64, r64 = v.astype(np.float64), v_old.astype(np.float64), ret.astype(np.float64)
+    if clip:
+        vc = vo64 + np.clip(vd - vo64, -clip, clip)
+        kink = (np.abs(np.abs(vd - vo64) - clip) < 1e-5) | (np.abs((vc - r64) ** 2 - (vd - r64) ** 2) < 1e-5)
+    else:
+        kink = np.zeros(w.R, bool)
+    kink &= mask != 0
+    assert st["n_tokens"] == N
+    assert abs(st["n_clipped"] - ref["n_clipped"]) <= int(kink.sum())
+    assert_scalar_close("value loss", st["loss"], ref["loss"])
+    assert_scalar_close("mean_abs_err", st["mean_abs_err"], ref["mean_abs_err"])
+    ok = ~kink
+    np.testing.assert_allclose(dv[ok], ref["dvalues"][ok], rtol=1e-5, atol=1e-6)
+    assert np.all(dv[mask == 0] == 0)
+
+
+# ----------------------------------------------------------------- autograd and CUDA graphs
+def _small_inputs_dev(name="qwen_vocab_bf16_c2"):
+    w = SMALL[name]
+    small, logits = build_case(w)
+    return w, small, logits, to_dev(small["ids"]), to_dev(small["mask"]), to_dev(small["rewards"])
+
+
+def test_autograd_function_matches_direct_call():
+    w, small, logits, ids, mask, rewards = _small_inputs_dev()
+    opts = dict(eps=w.eps, c_ent=0.01, group_size=w.group, agg="seq_mean_token_mean")
+    direct = torch_api.policy_loss(logits, ids, mask, rewards, w.B, w.T, **opts)
+    x = logits.clone().requires_grad_(True)
+    loss, logp, ent = torch_api.FusedPolicyLoss.apply(x, ids, mask, rewards, w.B, w.T, opts)
+    (3.0 * loss).backward()
+    st = torch_api.read_stats(direct["stats"])
+    assert float(loss.detach()) == st["loss"]
+    assert torch.equal(logp, direct["logp"]) and torch.equal(ent, direct["entropy"])
+    expect = direct["dlogits"] * torch.tensor(3.0, dtype=logits.dtype, device=logits.device)
+    assert torch.equal(x.grad.view(torch.int16), expect.view(torch.int16))
+
+
+def test_cuda_graph_capture_replays_the_step():
+    w, small, logits, ids, mask, rewards = _small_inputs_dev()
+    adv = torch.empty(w.B, device="cuda")
+    dl = torch.empty_like(logits)
+    lp = torch.empty(w.R, device="cuda")
+    en = torch.empty(w.R, device="cuda")
+    ws = torch_api.new_workspace(w.R, "cuda")
+    st = torch_api.new_stats("cuda")
+
+    def step(s=None):
+        torch_api.group_advantages(rewards, w.group, out=adv, stream=s)
+        torch_api.policy_loss(logits, ids, mask, adv, w.B, w.T, eps=w.eps, c_ent=0.01,
+                              grad_scale=9.0, dlogits=dl, logp_out=lp, entropy_out=en,
+                              workspace=ws, stats=st, stream=s)
+
+    step()  # warm-up: launch plans are cached before capture
+    torch.cuda.synchronize()
+    eager = (dl.clone(), st.clone(), lp.clone())
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    dl.zero_()
+    st.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dl.view(torch.int16), eager[0].view(torch.int16))
+    assert torch.equal(st, eager[1]) and torch.equal(lp, eager[2])
+    # new inputs in the same buffers: the replay follows them
+    logits.mul_(0.5)
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = (dl.clone(), st.clone())
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(dl.view(torch.int16), replayed[0].view(torch.int16))
+    assert torch.equal(st, replayed[1])

@@ -450,3 +450,26 @@ def value_loss(values, values_old, returns, mask, clip_eps=None, grad_scale=1.0)
     n_clipped = int((use_c & m).sum())
     return dict(loss=loss, dvalues=dvalues, n_tokens=N, n_clipped=n_clipped,
                 clip_frac=n_clipped / N, mean_abs_err=math.fsum(np.abs(v - ret)[m]) / N)
+
+
+def masked_whiten(x, mask, eps=1e-8, shift_mean=True):
+    """Masked advantage whitening over the valid tokens of a batch.
+
+    The pages name advantage estimation and reward normalisation as parts of
+    the update (ainews.cool RL.cu article, "PPO 更新内核" bullet and the
+    paragraph after the benchmark table); the usual normalisation of PPO-GAE
+    advantages is this one:
+        mu  = (1/N) sum_t m_t x_t,  var = (1/(N-1)) sum_t m_t (x_t - mu)^2
+        out = (x - mu) / sqrt(var + eps)      (x / sqrt(var + eps) without the
+                                               mean shift), 0 on masked tokens
+    N < 2 gives x - mu (or x) divided by sqrt(eps): var is taken as 0.
+    """
+    x = np.asarray(x, np.float64).reshape(-1)
+    m = np.asarray(mask).reshape(-1) != 0
+    N = int(m.sum())
+    if N == 0:
+        return np.zeros(x.size)
+    mu = math.fsum(x[m]) / N
+    var = math.fsum((x[m] - mu) ** 2) / (N - 1) if N > 1 else 0.0
+    out = ((x - mu) if shift_mean else x) / math.sqrt(var + eps)
+    return np.where(m, out, 0.0)

@@ -522,3 +522,24 @@ def test_value_loss_central_differences():
         vm[i] -= h
         fd = (oracle.value_loss(vp, vo, ret, m, 0.3)["loss"] - oracle.value_loss(vm, vo, ret, m, 0.3)["loss"]) / (2 * h)
         assert abs(fd - o["dvalues"][i]) < 1e-7
+
+
+# ----------------------------------------------------------------------------- whitening
+def test_masked_whiten_matches_numpy_and_normalises():
+    rng = np.random.default_rng(60)
+    x = rng.normal(3.0, 2.5, 1000)
+    m = (rng.random(1000) < 0.6).astype(np.uint8)
+    w = oracle.masked_whiten(x, m, eps=0.0)
+    sel = x[m == 1]
+    np.testing.assert_allclose(w[m == 1], (sel - sel.mean()) / sel.std(ddof=1), rtol=1e-12)
+    assert np.all(w[m == 0] == 0)
+    assert abs(w[m == 1].mean()) < 1e-12 and abs(w[m == 1].std(ddof=1) - 1.0) < 1e-12
+    w2 = oracle.masked_whiten(x, m, eps=0.0, shift_mean=False)
+    np.testing.assert_allclose(w2[m == 1], sel / sel.std(ddof=1), rtol=1e-12)
+
+
+def test_masked_whiten_degenerate():
+    assert np.all(oracle.masked_whiten([1.0, 2.0], [0, 0]) == 0)
+    one = oracle.masked_whiten([5.0, 7.0], [0, 1], eps=4.0)
+    assert one[1] == 0.0 and one[0] == 0.0          # single token: x - mu = 0
+    assert abs(oracle.masked_whiten([5.0], [1], eps=4.0, shift_mean=False)[0] - 2.5) < 1e-15

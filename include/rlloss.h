@@ -143,6 +143,20 @@ rl_status rl_gae_reverse_scan(const float* rewards, const float* values, const i
                               float* adv_out, float* returns_out, void* stream);
 
 /*
+ * Masked advantage whitening over the valid tokens of the batch (the usual
+ * normalisation of PPO-GAE advantages; the pages name reward normalisation and
+ * advantage estimation in the update, ainews.cool RL.cu article):
+ *   mu = (1/N) sum_t m_t x_t,  var = (1/(N-1)) sum_t m_t (x_t - mu)^2  (0 if N < 2)
+ *   out_t = (x_t - mu) / sqrt(var + eps)   (x_t / sqrt(var + eps) if !shift_mean)
+ *   out_t = 0 where mask_t == 0.
+ *   x, out : float[n], device (out may equal x);  mask : uint8[n].
+ * fp64 reductions, one launch of one CTA.  Errors: RL_ERR_SHAPE (n < 0),
+ * RL_ERR_NULL, RL_ERR_ARG (eps negative or NaN).  n == 0 launches nothing.
+ */
+rl_status rl_masked_whiten(const float* x, const unsigned char* mask, long long n, double eps,
+                           int shift_mean, float* out, void* stream);
+
+/*
  * Bytes of device workspace rl_policy_loss_fwd_bwd needs for n_rows rows.
  * The workspace must be zero-filled once before its first use (e.g. with
  * cudaMemset); every call that completes leaves it ready for the next.  A

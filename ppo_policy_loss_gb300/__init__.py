@@ -33,7 +33,7 @@ __all__ = [
     "rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_workspace_size",
     "rl_policy_loss_fwd_bwd", "rl_policy_loss_fwd_bwd_ex", "rl_policy_loss_desc_init",
     "rl_policy_loss_desc", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
-    "rl_read_device_status", "rl_value_loss_fwd_bwd", "rl_value_stats", "value_stats_from_bytes",
+    "rl_read_device_status", "rl_masked_whiten", "rl_value_loss_fwd_bwd", "rl_value_stats", "value_stats_from_bytes",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -100,6 +100,8 @@ def load(path: str | None = None):
     lib.rl_policy_loss_desc_init.restype = None
     lib.rl_policy_loss_fwd_bwd_ex.argtypes = [ctypes.POINTER(rl_policy_loss_desc), P]
     lib.rl_value_loss_fwd_bwd.argtypes = [P, P, P, P, LL, F, F, P, P, P]
+    lib.rl_masked_whiten.argtypes = [P, P, LL, D, I, P, P]
+    lib.rl_masked_whiten.restype = I
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
     lib.rl_read_device_status.argtypes = [P, P]
@@ -200,6 +202,11 @@ def rl_value_loss_fwd_bwd(values, values_old, returns, mask, n, clip_eps, grad_s
     _check(load().rl_value_loss_fwd_bwd(_ptr(values), _ptr(values_old), _ptr(returns), _ptr(mask),
                                         n, clip_eps, grad_scale, _ptr(dvalues), _ptr(stats_dev),
                                         _stream(stream)), "rl_value_loss_fwd_bwd")
+
+
+def rl_masked_whiten(x, mask, n, eps, shift_mean, out, stream=None):
+    _check(load().rl_masked_whiten(_ptr(x), _ptr(mask), n, eps, int(shift_mean), _ptr(out),
+                                   _stream(stream)), "rl_masked_whiten")
 
 
 def value_stats_from_bytes(raw: bytes) -> dict:

@@ -134,3 +134,78 @@ extern "C" rl_status rl_gae_reverse_scan(const float* rewards, const float* valu
       returns_out);
   return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------ masked whitening
+namespace rl {
+namespace {
+
+constexpr int kThreadsW = 1024;
+
+// One CTA: fp64 masked mean, unbiased variance, then (x - mu) / sqrt(var + eps)
+// (or x / sqrt(var + eps)); every element is read and written by the same
+// thread after the reductions, so out may alias x.
+__global__ void __launch_bounds__(kThreadsW, 1)
+masked_whiten_kernel(const float* x, const unsigned char* __restrict__ mask, long long n,
+                     double eps, int shift_mean, float* out) {
+  __shared__ double s_red[kThreadsW / 32][2];
+  __shared__ double s_mu, s_inv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  double sum = 0.0, cnt = 0.0;
+  for (long long i = tid; i < n; i += kThreadsW)
+    if (mask[i]) {
+      sum += static_cast<double>(x[i]);
+      cnt += 1.0;
+    }
+  sum = warp_sum(sum);
+  cnt = warp_sum(cnt);
+  if (lane == 0) {
+    s_red[warp][0] = sum;
+    s_red[warp][1] = cnt;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double S = 0.0, C = 0.0;
+    for (int w = 0; w < kThreadsW / 32; ++w) {
+      S += s_red[w][0];
+      C += s_red[w][1];
+    }
+    s_mu = C > 0.0 ? S / C : 0.0;
+    s_inv = C;  // count, until the variance is known
+  }
+  __syncthreads();
+  const double mu = s_mu, N = s_inv;
+  double sq = 0.0;
+  for (long long i = tid; i < n; i += kThreadsW)
+    if (mask[i]) {
+      const double d = static_cast<double>(x[i]) - mu;
+      sq += d * d;
+    }
+  sq = warp_sum(sq);
+  __syncthreads();
+  if (lane == 0) s_red[warp][0] = sq;
+  __syncthreads();
+  if (tid == 0) {
+    double Q = 0.0;
+    for (int w = 0; w < kThreadsW / 32; ++w) Q += s_red[w][0];
+    const double var = N > 1.0 ? Q / (N - 1.0) : 0.0;
+    s_inv = 1.0 / sqrt(var + eps);
+  }
+  __syncthreads();
+  const double inv = s_inv, shift = shift_mean ? mu : 0.0;
+  for (long long i = tid; i < n; i += kThreadsW)
+    out[i] = mask[i] ? static_cast<float>((static_cast<double>(x[i]) - shift) * inv) : 0.f;
+}
+
+}  // namespace
+}  // namespace rl
+
+extern "C" rl_status rl_masked_whiten(const float* x, const unsigned char* mask, long long n,
+                                      double eps, int shift_mean, float* out, void* stream) {
+  if (n < 0) return RL_ERR_SHAPE;
+  if (!(eps >= 0.0) || !std::isfinite(eps)) return RL_ERR_ARG;
+  if (n == 0) return RL_OK;
+  if (!x || !mask || !out) return RL_ERR_NULL;
+  rl::masked_whiten_kernel<<<1, rl::kThreadsW, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, mask, n, eps, shift_mean, out);
+  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}

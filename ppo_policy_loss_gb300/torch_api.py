@@ -9,7 +9,8 @@ import torch
 
 from . import (AGGREGATIONS, DTYPES, RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN,
                STATS_BYTES, rl_gae_reverse_scan, rl_group_advantages, rl_policy_loss_desc_init,
-               VALUE_STATS_BYTES, rl_policy_loss_fwd_bwd_ex, rl_policy_loss_workspace_size,
+               VALUE_STATS_BYTES, rl_masked_whiten, rl_policy_loss_fwd_bwd_ex,
+               rl_policy_loss_workspace_size,
                rl_value_loss_fwd_bwd, stats_from_bytes, value_stats_from_bytes)
 
 _DT = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
@@ -142,3 +143,11 @@ class FusedPolicyLoss(torch.autograd.Function):
         if grad_loss is not None and float(grad_loss) != 1.0:
             dlogits = dlogits * grad_loss.to(dlogits.dtype)
         return dlogits, None, None, None, None, None, None
+
+
+def masked_whiten(x: torch.Tensor, mask: torch.Tensor, eps: float = 1e-8, shift_mean: bool = True,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Masked advantage whitening (rl_masked_whiten)."""
+    out = torch.empty_like(x) if out is None else out
+    rl_masked_whiten(x, mask, x.numel(), eps, shift_mean, out, stream)
+    return out

@@ -457,3 +457,84 @@ def test_cuda_graph_capture_replays_the_step():
     torch.cuda.synchronize()
     assert torch.equal(dl.view(torch.int16), replayed[0].view(torch.int16))
     assert torch.equal(st, replayed[1])
+
+
+# ----------------------------------------------------------------- whitening
+@pytest.mark.parametrize("shift", [True, False])
+def test_masked_whiten_ppo_advantages(shift):
+    w = W["ppo_gae"]
+    small = synth.small_inputs(w)
+    A, _ = oracle.gae(small["rewards"], small["values"], small["lengths"], w.gamma, w.lam)
+    A = A.astype(np.float32).reshape(-1)
+    rng = np.random.default_rng(13)
+    L = rng.integers(0, w.T + 1, w.B)
+    mask = (np.arange(w.T)[None, :] < L[:, None]).astype(np.uint8).reshape(-1)
+    ref = oracle.masked_whiten(A, mask, 1e-8, shift)
+    d = to_dev(A)
+    got = torch_api.masked_whiten(d, to_dev(mask), 1e-8, shift).cpu().numpy()
+    assert np.all(np.abs(got - ref) <= ADV_TOL * np.maximum(np.abs(ref), 1.0))
+    torch_api.masked_whiten(d, to_dev(mask), 1e-8, shift, out=d)  # in place
+    assert np.array_equal(d.cpu().numpy(), got)
+
+
+# ----------------------------------------------------------------- randomized sweep
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    dtype = ["f32", "bf16", "f16"][rng.integers(0, 3)]
+    es = {"f32": 4, "bf16": 2, "f16": 2}[dtype]
+    u = rng.random()
+    V = (int(rng.choice([1, 2, 3, 7, 8, 9, 63, 64, 65])) if u < 0.4 else
+         int(rng.integers(1, 5001)) if u < 0.8 else int(rng.integers(50000, 120001)))
+    align = 16 // es
+    ld = -(-V // align) * align + align * int(rng.integers(0, 3))
+    G = int(rng.integers(1, 4))
+    n_prompts = int(rng.integers(1, 4))
+    T = int(rng.integers(1, 12))
+    style = rng.integers(0, 4)
+    lengths = ("uniform", 0, 0) if style == 0 else ("full",) if style == 1 else ("uniform", 0, T)
+    w = W["tiny_grpo"].scaled(dtype=dtype, V=V, group=G + 1, n_prompts=n_prompts, T=T,
+                              lengths=lengths, seed=2000 + seed,
+                              c_ent=float(rng.choice([0.0, 0.03])),
+                              beta=float(rng.choice([0.0, 0.05])))
+    opts = dict(with_old=bool(rng.integers(0, 2)), in_place=bool(rng.integers(0, 2)),
+                agg=str(rng.choice(oracle.AGGREGATIONS)),
+                eps_high=float(rng.choice([-1.0, 0.3])))
+    return w, ld, opts
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_randomized_shapes_and_options(seed):
+    w, ld, o = _random_case(seed)
+    small, logits = build_case(w, ld=ld)
+    V, R = w.V, w.R
+    mask, ids = small["mask"], small["ids"]
+    A = oracle.group_advantages(small["rewards"], w.group)
+    arow = np.repeat(A, w.T)
+    host = storage_np(logits)[:, :V]
+    lse, logp, ent = oracle.row_stats(host, w.dtype, V, ids, mask)
+    lo, rf = composed_old_ref(logp, small, mask, R)
+    eps_high = None if o["eps_high"] < 0 else o["eps_high"]
+    ref = oracle.loss_from_stats(logp, ent, mask, arow, lo if o["with_old"] else None,
+                                 rf if w.beta else None, w.eps, w.beta, w.c_ent, eps_high=eps_high,
+                                 agg=o["agg"], T=w.T, agg_norm=50.0)
+    band = (band_mask(ref, w.eps) | (np.abs(ref["r"] - (1 + (eps_high or w.eps))) < CLIP_BAND)) & (mask != 0)
+    N = ref["n_tokens"]
+    gs = float(max(N, 1))
+    src = logits.clone() if o["in_place"] else logits
+    dst = src if o["in_place"] else torch.full_like(logits, 7.0)
+    out = torch_api.policy_loss(src, to_dev(ids), to_dev(mask), to_dev(A.astype(np.float32)),
+                                w.B, w.T, V=V, logp_old=to_dev(lo) if o["with_old"] else None,
+                                ref_logp=to_dev(rf) if w.beta else None, eps=w.eps, beta=w.beta,
+                                c_ent=w.c_ent, grad_scale=gs, dlogits=dst, eps_high=eps_high,
+                                agg=o["agg"], agg_norm=50.0)
+    torch.cuda.synchronize()
+    st = torch_api.read_stats(out["stats"])
+    assert_stats_match(st, ref, int(band.sum()))
+    assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
+    rows = np.nonzero(~band)[0]
+    d_ref = oracle.dlogits_rows(host, w.dtype, V, ids, rows, lse[rows], ent[rows], ref["g"][rows],
+                                gs * ref["weights"][rows], w.c_ent, w.dtype)
+    assert_dlogits_close(storage_np(out["dlogits"][:, :V])[rows], d_ref, w.dtype,
+                         where=f"seed {seed} {w.dtype} V={V} ld={ld} {o}")
+    if ld != V and not o["in_place"]:
+        assert bool((out["dlogits"][:, V:] == 7.0).all())

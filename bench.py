@@ -15,9 +15,13 @@ the other configurations (see ppo_policy_loss_gb300/synth.py).
                     [--workload NAME]
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own
-replica of the workload on its GPU (the path has no cross-rank exchange
-step); value = all ranks' tokens / max-over-ranks time.  ``--impl reference``
-times the fp64 CPU oracle instead, on a bounded sample of the same workload.
+batch of the workload on its GPU (weak scaling); by default each rank's loss
+is normalised by its own tokens (independent replicas, no collective on the
+data path), and with ``--global-token-mean`` by the tokens of all ranks (the
+path's one exchange: an all-reduce of the token counts before the loss and
+of the loss shares after).  value = all ranks' tokens / max-over-ranks time.
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
+of the same workload.
 """
 from __future__ import annotations
 
@@ -224,10 +228,17 @@ class Step:
         self.stats = torch_api.new_stats(dev)
         self.ld = inp["logits"].stride(0)
 
-    def launch(self, stream, ev=None):
-        """2 launches: the advantages, then the fused loss (bracketed by ev)."""
+    def launch(self, stream, ev=None, global_mean=False):
+        """2 launches: the advantages, then the fused loss (bracketed by ev).
+        With global_mean (data parallel over ranks): 3 launches and two small
+        all-reduces, the token counts before the loss and its shares after."""
         import ppo_policy_loss_gb300 as rl
         w, d = self.w, self.d
+        if global_mean:
+            import torch.distributed as dist
+            from ppo_policy_loss_gb300 import torch_api
+            self.counts = torch_api.count_tokens(d["mask"], w.B, w.T, stream=stream)
+            dist.all_reduce(self.counts)
         if w.advantage == "gae":
             rl.rl_gae_reverse_scan(d["rewards"], d["values"], d["lengths"], w.B, w.T, w.gamma,
                                    w.lam, self.adv, None, stream)
@@ -238,13 +249,34 @@ class Step:
             layout = rl.RL_ADV_PER_SEQ
         if ev is not None:
             ev[0].record(stream)
-        rl.rl_policy_loss_fwd_bwd(d["logits"], w.dtype, w.B, w.T, w.V, self.ld, d["ids"],
-                                  d["logp_old"], d["ref"] if w.beta != 0 else None, d["mask"],
-                                  self.adv, layout, w.eps, w.beta, w.c_ent, 1.0, self.dlogits,
-                                  self.logp, self.ent, self.stats, self.ws, self.ws.numel(),
-                                  stream)
+        if global_mean:
+            desc = rl.rl_policy_loss_desc_init()
+            p = lambda t: t.data_ptr() if t is not None else None
+            desc.logits, desc.dtype, desc.B, desc.T, desc.V, desc.ld = (
+                p(d["logits"]), rl.DTYPES[w.dtype], w.B, w.T, w.V, self.ld)
+            desc.ids, desc.logp_old, desc.mask, desc.adv = (p(d["ids"]), p(d["logp_old"]),
+                                                            p(d["mask"]), p(self.adv))
+            desc.ref_logp = p(d["ref"]) if w.beta != 0 else None
+            desc.adv_layout, desc.eps, desc.eps_high = layout, w.eps, w.eps
+            desc.beta, desc.c_ent, desc.grad_scale = w.beta, w.c_ent, 1.0
+            desc.dlogits, desc.logp_out, desc.entropy_out = (p(self.dlogits), p(self.logp),
+                                                             p(self.ent))
+            desc.stats_dev, desc.workspace, desc.workspace_bytes = (p(self.stats), p(self.ws),
+                                                                    self.ws.numel())
+            desc.global_counts = p(self.counts)
+            rl.rl_policy_loss_fwd_bwd_ex(desc, stream)
+        else:
+            rl.rl_policy_loss_fwd_bwd(d["logits"], w.dtype, w.B, w.T, w.V, self.ld, d["ids"],
+                                      d["logp_old"], d["ref"] if w.beta != 0 else None,
+                                      d["mask"], self.adv, layout, w.eps, w.beta, w.c_ent, 1.0,
+                                      self.dlogits, self.logp, self.ent, self.stats, self.ws,
+                                      self.ws.numel(), stream)
         if ev is not None:
             ev[1].record(stream)
+        if global_mean:
+            import torch.distributed as dist
+            self.loss_share = self.stats[:8].view(__import__("torch").float64).clone()
+            dist.all_reduce(self.loss_share)
 
 
 def workload_for(args):
@@ -283,8 +315,9 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    gm = bool(args.global_token_mean and world > 1)
     for _ in range(args.warmup):
-        step.launch(stream)
+        step.launch(stream, global_mean=gm)
     barrier()
     st = torch_api.read_stats(step.stats)
     assert st["device_error"] == 0 and st["n_tokens"] == n_valid, st
@@ -300,7 +333,7 @@ def run_gpu(args):
     time.sleep(0.3)
     t0.record(stream)
     for i in range(args.steps):
-        step.launch(stream, kev[i])
+        step.launch(stream, kev[i], global_mean=gm)
     t1.record(stream)
     barrier()
     clocks = sampler.stop()
@@ -330,7 +363,9 @@ def run_gpu(args):
                    "valid_tokens_per_s": world * n_valid / (ms_step / 1e3),
                    "l2": (f"inputs ({w.R * w.V * w.elem_bytes / 1e9:.1f} GB logits) vs 129 MB "
                           "L2; no flush"),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "parallelism": ("data parallel, global token mean (all-reduce of the "
+                                   "token counts and of the loss shares)" if gm else
+                                   "replicas" if world > 1 else "single GPU"),
                    "launch_shape": {"cluster": shape[0], "clusters": shape[1],
                                     "smem": shape[2]}},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -338,7 +373,7 @@ def run_gpu(args):
                      "traffic": traffic, "alg_bytes_per_launch": bytes_launch,
                      "kernel": "rl_policy_loss_fwd_bwd", "kernel_ms": kern_ms},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if gm else 2) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -556,6 +591,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--global-token-mean", action="store_true",
+                    help="with N > 1: normalise by the token count summed over ranks")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profiling only: keep the first SEQS sequences")
     args = ap.parse_args()

@@ -271,7 +271,26 @@ typedef struct {
   rl_loss_stats* stats_dev;
   void* workspace;
   size_t workspace_bytes;
+  /* Data parallelism over ranks: device long long[2] = {N, B'} summed over all
+   * ranks (see rl_count_tokens), or NULL for this call's own counts.  With it,
+   * the gradient scales by the global N (or B'), and loss, pg_term, kl_term,
+   * ent_term and clip_frac are this rank's share of the global means (their
+   * sum over ranks is the global value); n_tokens stays this rank's count. */
+  const long long* global_counts;
 } rl_policy_loss_desc;
+
+/*
+ * Token counts of a batch for data parallelism: counts_dev[0] = N (nonzero
+ * mask bytes), counts_dev[1] = B' (sequences of T rows with any valid token).
+ * Sum them over ranks (e.g. an all-reduce) and pass them as
+ * rl_policy_loss_desc.global_counts so every rank normalises by the global
+ * counts; the data path then needs only that 16-byte exchange and, after the
+ * loss, a sum of the ranks' loss shares.  mask: uint8[B*T], device;
+ * counts_dev: long long[2], device, written.  One launch of one CTA.
+ * Errors: RL_ERR_SHAPE (B < 0, T < 0), RL_ERR_NULL.
+ */
+rl_status rl_count_tokens(const unsigned char* mask, long long B, long long T,
+                          long long* counts_dev, void* stream);
 
 /* Fill *desc with the defaults above (all pointers NULL, sizes 0). */
 void rl_policy_loss_desc_init(rl_policy_loss_desc* desc);

@@ -273,7 +273,7 @@ def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent, 
 AGGREGATIONS = ("token_mean", "seq_mean_token_mean", "seq_mean_token_sum", "token_sum_norm")
 
 
-def loss_weights(mask, T, agg="token_mean", agg_norm=None):
+def loss_weights(mask, T, agg="token_mean", agg_norm=None, global_counts=None):
     """Weight w_t of each token in loss = -sum_t w_t J_t (0 on masked tokens).
 
     The pages name the masked loss only as the PPO/GRPO objective; the four
@@ -286,15 +286,17 @@ def loss_weights(mask, T, agg="token_mean", agg_norm=None):
       token_sum_norm      w = 1 / agg_norm           (token sum over a fixed
                                                       normaliser, e.g. B * T_max)
     L_b = valid tokens of sequence b (row b*T + t); B' = sequences with L_b > 0.
+    With ``global_counts`` = (N, B') of a whole data-parallel batch, of which
+    ``mask`` is one rank's share, N and B' are those totals.
     """
     m = np.asarray(mask, dtype=np.uint8).reshape(-1) != 0
     w = np.zeros(m.size)
     if agg == "token_mean":
-        N = int(m.sum())
+        N = int(m.sum()) if global_counts is None else int(global_counts[0])
         w[m] = 1.0 / N if N else 0.0
     elif agg in ("seq_mean_token_mean", "seq_mean_token_sum"):
         L = m.reshape(-1, T).sum(axis=1)
-        Bp = int((L > 0).sum())
+        Bp = int((L > 0).sum()) if global_counts is None else int(global_counts[1])
         Lrow = np.repeat(L, T)
         if agg == "seq_mean_token_mean":
             w[m] = 1.0 / (Bp * Lrow[m])
@@ -309,7 +311,7 @@ def loss_weights(mask, T, agg="token_mean", agg_norm=None):
 
 def loss_from_stats(logp, ent, mask, adv_row, logp_old=None, ref_logp=None, eps=0.2,
                     beta=0.0, c_ent=0.0, eps_high=None, agg="token_mean", T=None,
-                    agg_norm=None):
+                    agg_norm=None, global_counts=None):
     """Loss and monitoring statistics from per-row (logp, H) (fp64, math.fsum sums).
 
     loss = -sum_t w_t J_t with the weights of ``loss_weights`` (token_mean:
@@ -319,24 +321,25 @@ def loss_from_stats(logp, ent, mask, adv_row, logp_old=None, ref_logp=None, eps=
     per-token arrays of token_objective and the weights.
     """
     m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
-    N = count(m)
+    N = count(m)                      # this call's valid tokens
+    Nd = N if global_counts is None else int(global_counts[0])  # the means' denominator
     obj = token_objective(logp, ent, m, adv_row, logp_old, ref_logp, eps, beta, c_ent, eps_high)
     mb = m.astype(bool)
     T = m.size if T is None else T
-    w = loss_weights(m, T, agg, agg_norm) if N else np.zeros(m.size)
+    w = loss_weights(m, T, agg, agg_norm, global_counts) if N else np.zeros(m.size)
     if N > 0:
         if agg == "token_mean":
-            loss = -math.fsum(obj["J"][mb]) / N
+            loss = -math.fsum(obj["J"][mb]) / Nd
         else:
             loss = -math.fsum((w * obj["J"])[mb])
-        pg_term = math.fsum(obj["pg"][mb]) / N
-        kl_term = math.fsum(obj["kl"][mb]) / N
-        ent_term = math.fsum(obj["H"][mb]) / N
+        pg_term = math.fsum(obj["pg"][mb]) / Nd
+        kl_term = math.fsum(obj["kl"][mb]) / Nd
+        ent_term = math.fsum(obj["H"][mb]) / Nd
     else:
         loss = pg_term = kl_term = ent_term = 0.0
     n_clipped = int(obj["clipped"].sum())
     return dict(loss=loss, pg_term=pg_term, kl_term=kl_term, ent_term=ent_term, n_tokens=N,
-                n_clipped=n_clipped, clip_frac=(n_clipped / N if N else 0.0),
+                n_clipped=n_clipped, clip_frac=(n_clipped / Nd if N else 0.0),
                 logp=np.where(mb, logp, 0.0), entropy=np.where(mb, ent, 0.0), weights=w, **obj)
 
 

@@ -33,7 +33,7 @@ __all__ = [
     "rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_workspace_size",
     "rl_policy_loss_fwd_bwd", "rl_policy_loss_fwd_bwd_ex", "rl_policy_loss_desc_init",
     "rl_policy_loss_desc", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
-    "rl_read_device_status", "rl_masked_whiten", "rl_value_loss_fwd_bwd", "rl_value_stats", "value_stats_from_bytes",
+    "rl_read_device_status", "rl_masked_whiten", "rl_count_tokens", "rl_value_loss_fwd_bwd", "rl_value_stats", "value_stats_from_bytes",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -63,7 +63,7 @@ class rl_policy_loss_desc(ctypes.Structure):
                 ("agg", ctypes.c_int), ("agg_norm", ctypes.c_double), ("dlogits", ctypes.c_void_p),
                 ("logp_out", ctypes.c_void_p), ("entropy_out", ctypes.c_void_p),
                 ("stats_dev", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("global_counts", ctypes.c_void_p)]
 
 
 class rl_value_stats(ctypes.Structure):
@@ -101,6 +101,8 @@ def load(path: str | None = None):
     lib.rl_policy_loss_fwd_bwd_ex.argtypes = [ctypes.POINTER(rl_policy_loss_desc), P]
     lib.rl_value_loss_fwd_bwd.argtypes = [P, P, P, P, LL, F, F, P, P, P]
     lib.rl_masked_whiten.argtypes = [P, P, LL, D, I, P, P]
+    lib.rl_count_tokens.argtypes = [P, LL, LL, P, P]
+    lib.rl_count_tokens.restype = I
     lib.rl_masked_whiten.restype = I
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
@@ -207,6 +209,11 @@ def rl_value_loss_fwd_bwd(values, values_old, returns, mask, n, clip_eps, grad_s
 def rl_masked_whiten(x, mask, n, eps, shift_mean, out, stream=None):
     _check(load().rl_masked_whiten(_ptr(x), _ptr(mask), n, eps, int(shift_mean), _ptr(out),
                                    _stream(stream)), "rl_masked_whiten")
+
+
+def rl_count_tokens(mask, B, T, counts_dev, stream=None):
+    _check(load().rl_count_tokens(_ptr(mask), B, T, _ptr(counts_dev), _stream(stream)),
+           "rl_count_tokens")
 
 
 def value_stats_from_bytes(raw: bytes) -> dict:

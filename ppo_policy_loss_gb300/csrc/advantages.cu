@@ -209,3 +209,52 @@ extern "C" rl_status rl_masked_whiten(const float* x, const unsigned char* mask,
       x, mask, n, eps, shift_mean, out);
   return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------ token counts
+namespace rl {
+namespace {
+
+constexpr int kThreadsC = 1024;
+
+// One CTA: N = nonzero mask bytes, B' = sequences (rows of T) with any.
+__global__ void __launch_bounds__(kThreadsC, 1)
+count_tokens_kernel(const unsigned char* __restrict__ mask, long long B, long long T,
+                    long long* counts) {
+  __shared__ long long s_n[kThreadsC / 32], s_b[kThreadsC / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  long long n = 0, nb = 0;
+  for (long long b = warp; b < B; b += kThreadsC / 32) {
+    long long c = 0;
+    for (long long t = lane; t < T; t += 32) c += mask[b * T + t] != 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    n += c;
+    nb += c > 0;
+  }
+  if (lane == 0) {
+    s_n[warp] = n;
+    s_b[warp] = nb;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    long long N = 0, Bp = 0;
+    for (int w = 0; w < kThreadsC / 32; ++w) {
+      N += s_n[w];
+      Bp += s_b[w];
+    }
+    counts[0] = N;
+    counts[1] = Bp;
+  }
+}
+
+}  // namespace
+}  // namespace rl
+
+extern "C" rl_status rl_count_tokens(const unsigned char* mask, long long B, long long T,
+                                     long long* counts_dev, void* stream) {
+  if (B < 0 || T < 0) return RL_ERR_SHAPE;
+  if (!counts_dev || (B * T > 0 && !mask)) return RL_ERR_NULL;
+  rl::count_tokens_kernel<<<1, rl::kThreadsC, 0, static_cast<cudaStream_t>(stream)>>>(mask, B, T,
+                                                                                     counts_dev);
+  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}

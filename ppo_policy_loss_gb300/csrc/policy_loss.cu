@@ -121,6 +121,7 @@ struct LossArgs {
   float beta, c_ent, grad_scale;
   int agg;              // rl_loss_agg
   double agg_w;         // RL_AGG_TOKEN_SUM_NORM: 1 / agg_norm
+  const long long* global_counts;  // device [N, B'] over all ranks, or null (local counts)
 };
 
 // ------------------------------------------------------------------ element formats
@@ -606,12 +607,16 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       cnt = 0;
       for (int w = 0; w < kConsumerWarps; ++w) cnt += sm.wcount[w];
     }
-    const long long N = cnt;
+    const long long N_local = cnt;
+    // Data parallel over ranks: the means run over every rank's tokens.
+    const long long N = a.global_counts ? a.global_counts[0] : N_local;
     const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
     const bool with_entropy = a.c_ent != 0.f;
     const bool seq_agg = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN || a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM;
     long long Bp = 0;  // sequences with at least one valid token
-    if (seq_agg) {
+    if (seq_agg && a.global_counts) {
+      Bp = a.global_counts[1];
+    } else if (seq_agg) {
       const long long nseq = a.R / a.T;
       long long nb = 0;
       for (long long b = warp; b < nseq; b += kConsumerWarps)
@@ -908,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         out.kl_term = tot[2] * inv;
         out.ent_term = tot[3] * inv;
         out.clip_frac = tot[4] * inv;
-        out.n_tokens = N;
+        out.n_tokens = N_local;
         out.n_clipped = static_cast<long long>(tot[4]);
         out.device_error = static_cast<int>(stw);
         out.reserved = 0;
@@ -1175,6 +1180,7 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   args.grad_scale = d->grad_scale;
   args.agg = d->agg;
   args.agg_w = d->agg == RL_AGG_TOKEN_SUM_NORM ? 1.0 / d->agg_norm : 0.0;
+  args.global_counts = d->global_counts;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

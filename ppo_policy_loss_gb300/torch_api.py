@@ -9,7 +9,7 @@ import torch
 
 from . import (AGGREGATIONS, DTYPES, RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN,
                STATS_BYTES, rl_gae_reverse_scan, rl_group_advantages, rl_policy_loss_desc_init,
-               VALUE_STATS_BYTES, rl_masked_whiten, rl_policy_loss_fwd_bwd_ex,
+               VALUE_STATS_BYTES, rl_count_tokens, rl_masked_whiten, rl_policy_loss_fwd_bwd_ex,
                rl_policy_loss_workspace_size,
                rl_value_loss_fwd_bwd, stats_from_bytes, value_stats_from_bytes)
 
@@ -56,7 +56,7 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
                 dlogits="new", logp_out="new", entropy_out="new", workspace=None, stats=None,
                 stream=None, eps_high: float | None = None, agg: str = "token_mean",
                 agg_norm: float = 1.0, group_size: int | None = None, ddof: int = 1,
-                std_eps: float = 1e-4) -> dict:
+                std_eps: float = 1e-4, global_counts: torch.Tensor | None = None) -> dict:
     """Run the fused loss on [B*T, ld] logits (rl_policy_loss_fwd_bwd_ex).
 
     ``dlogits`` / ``logp_out`` / ``entropy_out``: "new" allocates, None skips,
@@ -96,6 +96,7 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
     d.agg, d.agg_norm = AGGREGATIONS[agg], agg_norm
     d.dlogits, d.logp_out, d.entropy_out = p(dlogits), p(logp_out), p(entropy_out)
     d.stats_dev, d.workspace, d.workspace_bytes = p(stats), p(workspace), workspace.numel()
+    d.global_counts = p(global_counts)
     rl_policy_loss_fwd_bwd_ex(d, stream)
     return dict(dlogits=dlogits, logp=logp_out, entropy=entropy_out, stats=stats,
                 workspace=workspace)
@@ -150,4 +151,12 @@ def masked_whiten(x: torch.Tensor, mask: torch.Tensor, eps: float = 1e-8, shift_
     """Masked advantage whitening (rl_masked_whiten)."""
     out = torch.empty_like(x) if out is None else out
     rl_masked_whiten(x, mask, x.numel(), eps, shift_mean, out, stream)
+    return out
+
+
+def count_tokens(mask: torch.Tensor, B: int, T: int, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Device int64[2] = (N, B') of the batch (rl_count_tokens)."""
+    out = torch.empty(2, dtype=torch.int64, device=mask.device) if out is None else out
+    rl_count_tokens(mask, B, T, out, stream)
     return out

@@ -538,3 +538,32 @@ def test_randomized_shapes_and_options(seed):
                          where=f"seed {seed} {w.dtype} V={V} ld={ld} {o}")
     if ld != V and not o["in_place"]:
         assert bool((out["dlogits"][:, V:] == 7.0).all())
+
+
+# ----------------------------------------------------------------- data parallelism
+@pytest.mark.parametrize("agg", ["token_mean", "seq_mean_token_mean", "seq_mean_token_sum"])
+def test_global_counts_split_batch(agg):
+    w = W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=16, V=40000,
+                                    lengths=("uniform", 0, 16), c_ent=0.01)
+    small, logits = build_case(w)
+    mask = small["mask"].copy()
+    mask.reshape(w.B, w.T)[2] = 0
+    m_d, ids_d = to_dev(mask), to_dev(small["ids"])
+    adv_d = to_dev(oracle.group_advantages(small["rewards"], w.group).astype(np.float32))
+    counts = torch_api.count_tokens(m_d, w.B, w.T)
+    L = mask.reshape(w.B, w.T).sum(1)
+    assert counts.tolist() == [int(mask.sum()), int((L > 0).sum())]
+    kw = dict(eps=w.eps, c_ent=w.c_ent, grad_scale=3.0, agg=agg)
+    full = torch_api.policy_loss(logits, ids_d, m_d, adv_d, w.B, w.T, **kw)
+    h = w.B // 2
+    halves = [torch_api.policy_loss(logits[s * h * w.T:(s + 1) * h * w.T], ids_d[s * h * w.T:(s + 1) * h * w.T],
+                                    m_d[s * h * w.T:(s + 1) * h * w.T], adv_d[s * h:(s + 1) * h], h, w.T,
+                                    global_counts=counts, **kw) for s in range(2)]
+    torch.cuda.synchronize()
+    st = torch_api.read_stats(full["stats"])
+    parts = [torch_api.read_stats(x["stats"]) for x in halves]
+    for k in ("loss", "pg_term", "ent_term", "clip_frac"):
+        assert_scalar_close(k, parts[0][k] + parts[1][k], st[k])
+    assert parts[0]["n_tokens"] + parts[1]["n_tokens"] == st["n_tokens"]
+    cat = torch.cat([x["dlogits"] for x in halves])
+    assert torch.equal(cat.view(torch.int16), full["dlogits"].view(torch.int16))

@@ -543,3 +543,22 @@ def test_masked_whiten_degenerate():
     one = oracle.masked_whiten([5.0, 7.0], [0, 1], eps=4.0)
     assert one[1] == 0.0 and one[0] == 0.0          # single token: x - mu = 0
     assert abs(oracle.masked_whiten([5.0], [1], eps=4.0, shift_mean=False)[0] - 2.5) < 1e-15
+
+
+def test_global_counts_split_batch_shares_sum_to_the_whole():
+    # a batch split by sequences over two "ranks": with the whole batch's counts,
+    # the two shares of every mean add up to the single-batch value
+    z, ids, mask, adv, lo, rf, L = _seq_problem(70, B=6, T=7, lengths=[7, 3, 0, 5, 1, 6])
+    V = z.shape[1]
+    lse, logp, ent = oracle.row_stats(z, "f64", V, ids, mask, threads=1)
+    Bp = int((L > 0).sum())
+    gc = (int(mask.sum()), Bp)
+    for agg in oracle.AGGREGATIONS:
+        kw = dict(eps=0.2, beta=0.05, c_ent=0.02, agg=agg, T=7, agg_norm=30.0)
+        whole = oracle.loss_from_stats(logp, ent, mask, adv, lo, rf, **kw)
+        parts = [oracle.loss_from_stats(logp[sl], ent[sl], mask[sl], adv[sl], lo[sl], rf[sl],
+                                        global_counts=gc, **kw)
+                 for sl in (slice(0, 21), slice(21, 42))]
+        for k in ("loss", "pg_term", "kl_term", "ent_term", "clip_frac"):
+            assert abs(sum(p[k] for p in parts) - whole[k]) < 1e-13, (agg, k)
+        assert np.allclose(np.concatenate([p["weights"] for p in parts]), whole["weights"])

@@ -476,3 +476,21 @@ def masked_whiten(x, mask, eps=1e-8, shift_mean=True):
     var = math.fsum((x[m] - mu) ** 2) / (N - 1) if N > 1 else 0.0
     out = ((x - mu) if shift_mean else x) / math.sqrt(var + eps)
     return np.where(m, out, 0.0)
+
+
+# --------------------------------------------------------------------------- LM head
+def lmhead_row_stats(hidden, weight, ids, dtype="bf16", threads=None):
+    """Log-softmax statistics of logits = hidden @ weight^T, never rounded.
+
+    The logits the fused policy loss consumes come from the policy's LM head
+    (ainews.cool RL.cu article, "技术深度解析": the actor network with its
+    custom matrix multiplication); this is that projection followed by the row
+    statistics of ``row_stats``: a library matmul in float64 on the exactly
+    decoded bf16/fp16 inputs, then lse, logp of the sampled id and entropy.
+    hidden: [R, D], weight: [V, D] (element storage); returns (lse, logp, H).
+    """
+    Hm = decode(np.ascontiguousarray(hidden), dtype)
+    Wm = decode(np.ascontiguousarray(weight), dtype)
+    logits = Hm @ Wm.T
+    ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+    return row_stats(logits, F64, Wm.shape[0], ids, np.ones(logits.shape[0], np.uint8), threads)

@@ -562,3 +562,18 @@ def test_global_counts_split_batch_shares_sum_to_the_whole():
         for k in ("loss", "pg_term", "kl_term", "ent_term", "clip_frac"):
             assert abs(sum(p[k] for p in parts) - whole[k]) < 1e-13, (agg, k)
         assert np.allclose(np.concatenate([p["weights"] for p in parts]), whole["weights"])
+
+
+# ----------------------------------------------------------------------------- LM head
+def test_lmhead_row_stats_match_torch_fp64():
+    g = torch.Generator().manual_seed(90)
+    h = torch.randn(9, 192, generator=g).to(torch.bfloat16)
+    w = (torch.randn(333, 192, generator=g) * 0.2).to(torch.bfloat16)
+    ids = torch.randint(0, 333, (9,), generator=g)
+    st = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    lse, logp, H = oracle.lmhead_row_stats(st(h), st(w), ids.numpy(), "bf16", threads=1)
+    z = h.double() @ w.double().T
+    ref_lsm = torch.log_softmax(z, dim=1)
+    np.testing.assert_allclose(lse, torch.logsumexp(z, 1).numpy(), rtol=1e-13)
+    np.testing.assert_allclose(logp, ref_lsm[torch.arange(9), ids].numpy(), atol=1e-12)
+    np.testing.assert_allclose(H, -(ref_lsm.exp() * ref_lsm).sum(1).numpy(), rtol=1e-12)

@@ -382,6 +382,36 @@ rl_status rl_value_loss_fwd_bwd(const float* values, const float* values_old,
                                 rl_value_stats* stats_dev, void* stream);
 
 /*
+ * Per-row log-softmax statistics of LM-head logits, computed from the hidden
+ * states and the LM-head weight without writing the logits.  The actor's
+ * logits are its LM-head projection (ainews.cool RL.cu article, section
+ * "技术深度解析", actor network with custom matrix multiplication); the
+ * behaviour- and reference-policy log-probs the loss takes are these rows'
+ * log pi(y_r | .).  For each row r < R, with z_r = hidden_r . W^T (fp32
+ * accumulation of the exact bf16 products):
+ *   lse_out[r]     = log sum_v exp z_rv
+ *   logp_out[r]    = z_r,ids[r] - lse_out[r]     (NaN when ids[r] is outside [0, V))
+ *   entropy_out[r] = -sum_v p_rv log p_rv,  p_r = softmax(z_r)
+ *   hidden : bf16 [R, D] device, row stride ld_h elements (ld_h >= D), read only;
+ *   weight : bf16 [V, D] device, row stride ld_w elements (ld_w >= D), read only;
+ *            both 16-byte aligned, row strides multiples of 8 elements, D a
+ *            multiple of 8;
+ *   ids    : int64 [R] device;
+ *   logp_out, entropy_out, lse_out : float [R] device, each may be NULL;
+ *   status_dev : one unsigned int in device memory or NULL; the kernel ORs
+ *            RL_DEVERR_ID_RANGE (an id outside [0, V)) or RL_DEVERR_TIMEOUT
+ *            (a bounded on-chip wait gave up; outputs are garbage) into it.
+ * One launch of a persistent tensor-core kernel (tcgen05, TMA, tensor memory).
+ * Allocates nothing; stream-ordered.  Errors: RL_ERR_SHAPE (R < 0, V < 1,
+ * V > 2^31, D < 8, D not a multiple of 8, a stride below D), RL_ERR_NULL,
+ * RL_ERR_ALIGN, RL_ERR_CUDA.  R == 0 launches nothing.
+ */
+rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
+                             long long R, long long D, long long V, const long long* ids,
+                             float* logp_out, float* entropy_out, float* lse_out,
+                             unsigned int* status_dev, void* stream);
+
+/*
  * The launch shape rl_policy_loss_fwd_bwd would use on the current device for
  * this row shape: CTAs per cluster (one vocabulary slice each), clusters in
  * the persistent grid and dynamic shared memory per CTA.  Host-only query.

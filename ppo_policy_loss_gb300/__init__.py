@@ -33,7 +33,8 @@ __all__ = [
     "rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_workspace_size",
     "rl_policy_loss_fwd_bwd", "rl_policy_loss_fwd_bwd_ex", "rl_policy_loss_desc_init",
     "rl_policy_loss_desc", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
-    "rl_read_device_status", "rl_masked_whiten", "rl_count_tokens", "rl_value_loss_fwd_bwd", "rl_value_stats", "value_stats_from_bytes",
+    "rl_read_device_status", "rl_masked_whiten", "rl_count_tokens", "rl_value_loss_fwd_bwd",
+    "rl_value_stats", "value_stats_from_bytes", "rl_lmhead_logprobs",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -102,8 +103,10 @@ def load(path: str | None = None):
     lib.rl_value_loss_fwd_bwd.argtypes = [P, P, P, P, LL, F, F, P, P, P]
     lib.rl_masked_whiten.argtypes = [P, P, LL, D, I, P, P]
     lib.rl_count_tokens.argtypes = [P, LL, LL, P, P]
+    lib.rl_lmhead_logprobs.argtypes = [P, LL, P, LL, LL, LL, LL, P, P, P, P, P, P]
     lib.rl_count_tokens.restype = I
     lib.rl_masked_whiten.restype = I
+    lib.rl_lmhead_logprobs.restype = I
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
     lib.rl_read_device_status.argtypes = [P, P]
@@ -220,6 +223,13 @@ def value_stats_from_bytes(raw: bytes) -> dict:
     """Decode a host copy of one rl_value_stats record."""
     st = rl_value_stats.from_buffer_copy(bytes(raw))
     return {name: getattr(st, name) for name, _ in rl_value_stats._fields_}
+
+
+def rl_lmhead_logprobs(hidden, ld_h, weight, ld_w, R, D, V, ids, logp_out, entropy_out, lse_out,
+                       status_dev=None, stream=None):
+    _check(load().rl_lmhead_logprobs(_ptr(hidden), ld_h, _ptr(weight), ld_w, R, D, V, _ptr(ids),
+                                     _ptr(logp_out), _ptr(entropy_out), _ptr(lse_out),
+                                     _ptr(status_dev), _stream(stream)), "rl_lmhead_logprobs")
 
 
 def rl_policy_loss_launch_shape(dtype, V, n_rows):

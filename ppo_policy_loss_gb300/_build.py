@@ -1,6 +1,6 @@
 """In-tree build of librlloss.so for sm_103a with nvcc (no cmake, no torch extension).
 
-The three translation units are compiled in parallel, then linked into
+The translation units are compiled in parallel, then linked into
 ``ppo_policy_loss_gb300/librlloss.so`` against the shared CUDA runtime (the same
 libcudart PyTorch loads, so device pointers and streams are shared).
 """
@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "librlloss.so")
-SOURCES = ["policy_loss.cu", "advantages.cu", "critic.cu", "status.cu"]
+SOURCES = ["policy_loss.cu", "advantages.cu", "critic.cu", "status.cu", "lmhead.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I" + INCLUDE]

@@ -1,0 +1,440 @@
+// lmhead.cu — rl_lmhead_logprobs: the LM-head projection fused with the
+// log-softmax statistics, on the 5th-generation tensor cores (sm_103a).
+//
+// The logits the policy loss consumes are the actor's LM-head output
+// (ainews.cool RL.cu article, section "技术深度解析": the actor network with
+// its custom matrix multiplication).  For the log-probabilities of sampled
+// tokens (the behaviour- and reference-policy log-probs of the update) only
+// three numbers per row are needed, so this kernel never writes the
+// R x V logits: it forms them tile by tile in tensor memory and folds each
+// tile into online row statistics.
+//
+//   logits tile [128 rows x 256 vocab] = hidden[128 x D] . W[256 x D]^T
+//
+//   * warp 0 (one lane): TMA producer.  128B-swizzled tiles of hidden
+//     (128 x 64) and W (256 x 64) through a 4-stage ring of 48 KB stages,
+//     guarded by full/empty mbarriers.
+//   * warp 1 (one lane): MMA issuer.  tcgen05.mma.kind::f16 (bf16 inputs,
+//     fp32 accumulation), M=128 N=256 K=16, into one of two 256-column TMEM
+//     accumulators; tcgen05.commit frees each smem stage and, after the last
+//     K block, hands the accumulator to the epilogue.
+//   * warps 2-5 (128 threads, one row each): tcgen05.ld of 32 columns at a
+//     time, online (max, sum 2^x, sum 2^x x) per row, the sampled id's logit,
+//     then lse, log-prob and entropy per row.  Freeing each accumulator lets
+//     the MMAs of the next tile overlap this epilogue.
+//   * Persistent over 128-row tiles; all CTAs sweep W in step, so its tiles
+//     are shared through L2.
+//   * Every mbarrier wait is bounded; on timeout the kernel raises an error
+//     flag, waits for its own copies and tensor-core work, frees its tensor
+//     memory and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "rl_device.cuh"
+
+namespace rl {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;   // tile shape (bf16: 64 elements = 128 B)
+constexpr int kUmmaK = 16;                      // K of one tcgen05.mma.kind::f16
+constexpr int kStagesL = 4;
+constexpr uint32_t kStageA = kBM * kBK * 2;     // 16 KB
+constexpr uint32_t kStageB = kBN * kBK * 2;     // 32 KB
+constexpr int kThreadsL = 192;                  // producer, MMA, 4 epilogue warps
+constexpr uint32_t kTmemCols = 2 * kBN;         // two fp32 accumulators
+constexpr float kFloor = -1.0e30f;              // start of the running row maximum
+
+struct LmSmem {
+  alignas(1024) unsigned char a[kStagesL][kStageA];
+  alignas(1024) unsigned char b[kStagesL][kStageB];
+  unsigned long long full[kStagesL], empty[kStagesL];
+  unsigned long long acc_full[2], acc_empty[2];
+  unsigned long long drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct LmArgs {
+  long long R, D, V;
+  const long long* ids;
+  float* logp_out;
+  float* entropy_out;
+  float* lse_out;
+  unsigned int* status;  // nullable: RL_DEVERR_* bits
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] . B[smem]^T, bf16 in, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// v[j] through a tree of selects on the bits of j (constant register
+// indices only, so v stays in registers).
+__device__ __forceinline__ float select32(const float (&v)[32], int j) {
+  float h[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) h[i] = (j & 16) ? v[i + 16] : v[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = (j & 8) ? h[i + 8] : h[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = (j & 4) ? h[i + 4] : h[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) h[i] = (j & 2) ? h[i + 2] : h[i];
+  return (j & 1) ? h[1] : h[0];
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 B, 8-row (1024 B) swizzle atoms.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);     // start address
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: one 8-row atom
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 D, bf16 A and B, both K-major, M x N.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+template <bool kDrain>
+__device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (kDrain) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+  }
+  return wait_bounded<false>(bar, parity, abort);
+}
+
+// ------------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(kThreadsL, 1)
+lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+                       const LmArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  // the swizzled tiles need 1024-byte alignment
+  LmSmem& sm = *reinterpret_cast<LmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  volatile int* abort_flag = &sm.abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_mt = static_cast<int>((a.R + kBM - 1) / kBM);
+  const int n_nt = static_cast<int>((a.V + kBN - 1) / kBN);
+  const int n_kb = static_cast<int>((a.D + kBK - 1) / kBK);  // columns past D read as zeros
+
+  if (tid == 0) {
+    for (int s = 0; s < kStagesL; ++s) {
+      mbar_init(smem_addr(&sm.full[s]), 1);
+      mbar_init(smem_addr(&sm.empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sm.acc_full[s]), 1);
+      mbar_init(smem_addr(&sm.acc_empty[s]), kBM);
+    }
+    mbar_init(smem_addr(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_h)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool stop = false;
+      for (int mt = blockIdx.x; mt < n_mt && !stop; mt += gridDim.x) {
+        for (int nt = 0; nt < n_nt && !stop; ++nt) {
+          for (int kb = 0; kb < n_kb; ++kb, ++it) {
+            const uint32_t s = it % kStagesL, round = it / kStagesL;
+            if (round > 0 && !lm_wait<false>(smem_addr(&sm.empty[s]), (round - 1) & 1, abort_flag)) {
+              stop = true;
+              break;
+            }
+            const uint32_t fb = smem_addr(&sm.full[s]);
+            mbar_arrive_expect_tx(fb, kStageA + kStageB);
+            tma_load_2d(smem_addr(sm.a[s]), &tmap_h, kb * kBK, mt * kBM, fb);
+            tma_load_2d(smem_addr(sm.b[s]), &tmap_w, kb * kBK, nt * kBN, fb);
+          }
+        }
+      }
+      if (stop)  // copies already issued land before the CTA can exit
+        for (uint32_t k = it > kStagesL ? it - kStagesL : 0; k < it; ++k)
+          lm_wait<true>(smem_addr(&sm.full[k % kStagesL]), (k / kStagesL) & 1, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool stop = false, issued = false;
+      for (int mt = blockIdx.x; mt < n_mt && !stop; mt += gridDim.x) {
+        for (int nt = 0; nt < n_nt && !stop; ++nt, ++acc_it) {
+          const uint32_t buf = acc_it & 1, use = acc_it >> 1;
+          if (use > 0 && !lm_wait<false>(smem_addr(&sm.acc_empty[buf]), (use - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + buf * kBN;
+          for (int kb = 0; kb < n_kb; ++kb, ++it) {
+            const uint32_t s = it % kStagesL;
+            if (!lm_wait<false>(smem_addr(&sm.full[s]), (it / kStagesL) & 1, abort_flag)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_addr(sm.a[s]), b_base = smem_addr(sm.b[s]);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              umma_bf16(d_tmem, smem_desc_sw128(a_base + k * kUmmaK * 2), smem_desc_sw128(b_base + k * kUmmaK * 2),
+                        kIdesc, (kb | k) != 0);
+            issued = true;
+            umma_commit(smem_addr(&sm.empty[s]));  // the stage is free once these MMAs have read it
+          }
+          if (stop) break;
+          umma_commit(smem_addr(&sm.acc_full[buf]));  // accumulator ready for the epilogue
+        }
+      }
+      if (stop && issued) {  // every MMA already issued completes before the memory is freed
+        umma_commit(smem_addr(&sm.drain));
+        lm_wait<true>(smem_addr(&sm.drain), 0, abort_flag);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_it = 0;
+    bool stop = false;
+    for (int mt = blockIdx.x; mt < n_mt && !stop; mt += gridDim.x) {
+      const long long row = static_cast<long long>(mt) * kBM + r_in_tile;
+      const long long y = row < a.R ? a.ids[row] : -1;
+      float m = kFloor, zy = -INFINITY;
+      float2 s2 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
+      for (int nt = 0; nt < n_nt; ++nt, ++acc_it) {
+        const uint32_t buf = acc_it & 1, use = acc_it >> 1;
+        // warp-uniform outcome: the tensor-memory loads below are warp-collective
+        if (!__all_sync(0xffffffffu, lm_wait<false>(smem_addr(&sm.acc_full[buf]), use & 1, abort_flag))) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const long long n0 = static_cast<long long>(nt) * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          float v[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_addr + buf * kBN + c * 32, v);
+          const long long col0 = n0 + c * 32;
+          const int nv = static_cast<int>(min(32LL, max(0LL, a.V - col0)));
+          if (y >= col0 && y < col0 + 32) zy = select32(v, static_cast<int>(y - col0));
+          float vm = kFloor;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nv) vm = max_nan(vm, v[i]);
+          if (vm > m) {  // rescale the running sums to the new max
+            const float d = (vm - m) * kLog2e;
+            const float f = ex2_approx(-d);
+            const float2 f2 = make_float2(f, f), nd2 = make_float2(-d, -d);
+            t2 = __fmul2_rn(f2, __ffma2_rn(nd2, s2, t2));
+            s2 = __fmul2_rn(f2, s2);
+            m = vm;
+          }
+          const float2 L2 = make_float2(kLog2e, kLog2e);
+          const float2 nmL = make_float2(-m * kLog2e, -m * kLog2e);
+          if (nv == 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), L2, nmL);
+              const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              s2 = __fadd2_rn(s2, e);
+              t2 = __ffma2_rn(e, x, t2);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i < nv) {
+                const float x = fmaf(v[i], kLog2e, -m * kLog2e);
+                const float e = ex2_approx(x);
+                s2.x += e;
+                t2.x = fmaf(e, x, t2.x);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sm.acc_empty[buf]));  // the MMA warp may overwrite this accumulator
+      }
+      if (!stop && row < a.R) {
+        const float S = s2.x + s2.y, Tt = t2.x + t2.y;
+        const float log2S = log2f(S);
+        const float lse = fmaf(log2S, kLn2, m);
+        const float H = kLn2 * (log2S - Tt / S);
+        const bool y_ok = y >= 0 && y < a.V;
+        if (a.logp_out) a.logp_out[row] = y_ok ? zy - lse : __int_as_float(0x7fc00000);
+        if (a.entropy_out) a.entropy_out[row] = H;
+        if (a.lse_out) a.lse_out[row] = lse;
+        if (!y_ok && a.status) atomicOr(a.status, RL_DEVERR_ID_RANGE);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0 && a.status) atomicOr(a.status, RL_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_lm_mu;
+EncodeTiled g_encode = nullptr;
+int g_lm_attr_dev = -1;
+
+rl_status encode_fn(EncodeTiled* out) {
+  std::lock_guard<std::mutex> lock(g_lm_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return RL_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  *out = g_encode;
+  return RL_OK;
+}
+
+// 2-D bf16 tensor map [rows, cols] (row stride ld elements), box box_rows x 64, 128B swizzle.
+bool make_map(EncodeTiled enc, CUtensorMap* map, const void* base, long long rows, long long cols, long long ld,
+              uint32_t box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace rl
+
+extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
+                                        long long R, long long D, long long V, const long long* ids,
+                                        float* logp_out, float* entropy_out, float* lse_out,
+                                        unsigned int* status_dev, void* stream) {
+  using namespace rl;
+  if (R < 0 || D < 8 || D % 8 != 0 || V < 1 || V > (1LL << 31) || ld_h < D || ld_w < D)
+    return RL_ERR_SHAPE;
+  if (R == 0) return RL_OK;
+  if (!hidden || !weight || !ids) return RL_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(weight) & 15) ||
+      ((ld_h * 2) & 15) || ((ld_w * 2) & 15))
+    return RL_ERR_ALIGN;
+  EncodeTiled enc = nullptr;
+  if (encode_fn(&enc) != RL_OK) return RL_ERR_CUDA;
+  CUtensorMap mh, mw;
+  if (!make_map(enc, &mh, hidden, R, D, ld_h, kBM) || !make_map(enc, &mw, weight, V, D, ld_w, kBN))
+    return RL_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return RL_ERR_CUDA;
+  const int smem = static_cast<int>(sizeof(LmSmem)) + 1024;
+  {
+    std::lock_guard<std::mutex> lock(g_lm_mu);
+    if (g_lm_attr_dev != dev) {
+      if (cudaFuncSetAttribute(lmhead_logprobs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return RL_ERR_CUDA;
+      g_lm_attr_dev = dev;
+    }
+  }
+  LmArgs args;
+  args.R = R;
+  args.D = D;
+  args.V = V;
+  args.ids = ids;
+  args.logp_out = logp_out;
+  args.entropy_out = entropy_out;
+  args.lse_out = lse_out;
+  args.status = status_dev;
+  const long long n_mt = (R + kBM - 1) / kBM;
+  const int grid = static_cast<int>(n_mt < sms ? n_mt : sms);
+  lmhead_logprobs_kernel<<<grid, kThreadsL, smem, static_cast<cudaStream_t>(stream)>>>(mh, mw, args);
+  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}

@@ -165,3 +165,22 @@ def logits(w: Workload, device="cpu", ld: int | None = None):
     if w.R:
         fill_logits(w, out)
     return out
+
+
+def lmhead_inputs(R: int, D: int, V: int, seed: int, logit_sd: float = 2.0, ld_h: int | None = None,
+                  ld_w: int | None = None):
+    """Host torch bf16 tensors for the LM-head path: hidden [R, ld_h] with
+    entries N(0, 1), weight [V, ld_w] with entries N(0, logit_sd^2 / D), both
+    drawn in float32 and rounded to bf16 (padding columns past D are zero),
+    and ids int64 [R] uniform on [0, V).  hidden @ weight^T then has entries
+    of standard deviation about logit_sd, the spread of the logits above."""
+    import torch
+    ld_h = D if ld_h is None else ld_h
+    ld_w = D if ld_w is None else ld_w
+    gen = torch.Generator().manual_seed(seed)
+    hidden = torch.zeros((R, ld_h), dtype=torch.bfloat16)
+    hidden[:, :D] = torch.randn((R, D), generator=gen).to(torch.bfloat16)
+    weight = torch.zeros((V, ld_w), dtype=torch.bfloat16)
+    weight[:, :D] = (torch.randn((V, D), generator=gen) * (logit_sd / D ** 0.5)).to(torch.bfloat16)
+    ids = torch.randint(0, V, (R,), generator=gen, dtype=torch.int64)
+    return hidden, weight, ids

@@ -179,3 +179,33 @@ def test_desc_null(lib):
 
 def test_fixed_form_rejects_group_rewards_layout(lib):
     assert call_loss(lib, adv_layout=rl.RL_ADV_GROUP_REWARDS) == rl.RL_ERR_DTYPE
+
+
+def call_lmhead(lib, **over):
+    a = dict(hidden=FAKE, ld_h=1024, weight=FAKE + 0x1000000, ld_w=1024, R=256, D=1024, V=151936,
+             ids=FAKE + 0x2000000, logp=FAKE + 0x3000000, ent=None, lse=None, status=None,
+             stream=None)
+    a.update(over)
+    return lib.rl_lmhead_logprobs(a["hidden"], a["ld_h"], a["weight"], a["ld_w"], a["R"], a["D"],
+                                  a["V"], a["ids"], a["logp"], a["ent"], a["lse"], a["status"],
+                                  a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(R=-1), rl.RL_ERR_SHAPE),
+    (dict(D=0), rl.RL_ERR_SHAPE),
+    (dict(D=1020, ld_h=1020, ld_w=1020), rl.RL_ERR_SHAPE),    # D not a multiple of 8
+    (dict(V=0), rl.RL_ERR_SHAPE),
+    (dict(V=(1 << 31) + 1), rl.RL_ERR_SHAPE),
+    (dict(ld_h=1000), rl.RL_ERR_SHAPE),                       # stride below D
+    (dict(ld_w=512), rl.RL_ERR_SHAPE),
+    (dict(hidden=None), rl.RL_ERR_NULL),
+    (dict(weight=None), rl.RL_ERR_NULL),
+    (dict(ids=None), rl.RL_ERR_NULL),
+    (dict(hidden=FAKE + 8), rl.RL_ERR_ALIGN),
+    (dict(weight=FAKE + 0x1000002), rl.RL_ERR_ALIGN),
+    (dict(ld_h=1028), rl.RL_ERR_ALIGN),                       # row stride not a multiple of 16 B
+    (dict(R=0), rl.RL_OK),                                    # nothing to launch
+])
+def test_lmhead_host_errors(lib, over, expect):
+    assert call_lmhead(lib, **over) == expect

@@ -1,0 +1,127 @@
+"""GPU parity of rl_lmhead_logprobs (the LM-head projection fused with the
+row log-softmax statistics, on the tensor cores) against the fp64 oracle:
+the exact product of the bf16 inputs, then lse, log-prob of the sampled id
+and entropy per row.
+
+Tolerance: the kernel accumulates the exact bf16 products in fp32, so each
+logit carries an absolute error of at most about D * 2^-24 * sum|h_d w_vd|
+(a few 1e-6 here); the row statistics then follow the policy-loss kernel's
+fp32 arithmetic, whose bound is LOGP_ATOL (2e-3 absolute) on lse, logp and
+entropy.  Small cases compare every row; the full Qwen3 LM-head shape
+(D = 1024, V = 151936) compares sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ppo_policy_loss_gb300 as rl
+from ppo_policy_loss_gb300 import synth
+from _parity import LOGP_ATOL, storage_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    rl.build()
+    rl.load()
+
+
+def run_gpu(hidden, weight, ids, D, V, status=None):
+    dev = torch.device("cuda:0")
+    h, w, i = hidden.to(dev), weight.to(dev), ids.to(dev)
+    R = hidden.shape[0]
+    lse = torch.full((R,), 7.0, device=dev)
+    logp = torch.full((R,), 7.0, device=dev)
+    ent = torch.full((R,), 7.0, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    rl.rl_lmhead_logprobs(h, h.stride(0), w, w.stride(0), R, D, V, i, logp, ent, lse, st)
+    torch.cuda.synchronize()
+    return lse.cpu().numpy(), logp.cpu().numpy(), ent.cpu().numpy(), int(st.item())
+
+
+def oracle_rows(hidden, weight, ids, D, rows=None):
+    h = storage_np(hidden)[:, :D]
+    w = storage_np(weight)[:, :D]
+    idn = ids.numpy()
+    if rows is not None:
+        h, idn = h[rows], idn[rows]
+    return oracle.lmhead_row_stats(h, w, idn, "bf16")
+
+
+def check(got, ref, rows=slice(None)):
+    for name, g, r in zip(("lse", "logp", "entropy"), got, ref):
+        g = g[rows]
+        assert np.isfinite(g).all(), name
+        err = np.abs(g.astype(np.float64) - r)
+        assert err.max() <= LOGP_ATOL, (name, float(err.max()), int(err.argmax()))
+
+
+@pytest.mark.parametrize("R,D,V,ld_h,ld_w,sd,seed", [
+    (128, 64, 256, None, None, 2.0, 1),          # one tile
+    (128, 128, 512, None, None, 2.0, 2),         # two K blocks, two N tiles
+    (300, 200, 1000, 208, 256, 2.0, 3),          # ragged R, D (zero-filled K tail), V; padded strides
+    (1, 8, 1, None, None, 1.0, 4),               # the smallest shape
+    (257, 64, 33, None, None, 8.0, 5),           # V below one tile, wide logits
+    (640, 256, 4096, None, None, 12.0, 6),       # running-max rescales across tiles
+])
+def test_lmhead_small(R, D, V, ld_h, ld_w, sd, seed):
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, seed, sd, ld_h, ld_w)
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V)
+    assert st == 0
+    check((lse, logp, ent), oracle_rows(hidden, weight, ids, D))
+
+
+def test_lmhead_persistent_tiles():
+    """More 128-row tiles than SMs: CTAs loop over tiles and reuse both
+    tensor-memory accumulators."""
+    R = 128 * 330 + 17
+    hidden, weight, ids = synth.lmhead_inputs(R, 128, 768, 7, 3.0)
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, 128, 768)
+    assert st == 0
+    check((lse, logp, ent), oracle_rows(hidden, weight, ids, 128))
+
+
+def test_lmhead_qwen3_shape_sampled_rows():
+    """The Qwen3-0.6B LM head (D 1024, V 151936) on 32 x 1024 rows; the
+    oracle recomputes 96 sampled rows, including the first and last."""
+    R, D, V = 32 * 1024, 1024, 151936
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 8, 3.0)
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V)
+    assert st == 0
+    assert np.isfinite(lse).all() and np.isfinite(logp).all() and np.isfinite(ent).all()
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([[0, R - 1], rng.choice(R, 94, replace=False)]))
+    ref = oracle_rows(hidden, weight, ids, D, rows)
+    check((lse[rows], logp[rows], ent[rows]), ref)
+    # logp <= 0 and 0 <= H <= log V hold for every row
+    assert (logp <= 1e-5).all() and (ent >= -1e-5).all() and (ent <= np.log(V) + 1e-4).all()
+
+
+def test_lmhead_bad_id_sets_status():
+    hidden, weight, ids = synth.lmhead_inputs(130, 64, 300, 9)
+    ids[5] = 300
+    ids[129] = -1
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, 64, 300)
+    assert st & rl.RL_DEVERR_ID_RANGE
+    assert np.isnan(logp[5]) and np.isnan(logp[129])
+    good = np.setdiff1d(np.arange(130), [5, 129])
+    ids_ok = ids.clone()
+    ids_ok[5] = 0
+    ids_ok[129] = 0
+    ref = oracle_rows(hidden, weight, ids_ok, 64)
+    check((lse, logp, ent), [r[good] for r in ref], good)
+
+
+def test_lmhead_optional_outputs_and_empty():
+    hidden, weight, ids = synth.lmhead_inputs(200, 64, 500, 10)
+    dev = torch.device("cuda:0")
+    h, w, i = hidden.to(dev), weight.to(dev), ids.to(dev)
+    logp = torch.empty(200, device=dev)
+    rl.rl_lmhead_logprobs(h, 64, w, 64, 200, 64, 500, i, logp, None, None, None)
+    torch.cuda.synchronize()
+    ref = oracle_rows(hidden, weight, ids, 64)
+    assert np.abs(logp.cpu().numpy() - ref[1]).max() <= LOGP_ATOL
+    rl.rl_lmhead_logprobs(h, 64, w, 64, 0, 64, 500, i, logp, None, None, None)  # R = 0: no launch
+    torch.cuda.synchronize()

@@ -12,7 +12,7 @@ than L2, so no flush is needed between steps.  ``--workload`` selects one of
 the other configurations (see ppo_policy_loss_gb300/synth.py).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload NAME]
+                    [--workload NAME] [--lmhead]
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own
 batch of the workload on its GPU (weak scaling); by default each rank's loss
@@ -22,6 +22,11 @@ path's one exchange: an all-reduce of the token counts before the loss and
 of the loss shares after).  value = all ranks' tokens / max-over-ranks time.
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
 of the same workload.
+
+``--lmhead`` times the other tensor-core path instead: rl_lmhead_logprobs on
+the Qwen3-0.6B LM head (D=1024, V=151936 bf16) over the same 32 x 1024 rows,
+i.e. the policy's log-probs of the sampled tokens straight from the hidden
+states, with a tensor-core roofline (2 R D V flops per launch).
 """
 from __future__ import annotations
 
@@ -43,6 +48,9 @@ sys.path.insert(0, ROOT)
 METRIC = "fused GRPO loss+dlogits tokens/s at V=151936 bf16; % of HBM roofline"
 WORKLOAD = "qwen3_0p6b_grpo"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+LMHEAD_METRIC = "fused LM-head + log-softmax rows/s (Qwen3-0.6B head D=1024, V=151936 bf16); % of tensor roofline"
+LMHEAD_SHAPE = dict(R=32 * 1024, D=1024, V=151936, logit_sd=3.0, seed=202)
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
 DESCRIBE = {
     "tiny_grpo": "tiny GRPO: 2 prompts x group 4 = 8 seqs, T=16, V=1024 fp32",
@@ -66,6 +74,15 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def hbm_peak():
@@ -578,6 +595,185 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ----------------------------------------------------------------------------- LM-head leg
+def lmhead_config(R, D, V):
+    return {"workload": f"qwen3_0p6b_lmhead: {R} rows (32 seqs x T=1024) x D={D} hidden -> "
+                        f"V={V} bf16 LM head, hidden ~N(0,1), W ~N(0, 9/D), ids uniform",
+            "rows": R, "D": D, "V": V,
+            "l2": f"weight {V * D * 2 / 1e9:.2f} GB > 129 MB L2, swept every launch; no flush"}
+
+
+def lmhead_inputs_dev(dev):
+    import torch
+    c = LMHEAD_SHAPE
+    g = torch.Generator(device=dev).manual_seed(c["seed"])
+    h = torch.randn((c["R"], c["D"]), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((c["V"], c["D"]), generator=g, device=dev)
+         * (c["logit_sd"] / c["D"] ** 0.5)).to(torch.bfloat16)
+    ids = torch.randint(0, c["V"], (c["R"],), generator=g, device=dev)
+    return h, w, ids
+
+
+def lmhead_cpu(h, w, ids, budget_s, n_rows=64):
+    """The oracle (fp64 matmul, then row statistics) on a sample of rows."""
+    import oracle
+    rows = np.unique(np.linspace(0, h.shape[0] - 1, n_rows).round().astype(np.int64))
+    hs, ws_, idn = _storage(h[rows].cpu()), _storage(w.cpu()), ids.cpu().numpy()[rows]
+    threads = oracle.default_threads()
+    t0, done = time.time(), 0
+    while True:
+        oracle.lmhead_row_stats(hs, ws_, idn, "bf16", threads)
+        done += rows.size
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": done / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{rows.size} rows spread over the {h.shape[0]}-row batch, full V={w.shape[0]}, "
+                       f"D={w.shape[1]}; numpy fp64 matmul + C row statistics, repeated for "
+                       f"{dt:.1f} s")}
+
+
+def run_lmhead(args):
+    import torch
+
+    import ppo_policy_loss_gb300 as rl
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    rl.build()
+    rl.load()
+    h, w, ids = lmhead_inputs_dev(dev)
+    R, D = h.shape
+    V = w.shape[0]
+    logp = torch.empty(R, device=dev)
+    ent = torch.empty(R, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(max(16, rl.rl_lmhead_workspace_size(R, V)), dtype=torch.uint8, device=dev)
+    n_sl, grid, _ = rl.rl_lmhead_plan(R, V, ws.numel())
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(hh, out_lp, out_en):
+        rl.rl_lmhead_logprobs(hh, D, w, D, R, D, V, ids, out_lp, out_en, None, status, ws,
+                              ws.numel(), stream)
+
+    for _ in range(args.warmup):
+        launch(h, logp, ent)
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(int(vis.split(",")[local]) if vis else local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    sampler.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(args.steps):
+        kev[i][0].record(stream)
+        launch(h, logp, ent)
+        kev[i][1].record(stream)
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    ms_step = max_over_ranks(t0.elapsed_time(t1), dev) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    flops = 2.0 * R * D * V
+    peak, peak_kind = bf16_peak()
+    achieved = flops / (kern_ms / 1e3) / 1e12
+
+    # end to end: hidden states and ids uploaded from pinned host memory, the
+    # log-probs and entropies read back, every step (the weight stays resident)
+    e2e = None
+    if args.e2e_steps > 0:
+        hh = torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
+        hh.copy_(h)
+        hid = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True)
+        hid.copy_(ids)
+        o_lp = torch.empty(R, pin_memory=True)
+        o_en = torch.empty(R, pin_memory=True)
+        dh, dids = torch.empty_like(h), torch.empty_like(ids)
+        steps = max(1, min(args.steps, args.e2e_steps))
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            dh.copy_(hh, non_blocking=True)
+            dids.copy_(hid, non_blocking=True)
+            rl.rl_lmhead_logprobs(dh, D, w, D, R, D, V, dids, logp, ent, None, status, ws,
+                                  ws.numel(), stream)
+            o_lp.copy_(logp, non_blocking=True)
+            o_en.copy_(ent, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1), dev) / steps
+        e2e = {"value": world * R / (ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": R * D * 2 + R * 8, "d2h_bytes_per_step": 2 * R * 4,
+               "ms_per_step": ms, "steps": steps,
+               "note": "LM-head weight resident on the device (model state)"}
+    out = {
+        "metric": LMHEAD_METRIC, "value": world * R / (ms_step / 1e3), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded)", "config": dict(lmhead_config(R, D, V),
+                                                    parallelism="replicas" if world > 1 else "single GPU",
+                                                    split={"vocab_slices": n_sl, "ctas": grid}),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": None,
+                     "alg_flops_per_launch": flops, "kernel": "rl_lmhead_logprobs",
+                     "kernel_ms": kern_ms},
+        "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = lmhead_cpu(h, w, ids, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_lmhead_reference(args):
+    """Reference arm of the LM-head leg: the oracle on host cores, bounded sample."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    c = LMHEAD_SHAPE
+    h, w, ids = lmhead_inputs_dev(torch.device("cpu"))
+    n = 16   # rows per step: each pass also decodes the whole weight to fp64
+    base = lmhead_cpu(h, w, ids, 0.0, n)
+    for _ in range(args.warmup - 1):
+        lmhead_cpu(h, w, ids, 0.0, n)
+    t0 = time.time()
+    for _ in range(args.steps):
+        lmhead_cpu(h, w, ids, 0.0, n)
+    dt = time.time() - t0
+    value = args.steps * n / dt
+    print(json.dumps({
+        "metric": LMHEAD_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": dict(lmhead_config(c["R"], c["D"], c["V"]), step_sample_rows=n),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": base["cores"],
+                         "kind": "oracle", "sample": "each step: " + base["sample"]},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,10 +791,14 @@ def main():
                     help="with N > 1: normalise by the token count summed over ranks")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profiling only: keep the first SEQS sequences")
+    ap.add_argument("--lmhead", action="store_true",
+                    help="time rl_lmhead_logprobs on the Qwen3-0.6B LM head instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.lmhead:
+        (run_lmhead_reference if args.impl == "reference" else run_lmhead)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -400,16 +400,43 @@ rl_status rl_value_loss_fwd_bwd(const float* values, const float* values_old,
  *   logp_out, entropy_out, lse_out : float [R] device, each may be NULL;
  *   status_dev : one unsigned int in device memory or NULL; the kernel ORs
  *            RL_DEVERR_ID_RANGE (an id outside [0, V)) or RL_DEVERR_TIMEOUT
- *            (a bounded on-chip wait gave up; outputs are garbage) into it.
+ *            (a bounded on-chip wait gave up; outputs are garbage) into it;
+ *   workspace : optional device scratch (16-byte aligned) of workspace_bytes,
+ *            zero-filled before its first use; every call leaves it
+ *            zero-filled again, except one that timed out.  With it the
+ *            launch may cut the vocabulary into slices so that the work
+ *            spreads evenly over the SMs (see rl_lmhead_workspace_size); NULL
+ *            or too small a workspace gives the unsliced launch, with the same
+ *            results up to fp32 rounding order.  Calls sharing a workspace
+ *            must not overlap on the GPU.
  * One launch of a persistent tensor-core kernel (tcgen05, TMA, tensor memory).
- * Allocates nothing; stream-ordered.  Errors: RL_ERR_SHAPE (R < 0, V < 1,
- * V > 2^31, D < 8, D not a multiple of 8, a stride below D), RL_ERR_NULL,
- * RL_ERR_ALIGN, RL_ERR_CUDA.  R == 0 launches nothing.
+ * Allocates nothing; stream-ordered.  Errors: RL_ERR_SHAPE (R < 0, R >= 2^31,
+ * V < 1, V > 2^31, D < 8, D not a multiple of 8, a stride below D),
+ * RL_ERR_NULL, RL_ERR_ALIGN, RL_ERR_CUDA.  R == 0 launches nothing.
  */
 rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
                              long long R, long long D, long long V, const long long* ids,
                              float* logp_out, float* entropy_out, float* lse_out,
-                             unsigned int* status_dev, void* stream);
+                             unsigned int* status_dev, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * Workspace bytes rl_lmhead_logprobs needs for its best work split of R rows
+ * over V on the current device (0 when the unsliced launch is already the
+ * best, or the shape is invalid, or no device answers).  Host-only query.
+ */
+size_t rl_lmhead_workspace_size(long long R, long long V);
+
+/*
+ * The work split rl_lmhead_logprobs would use with workspace_bytes of
+ * workspace on a GPU of sm_count SMs (sm_count < 1: the current device):
+ * vocabulary slices per 128-row tile, CTAs in the persistent grid and the
+ * workspace bytes that split uses (0 when unsliced).  Any output pointer may
+ * be NULL.  Host-only; with sm_count >= 1 it needs no GPU.  Errors:
+ * RL_ERR_SHAPE (R < 1 or as rl_lmhead_logprobs), RL_ERR_CUDA.
+ */
+rl_status rl_lmhead_plan(long long R, long long V, size_t workspace_bytes, int sm_count,
+                         int* n_slices, int* grid, size_t* workspace_needed);
 
 /*
  * The launch shape rl_policy_loss_fwd_bwd would use on the current device for

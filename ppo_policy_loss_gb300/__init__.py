@@ -35,6 +35,7 @@ __all__ = [
     "rl_policy_loss_desc", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
     "rl_read_device_status", "rl_masked_whiten", "rl_count_tokens", "rl_value_loss_fwd_bwd",
     "rl_value_stats", "value_stats_from_bytes", "rl_lmhead_logprobs",
+    "rl_lmhead_workspace_size", "rl_lmhead_plan",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -103,7 +104,12 @@ def load(path: str | None = None):
     lib.rl_value_loss_fwd_bwd.argtypes = [P, P, P, P, LL, F, F, P, P, P]
     lib.rl_masked_whiten.argtypes = [P, P, LL, D, I, P, P]
     lib.rl_count_tokens.argtypes = [P, LL, LL, P, P]
-    lib.rl_lmhead_logprobs.argtypes = [P, LL, P, LL, LL, LL, LL, P, P, P, P, P, P]
+    lib.rl_lmhead_logprobs.argtypes = [P, LL, P, LL, LL, LL, LL, P, P, P, P, P, P, SZ, P]
+    lib.rl_lmhead_workspace_size.argtypes = [LL, LL]
+    lib.rl_lmhead_workspace_size.restype = SZ
+    lib.rl_lmhead_plan.argtypes = [LL, LL, SZ, I, ctypes.POINTER(I), ctypes.POINTER(I),
+                                   ctypes.POINTER(SZ)]
+    lib.rl_lmhead_plan.restype = I
     lib.rl_count_tokens.restype = I
     lib.rl_masked_whiten.restype = I
     lib.rl_lmhead_logprobs.restype = I
@@ -226,10 +232,26 @@ def value_stats_from_bytes(raw: bytes) -> dict:
 
 
 def rl_lmhead_logprobs(hidden, ld_h, weight, ld_w, R, D, V, ids, logp_out, entropy_out, lse_out,
-                       status_dev=None, stream=None):
+                       status_dev=None, workspace=None, workspace_bytes=0, stream=None):
+    if workspace is not None and hasattr(workspace, "numel") and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
     _check(load().rl_lmhead_logprobs(_ptr(hidden), ld_h, _ptr(weight), ld_w, R, D, V, _ptr(ids),
                                      _ptr(logp_out), _ptr(entropy_out), _ptr(lse_out),
-                                     _ptr(status_dev), _stream(stream)), "rl_lmhead_logprobs")
+                                     _ptr(status_dev), _ptr(workspace), workspace_bytes,
+                                     _stream(stream)), "rl_lmhead_logprobs")
+
+
+def rl_lmhead_workspace_size(R, V) -> int:
+    return int(load().rl_lmhead_workspace_size(R, V))
+
+
+def rl_lmhead_plan(R, V, workspace_bytes, sm_count=0):
+    """(vocabulary slices per row tile, CTAs, workspace bytes used) of the launch
+    on a GPU of ``sm_count`` SMs (0: the current device)."""
+    ns, grid, need = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
+    _check(load().rl_lmhead_plan(R, V, workspace_bytes, sm_count, ctypes.byref(ns),
+                                 ctypes.byref(grid), ctypes.byref(need)), "rl_lmhead_plan")
+    return ns.value, grid.value, need.value
 
 
 def rl_policy_loss_launch_shape(dtype, V, n_rows):

@@ -22,8 +22,14 @@
 //     time, online (max, sum 2^x, sum 2^x x) per row, the sampled id's logit,
 //     then lse, log-prob and entropy per row.  Freeing each accumulator lets
 //     the MMAs of the next tile overlap this epilogue.
-//   * Persistent over 128-row tiles; all CTAs sweep W in step, so its tiles
-//     are shared through L2.
+//   * Persistent over work units (128-row tile, vocabulary slice): the host
+//     splits V into S slices so that the units spread evenly over the SMs
+//     (S = 1 when the row tiles alone do).  Units are dealt out round-robin,
+//     so the CTAs working at one time sweep the same slice of W in step and
+//     share its tiles through L2.  With S > 1 each unit leaves per-row partial
+//     statistics (max, sums, sampled logit) in the caller's workspace; the
+//     last unit of a row tile to finish, found with a per-tile ticket, merges
+//     the S partials in slice order (deterministic) and writes the outputs.
 //   * Every mbarrier wait is bounded; on timeout the kernel raises an error
 //     flag, waits for its own copies and tensor-core work, frees its tensor
 //     memory and exits.
@@ -56,10 +62,14 @@ struct LmSmem {
   unsigned long long drain;
   uint32_t tmem_base;
   int abort;
+  int merge;  // this unit completes its row tile (vocabulary slices > 1)
 };
 
 struct LmArgs {
   long long R, D, V;
+  int n_mt, n_nt, n_slices;
+  unsigned int* tickets;  // [n_mt] (n_slices > 1)
+  float4* partials;       // [n_slices][R]: (max, sum 2^x, sum 2^x x, sampled logit)
   const long long* ids;
   float* logp_out;
   float* entropy_out;
@@ -123,6 +133,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// First vocabulary tile of slice vs when n_nt tiles are cut into n_sl slices.
+__device__ __forceinline__ int slice_begin(int vs, int n_nt, int n_sl) {
+  return static_cast<int>(static_cast<long long>(vs) * n_nt / n_sl);
+}
+
 // v[j] through a tree of selects on the bits of j (constant register
 // indices only, so v stays in registers).
 __device__ __forceinline__ float select32(const float (&v)[32], int j) {
@@ -174,8 +189,7 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
   LmSmem& sm = *reinterpret_cast<LmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abort_flag = &sm.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_mt = static_cast<int>((a.R + kBM - 1) / kBM);
-  const int n_nt = static_cast<int>((a.V + kBN - 1) / kBN);
+  const int n_mt = a.n_mt, n_nt = a.n_nt, n_sl = a.n_slices, n_units = n_mt * n_sl;
   const int n_kb = static_cast<int>((a.D + kBK - 1) / kBK);  // columns past D read as zeros
 
   if (tid == 0) {
@@ -207,8 +221,9 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
     if (lane == 0) {
       uint32_t it = 0;
       bool stop = false;
-      for (int mt = blockIdx.x; mt < n_mt && !stop; mt += gridDim.x) {
-        for (int nt = 0; nt < n_nt && !stop; ++nt) {
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const int mt = u % n_mt, vs = u / n_mt;
+        for (int nt = slice_begin(vs, n_nt, n_sl); nt < slice_begin(vs + 1, n_nt, n_sl) && !stop; ++nt) {
           for (int kb = 0; kb < n_kb; ++kb, ++it) {
             const uint32_t s = it % kStagesL, round = it / kStagesL;
             if (round > 0 && !lm_wait<false>(smem_addr(&sm.empty[s]), (round - 1) & 1, abort_flag)) {
@@ -231,8 +246,9 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
       bool stop = false, issued = false;
-      for (int mt = blockIdx.x; mt < n_mt && !stop; mt += gridDim.x) {
-        for (int nt = 0; nt < n_nt && !stop; ++nt, ++acc_it) {
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const int vs = u / n_mt;
+        for (int nt = slice_begin(vs, n_nt, n_sl); nt < slice_begin(vs + 1, n_nt, n_sl) && !stop; ++nt, ++acc_it) {
           const uint32_t buf = acc_it & 1, use = acc_it >> 1;
           if (use > 0 && !lm_wait<false>(smem_addr(&sm.acc_empty[buf]), (use - 1) & 1, abort_flag)) {
             stop = true;
@@ -271,12 +287,13 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t acc_it = 0;
     bool stop = false;
-    for (int mt = blockIdx.x; mt < n_mt && !stop; mt += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      const int mt = u % n_mt, vs = u / n_mt;
       const long long row = static_cast<long long>(mt) * kBM + r_in_tile;
       const long long y = row < a.R ? a.ids[row] : -1;
       float m = kFloor, zy = -INFINITY;
       float2 s2 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
-      for (int nt = 0; nt < n_nt; ++nt, ++acc_it) {
+      for (int nt = slice_begin(vs, n_nt, n_sl); nt < slice_begin(vs + 1, n_nt, n_sl); ++nt, ++acc_it) {
         const uint32_t buf = acc_it & 1, use = acc_it >> 1;
         // warp-uniform outcome: the tensor-memory loads below are warp-collective
         if (!__all_sync(0xffffffffu, lm_wait<false>(smem_addr(&sm.acc_full[buf]), use & 1, abort_flag))) {
@@ -330,8 +347,38 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.acc_empty[buf]));  // the MMA warp may overwrite this accumulator
       }
-      if (!stop && row < a.R) {
-        const float S = s2.x + s2.y, Tt = t2.x + t2.y;
+      float S = s2.x + s2.y, Tt = t2.x + t2.y;
+      bool finish = true;
+      if (n_sl > 1) {
+        // Leave this slice's partial, then take the row tile's ticket.  Every
+        // epilogue thread reaches these barriers once per unit, stopped or not.
+        if (!stop && row < a.R)
+          __stcg(&a.partials[static_cast<long long>(vs) * a.R + row], make_float4(m, S, Tt, zy));
+        __threadfence();
+        stop = named_barrier_or(1, 4 * 32, stop);
+        if (tid == 2 * 32 && !stop)
+          sm.merge = atomicInc(&a.tickets[mt], n_sl - 1) == static_cast<unsigned>(n_sl - 1);
+        named_barrier(1, 4 * 32);
+        finish = !stop && sm.merge;
+        if (finish && row < a.R) {
+          __threadfence();
+          m = kFloor;
+          for (int k = 0; k < n_sl; ++k)
+            m = max_nan(m, __ldcg(&a.partials[static_cast<long long>(k) * a.R + row]).x);
+          S = 0.f;
+          Tt = 0.f;
+          zy = -INFINITY;
+          for (int k = 0; k < n_sl; ++k) {  // slice order: the result does not depend on arrival order
+            const float4 pk = __ldcg(&a.partials[static_cast<long long>(k) * a.R + row]);
+            const float d = (m - pk.x) * kLog2e;
+            const float f = ex2_approx(-d);
+            Tt += f * (pk.z - d * pk.y);
+            S += f * pk.y;
+            zy = fmaxf(zy, pk.w);
+          }
+        }
+      }
+      if (finish && !stop && row < a.R) {
         const float log2S = log2f(S);
         const float lse = fmaf(log2S, kLn2, m);
         const float H = kLn2 * (log2S - Tt / S);
@@ -390,20 +437,94 @@ bool make_map(EncodeTiled enc, CUtensorMap* map, const void* base, long long row
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Work split: S vocabulary slices per 128-row tile, chosen to minimise the
+// busiest CTA's tile count under the round-robin deal (with half a tile of
+// overhead per unit), within the workspace the caller gave.
+constexpr int kMaxSlices = 1024;
+
+struct LmPlan {
+  int n_mt, n_nt, n_slices, grid;
+  size_t ws_bytes;
+};
+
+size_t ticket_bytes(long long n_mt) { return (static_cast<size_t>(n_mt) * 4 + 255) & ~size_t(255); }
+
+size_t lm_ws_bytes(long long R, long long n_mt, int n_sl) {
+  if (n_sl <= 1) return 0;
+  return ticket_bytes(n_mt) + static_cast<size_t>(n_sl) * static_cast<size_t>(R) * 16;
+}
+
+LmPlan lm_plan(long long R, long long V, int sms, size_t ws_cap) {
+  LmPlan p;
+  p.n_mt = static_cast<int>((R + kBM - 1) / kBM);
+  p.n_nt = static_cast<int>((V + kBN - 1) / kBN);
+  auto cost = [&](int S) {
+    const long long units = static_cast<long long>(p.n_mt) * S;
+    const long long g = units < sms ? units : sms;
+    return static_cast<double>((units + g - 1) / g) * ((p.n_nt + S - 1) / S + 0.5);
+  };
+  int best = 1;
+  double best_cost = cost(1);
+  const int s_max = p.n_nt < kMaxSlices ? p.n_nt : kMaxSlices;
+  for (int S = 2; S <= s_max; ++S) {
+    if (lm_ws_bytes(R, p.n_mt, S) > ws_cap || static_cast<long long>(p.n_mt) * S > (1LL << 30)) break;
+    const double c = cost(S);
+    if (c < best_cost * 0.999) {
+      best = S;
+      best_cost = c;
+    }
+  }
+  p.n_slices = best;
+  const long long units = static_cast<long long>(p.n_mt) * best;
+  p.grid = static_cast<int>(units < sms ? units : sms);
+  p.ws_bytes = lm_ws_bytes(R, p.n_mt, best);
+  return p;
+}
+
+rl_status device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || *sms < 1)
+    return RL_ERR_CUDA;
+  return RL_OK;
+}
+
+bool lm_shape_ok(long long R, long long V) { return R >= 0 && R < (1LL << 31) && V >= 1 && V <= (1LL << 31); }
+
 }  // namespace
 }  // namespace rl
+
+extern "C" size_t rl_lmhead_workspace_size(long long R, long long V) {
+  using namespace rl;
+  int sms = 0;
+  if (R < 1 || !lm_shape_ok(R, V) || device_sms(&sms) != RL_OK) return 0;
+  return lm_plan(R, V, sms, ~size_t(0)).ws_bytes;
+}
+
+extern "C" rl_status rl_lmhead_plan(long long R, long long V, size_t workspace_bytes, int sm_count,
+                                    int* n_slices, int* grid, size_t* workspace_needed) {
+  using namespace rl;
+  if (R < 1 || !lm_shape_ok(R, V)) return RL_ERR_SHAPE;
+  int sms = sm_count;
+  if (sms < 1 && device_sms(&sms) != RL_OK) return RL_ERR_CUDA;
+  const LmPlan p = lm_plan(R, V, sms, workspace_bytes);
+  if (n_slices) *n_slices = p.n_slices;
+  if (grid) *grid = p.grid;
+  if (workspace_needed) *workspace_needed = p.ws_bytes;
+  return RL_OK;
+}
 
 extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
                                         long long R, long long D, long long V, const long long* ids,
                                         float* logp_out, float* entropy_out, float* lse_out,
-                                        unsigned int* status_dev, void* stream) {
+                                        unsigned int* status_dev, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
   using namespace rl;
-  if (R < 0 || D < 8 || D % 8 != 0 || V < 1 || V > (1LL << 31) || ld_h < D || ld_w < D)
-    return RL_ERR_SHAPE;
+  if (!lm_shape_ok(R, V) || D < 8 || D % 8 != 0 || ld_h < D || ld_w < D) return RL_ERR_SHAPE;
   if (R == 0) return RL_OK;
   if (!hidden || !weight || !ids) return RL_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(weight) & 15) ||
-      ((ld_h * 2) & 15) || ((ld_w * 2) & 15))
+      ((ld_h * 2) & 15) || ((ld_w * 2) & 15) || (reinterpret_cast<uintptr_t>(workspace) & 15))
     return RL_ERR_ALIGN;
   EncodeTiled enc = nullptr;
   if (encode_fn(&enc) != RL_OK) return RL_ERR_CUDA;
@@ -411,9 +532,7 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
   if (!make_map(enc, &mh, hidden, R, D, ld_h, kBM) || !make_map(enc, &mw, weight, V, D, ld_w, kBN))
     return RL_ERR_CUDA;
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return RL_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || device_sms(&sms) != RL_OK) return RL_ERR_CUDA;
   const int smem = static_cast<int>(sizeof(LmSmem)) + 1024;
   {
     std::lock_guard<std::mutex> lock(g_lm_mu);
@@ -424,17 +543,23 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
       g_lm_attr_dev = dev;
     }
   }
+  const LmPlan plan = lm_plan(R, V, sms, workspace ? workspace_bytes : 0);
   LmArgs args;
   args.R = R;
   args.D = D;
   args.V = V;
+  args.n_mt = plan.n_mt;
+  args.n_nt = plan.n_nt;
+  args.n_slices = plan.n_slices;
+  args.tickets = plan.n_slices > 1 ? static_cast<unsigned int*>(workspace) : nullptr;
+  args.partials = plan.n_slices > 1
+                      ? reinterpret_cast<float4*>(static_cast<char*>(workspace) + ticket_bytes(plan.n_mt))
+                      : nullptr;
   args.ids = ids;
   args.logp_out = logp_out;
   args.entropy_out = entropy_out;
   args.lse_out = lse_out;
   args.status = status_dev;
-  const long long n_mt = (R + kBM - 1) / kBM;
-  const int grid = static_cast<int>(n_mt < sms ? n_mt : sms);
-  lmhead_logprobs_kernel<<<grid, kThreadsL, smem, static_cast<cudaStream_t>(stream)>>>(mh, mw, args);
+  lmhead_logprobs_kernel<<<plan.grid, kThreadsL, smem, static_cast<cudaStream_t>(stream)>>>(mh, mw, args);
   return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }

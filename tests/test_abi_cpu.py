@@ -184,11 +184,11 @@ def test_fixed_form_rejects_group_rewards_layout(lib):
 def call_lmhead(lib, **over):
     a = dict(hidden=FAKE, ld_h=1024, weight=FAKE + 0x1000000, ld_w=1024, R=256, D=1024, V=151936,
              ids=FAKE + 0x2000000, logp=FAKE + 0x3000000, ent=None, lse=None, status=None,
-             stream=None)
+             ws=None, ws_bytes=0, stream=None)
     a.update(over)
     return lib.rl_lmhead_logprobs(a["hidden"], a["ld_h"], a["weight"], a["ld_w"], a["R"], a["D"],
                                   a["V"], a["ids"], a["logp"], a["ent"], a["lse"], a["status"],
-                                  a["stream"])
+                                  a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("over,expect", [
@@ -205,7 +205,40 @@ def call_lmhead(lib, **over):
     (dict(hidden=FAKE + 8), rl.RL_ERR_ALIGN),
     (dict(weight=FAKE + 0x1000002), rl.RL_ERR_ALIGN),
     (dict(ld_h=1028), rl.RL_ERR_ALIGN),                       # row stride not a multiple of 16 B
+    (dict(ws=FAKE + 0x4000008, ws_bytes=1 << 20), rl.RL_ERR_ALIGN),
+    (dict(R=1 << 31), rl.RL_ERR_SHAPE),
     (dict(R=0), rl.RL_OK),                                    # nothing to launch
 ])
 def test_lmhead_host_errors(lib, over, expect):
     assert call_lmhead(lib, **over) == expect
+
+
+def test_lmhead_plan_rejects_bad_shapes(lib):
+    with pytest.raises(rl.RlLossError):
+        rl.rl_lmhead_plan(0, 1000, 0, 152)
+    with pytest.raises(rl.RlLossError):
+        rl.rl_lmhead_plan(128, 0, 0, 152)
+
+
+@pytest.mark.parametrize("R,V", [(32768, 151936), (65536, 151936), (1024, 151936), (128, 151936),
+                                 (16384, 32000), (300, 1000), (40000, 768)])
+def test_lmhead_plan_balances_the_sms(lib, R, V):
+    """The chosen split keeps the busiest CTA within a few percent of an even
+    share of the 128 x 256 tiles (where the tile count allows), and without
+    workspace the launch is unsliced."""
+    sms = 152
+    n_mt, n_nt = -(-R // 128), -(-V // 256)
+    ns, grid, need = rl.rl_lmhead_plan(R, V, 1 << 40, sms)
+    assert 1 <= ns <= n_nt and grid == min(sms, n_mt * ns)
+    if ns > 1:
+        assert need >= ns * R * 16 + n_mt * 4
+    # busiest CTA under the round-robin deal, in tiles
+    load = [0] * grid
+    for u in range(n_mt * ns):
+        vs = u // n_mt
+        load[u % grid] += (vs + 1) * n_nt // ns - vs * n_nt // ns
+    ideal = n_mt * n_nt / sms
+    if ideal >= 8:
+        assert max(load) <= 1.06 * ideal, (ns, max(load), ideal)
+    assert rl.rl_lmhead_plan(R, V, 0, sms)[0] == 1
+    assert rl.rl_lmhead_plan(R, V, 0, sms)[2] == 0

@@ -28,16 +28,27 @@ def _built():
     rl.load()
 
 
-def run_gpu(hidden, weight, ids, D, V, status=None):
+def run_gpu(hidden, weight, ids, D, V, status=None, sliced=True, ws_bytes=None, dev_inputs=None):
+    """Run the kernel; with ``sliced`` the call gets a zeroed workspace (of
+    ``ws_bytes``, default the library's size for this shape), which it must
+    leave zeroed again."""
     dev = torch.device("cuda:0")
-    h, w, i = hidden.to(dev), weight.to(dev), ids.to(dev)
-    R = hidden.shape[0]
+    h, w, i = dev_inputs if dev_inputs is not None else (hidden.to(dev), weight.to(dev), ids.to(dev))
+    R = h.shape[0]
     lse = torch.full((R,), 7.0, device=dev)
     logp = torch.full((R,), 7.0, device=dev)
     ent = torch.full((R,), 7.0, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
-    rl.rl_lmhead_logprobs(h, h.stride(0), w, w.stride(0), R, D, V, i, logp, ent, lse, st)
+    ws = None
+    if sliced:
+        nb = rl.rl_lmhead_workspace_size(R, V) if ws_bytes is None else ws_bytes
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=dev)
+    rl.rl_lmhead_logprobs(h, h.stride(0), w, w.stride(0), R, D, V, i, logp, ent, lse, st,
+                          ws, ws.numel() if ws is not None else 0)
     torch.cuda.synchronize()
+    if ws is not None and rl.rl_lmhead_plan(R, V, ws.numel())[0] > 1:
+        n_mt = -(-R // 128)
+        assert int(ws[: n_mt * 4].view(torch.int32).abs().sum()) == 0, "tickets not reset"
     return lse.cpu().numpy(), logp.cpu().numpy(), ent.cpu().numpy(), int(st.item())
 
 
@@ -58,6 +69,7 @@ def check(got, ref, rows=slice(None)):
         assert err.max() <= LOGP_ATOL, (name, float(err.max()), int(err.argmax()))
 
 
+@pytest.mark.parametrize("sliced", [False, True])
 @pytest.mark.parametrize("R,D,V,ld_h,ld_w,sd,seed", [
     (128, 64, 256, None, None, 2.0, 1),          # one tile
     (128, 128, 512, None, None, 2.0, 2),         # two K blocks, two N tiles
@@ -66,21 +78,47 @@ def check(got, ref, rows=slice(None)):
     (257, 64, 33, None, None, 8.0, 5),           # V below one tile, wide logits
     (640, 256, 4096, None, None, 12.0, 6),       # running-max rescales across tiles
 ])
-def test_lmhead_small(R, D, V, ld_h, ld_w, sd, seed):
+def test_lmhead_small(R, D, V, ld_h, ld_w, sd, seed, sliced):
     hidden, weight, ids = synth.lmhead_inputs(R, D, V, seed, sd, ld_h, ld_w)
-    lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V)
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V, sliced=sliced)
     assert st == 0
     check((lse, logp, ent), oracle_rows(hidden, weight, ids, D))
 
 
-def test_lmhead_persistent_tiles():
-    """More 128-row tiles than SMs: CTAs loop over tiles and reuse both
+@pytest.mark.parametrize("sliced", [False, True])
+def test_lmhead_persistent_tiles(sliced):
+    """More 128-row tiles than SMs: CTAs loop over units and reuse both
     tensor-memory accumulators."""
     R = 128 * 330 + 17
     hidden, weight, ids = synth.lmhead_inputs(R, 128, 768, 7, 3.0)
-    lse, logp, ent, st = run_gpu(hidden, weight, ids, 128, 768)
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, 128, 768, sliced=sliced)
     assert st == 0
     check((lse, logp, ent), oracle_rows(hidden, weight, ids, 128))
+
+
+def test_lmhead_slice_counts_agree():
+    """Workspaces that cap the split at different slice counts (1, 2, 3 and
+    the library's choice) give the oracle's statistics on every row, and a
+    repeated call with one workspace is bitwise identical (the partials are
+    merged in slice order, whatever order the units finish in)."""
+    R, D, V = 1000, 256, 151936 // 4
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 11, 3.0)
+    ref = oracle_rows(hidden, weight, ids, D)
+    dev = torch.device("cuda:0")
+    dev_in = (hidden.to(dev), weight.to(dev), ids.to(dev))
+    n_mt = -(-R // 128)
+    seen = set()
+    for k in (1, 2, 3, None):
+        nb = None if k is None else ((n_mt * 4 + 255) // 256 * 256 + k * R * 16 if k > 1 else 0)
+        ns = rl.rl_lmhead_plan(R, V, rl.rl_lmhead_workspace_size(R, V) if nb is None else nb)[0]
+        seen.add(ns)
+        got = run_gpu(None, None, None, D, V, ws_bytes=nb, dev_inputs=dev_in)
+        assert got[3] == 0
+        check(got[:3], ref)
+        again = run_gpu(None, None, None, D, V, ws_bytes=nb, dev_inputs=dev_in)
+        for a_, b_ in zip(got[:3], again[:3]):
+            assert np.array_equal(a_, b_)
+    assert len(seen) >= 3, seen
 
 
 def test_lmhead_qwen3_shape_sampled_rows():
@@ -88,6 +126,7 @@ def test_lmhead_qwen3_shape_sampled_rows():
     oracle recomputes 96 sampled rows, including the first and last."""
     R, D, V = 32 * 1024, 1024, 151936
     hidden, weight, ids = synth.lmhead_inputs(R, D, V, 8, 3.0)
+    assert rl.rl_lmhead_plan(R, V, rl.rl_lmhead_workspace_size(R, V))[0] > 1
     lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V)
     assert st == 0
     assert np.isfinite(lse).all() and np.isfinite(logp).all() and np.isfinite(ent).all()

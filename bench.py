@@ -597,20 +597,21 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- LM-head leg
 def lmhead_config(R, D, V):
-    return {"workload": f"qwen3_0p6b_lmhead: {R} rows (32 seqs x T=1024) x D={D} hidden -> "
+    rows = "32 seqs x T=1024" if R == LMHEAD_SHAPE["R"] else "profiling slice"
+    return {"workload": f"qwen3_0p6b_lmhead: {R} rows ({rows}) x D={D} hidden -> "
                         f"V={V} bf16 LM head, hidden ~N(0,1), W ~N(0, 9/D), ids uniform",
             "rows": R, "D": D, "V": V,
             "l2": f"weight {V * D * 2 / 1e9:.2f} GB > 129 MB L2, swept every launch; no flush"}
 
 
-def lmhead_inputs_dev(dev):
+def lmhead_inputs_dev(dev, rows=0):
     import torch
     c = LMHEAD_SHAPE
     g = torch.Generator(device=dev).manual_seed(c["seed"])
-    h = torch.randn((c["R"], c["D"]), generator=g, device=dev).to(torch.bfloat16)
+    h = torch.randn((rows or c["R"], c["D"]), generator=g, device=dev).to(torch.bfloat16)
     w = (torch.randn((c["V"], c["D"]), generator=g, device=dev)
          * (c["logit_sd"] / c["D"] ** 0.5)).to(torch.bfloat16)
-    ids = torch.randint(0, c["V"], (c["R"],), generator=g, device=dev)
+    ids = torch.randint(0, c["V"], (h.shape[0],), generator=g, device=dev)
     return h, w, ids
 
 
@@ -646,7 +647,7 @@ def run_lmhead(args):
         dist.init_process_group("nccl", device_id=dev)
     rl.build()
     rl.load()
-    h, w, ids = lmhead_inputs_dev(dev)
+    h, w, ids = lmhead_inputs_dev(dev, args.lmhead_rows)
     R, D = h.shape
     V = w.shape[0]
     logp = torch.empty(R, device=dev)
@@ -793,6 +794,8 @@ def main():
                     help="profiling only: keep the first SEQS sequences")
     ap.add_argument("--lmhead", action="store_true",
                     help="time rl_lmhead_logprobs on the Qwen3-0.6B LM head instead")
+    ap.add_argument("--lmhead-rows", type=int, default=0,
+                    help="profiling only: rows of the LM-head leg (default 32768)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

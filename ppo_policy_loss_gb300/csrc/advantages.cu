@@ -27,6 +27,7 @@ __device__ __forceinline__ double warp_sum(double v) {
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 group_advantages_kernel(const float* rewards, int n_groups, int G, double std_eps,
                         int ddof, float* adv) {
+  allow_dependents();  // the loss launch may start its set-up beside this kernel
   const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= n_groups) return;
@@ -58,6 +59,7 @@ gae_kernel(const float* __restrict__ rewards, const float* __restrict__ values,
            const int* __restrict__ lengths, int B, int T, double gamma, double lam, float* adv,
            float* ret) {
   const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  allow_dependents();  // a following loss launch may start its set-up
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
   const long long base = static_cast<long long>(b) * T;
@@ -150,6 +152,7 @@ masked_whiten_kernel(const float* x, const unsigned char* __restrict__ mask, lon
   __shared__ double s_red[kThreadsW / 32][2];
   __shared__ double s_mu, s_inv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  allow_dependents();  // a following loss launch may start its set-up
   double sum = 0.0, cnt = 0.0;
   for (long long i = tid; i < n; i += kThreadsW)
     if (mask[i]) {
@@ -222,6 +225,7 @@ count_tokens_kernel(const unsigned char* __restrict__ mask, long long B, long lo
                     long long* counts) {
   __shared__ long long s_n[kThreadsC / 32], s_b[kThreadsC / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  allow_dependents();  // a following loss launch may start its set-up
   long long n = 0, nb = 0;
   for (long long b = warp; b < B; b += kThreadsC / 32) {
     long long c = 0;

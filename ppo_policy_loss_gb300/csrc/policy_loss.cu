@@ -534,6 +534,10 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
   }
   __syncthreads();
   cluster_sync_all();  // every peer's barriers exist before any remote arrive
+  // Launched with programmatic stream serialisation: the set-up above overlaps
+  // the previous kernel (e.g. the advantages); nothing in global memory is
+  // read before that kernel has finished.
+  grid_dependency_wait();
 
   const long long lo = static_cast<long long>(rank) * a.slice;
   const long long hi = min(a.V, lo + a.slice);
@@ -1183,17 +1187,19 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   args.global_counts = d->global_counts;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = pl.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(pl.cluster * pl.n_clusters));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = sizeof(LossSmem);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaErrorInvalidValue;
   switch (d->dtype) {
     case RL_F32:

@@ -188,6 +188,18 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return y;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream is still
+// running; grid_dependency_wait() blocks until that kernel has completed and
+// its memory is visible (it returns at once when there is no such kernel).
+// allow_dependents() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Spin on an mbarrier phase for at most kWaitLimitNs.  Returns false on
 // timeout (after raising `*abort`) or immediately if `*abort` is already set.
 template <bool kClusterScope>

@@ -577,3 +577,27 @@ def test_lmhead_row_stats_match_torch_fp64():
     np.testing.assert_allclose(lse, torch.logsumexp(z, 1).numpy(), rtol=1e-13)
     np.testing.assert_allclose(logp, ref_lsm[torch.arange(9), ids].numpy(), atol=1e-12)
     np.testing.assert_allclose(H, -(ref_lsm.exp() * ref_lsm).sum(1).numpy(), rtol=1e-12)
+
+
+def test_lmhead_one_hot_hidden_selects_weight_columns():
+    """A one-hot hidden state e_k makes the logits the k-th column of W
+    (z_v = W[v, k]), so the statistics reduce to scipy's logsumexp over that
+    column; a transposed or mis-indexed product fails this."""
+    from scipy.special import logsumexp
+    g = torch.Generator().manual_seed(91)
+    V, D = 50, 24
+    w = (torch.randn(V, D, generator=g) * 3).to(torch.bfloat16)
+    ks = np.array([0, 5, 23, 11])
+    h = torch.zeros(len(ks), D, dtype=torch.bfloat16)
+    h[np.arange(len(ks)), ks] = 1.0
+    ids = np.array([3, 0, 49, 17])
+    st = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    lse, logp, H = oracle.lmhead_row_stats(st(h), st(w), ids, "bf16", threads=1)
+    wf = w.double().numpy()
+    for r, k in enumerate(ks):
+        col = wf[:, k]
+        ref_lse = logsumexp(col)
+        p = np.exp(col - ref_lse)
+        assert abs(lse[r] - ref_lse) < 1e-12
+        assert abs(logp[r] - (col[ids[r]] - ref_lse)) < 1e-12
+        assert abs(H[r] + np.sum(p * np.log(p))) < 1e-12

@@ -52,6 +52,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 LMHEAD_METRIC = "fused LM-head + log-softmax rows/s (Qwen3-0.6B head D=1024, V=151936 bf16); % of tensor roofline"
 LMHEAD_SHAPE = dict(R=32 * 1024, D=1024, V=151936, logit_sd=3.0, seed=202)
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
+LMHEAD_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "lmhead.cu")
+LMHEAD_TRAFFIC = os.path.join(ROOT, "profiles", "lmhead_logprobs_qwen3_head_traffic.txt")
 DESCRIBE = {
     "tiny_grpo": "tiny GRPO: 2 prompts x group 4 = 8 seqs, T=16, V=1024 fp32",
     "qwen3_0p6b_grpo": "Qwen3-0.6B GRPO: 4 prompts x group 8 = 32 seqs, T=1024, V=151936 bf16, "
@@ -94,12 +96,12 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
+def kernel_sha(src=None) -> str:
+    with open(src or KERNEL_SRC, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload=WORKLOAD, path=None):
+def recorded_traffic(workload=WORKLOAD, path=None, src=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
     try:
@@ -109,7 +111,7 @@ def recorded_traffic(workload=WORKLOAD, path=None):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_sha") != kernel_sha():
+        if kv.get("kernel_sha") != kernel_sha(src):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -747,7 +749,9 @@ def run_lmhead(args):
                                                     parallelism="replicas" if world > 1 else "single GPU",
                                                     split={"vocab_slices": n_sl, "ctas": grid}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": (recorded_traffic(path=LMHEAD_TRAFFIC, src=LMHEAD_SRC)
+                                 if not args.lmhead_rows else None),
                      "alg_flops_per_launch": flops, "kernel": "rl_lmhead_logprobs",
                      "kernel_ms": kern_ms},
         "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,

@@ -49,7 +49,7 @@ METRIC = "fused GRPO loss+dlogits tokens/s at V=151936 bf16; % of HBM roofline"
 WORKLOAD = "qwen3_0p6b_grpo"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-LMHEAD_METRIC = "fused LM-head + log-softmax rows/s (Qwen3-0.6B head D=1024, V=151936 bf16); % of tensor roofline"
+LMHEAD_METRIC = "fused LM-head + log-softmax rows/s (Qwen3 head, V=151936 bf16); % of tensor roofline"
 LMHEAD_SHAPE = dict(R=32 * 1024, D=1024, V=151936, logit_sd=3.0, seed=202)
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
 LMHEAD_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "lmhead.cu")
@@ -616,19 +616,22 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- LM-head leg
 def lmhead_config(R, D, V):
     rows = "32 seqs x T=1024" if R == LMHEAD_SHAPE["R"] else "profiling slice"
-    return {"workload": f"qwen3_0p6b_lmhead: {R} rows ({rows}) x D={D} hidden -> "
+    name = {1024: "qwen3_0p6b_lmhead", 2048: "qwen3_1p7b_lmhead", 2560: "qwen3_4b_lmhead",
+            4096: "qwen3_8b_lmhead"}.get(D, f"lmhead_d{D}")
+    return {"workload": f"{name}: {R} rows ({rows}) x D={D} hidden -> "
                         f"V={V} bf16 LM head, hidden ~N(0,1), W ~N(0, 9/D), ids uniform",
             "rows": R, "D": D, "V": V,
             "l2": f"weight {V * D * 2 / 1e9:.2f} GB > 129 MB L2, swept every launch; no flush"}
 
 
-def lmhead_inputs_dev(dev, rows=0):
+def lmhead_inputs_dev(dev, rows=0, dim=0):
     import torch
     c = LMHEAD_SHAPE
+    D = dim or c["D"]
     g = torch.Generator(device=dev).manual_seed(c["seed"])
-    h = torch.randn((rows or c["R"], c["D"]), generator=g, device=dev).to(torch.bfloat16)
-    w = (torch.randn((c["V"], c["D"]), generator=g, device=dev)
-         * (c["logit_sd"] / c["D"] ** 0.5)).to(torch.bfloat16)
+    h = torch.randn((rows or c["R"], D), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((c["V"], D), generator=g, device=dev)
+         * (c["logit_sd"] / D ** 0.5)).to(torch.bfloat16)
     ids = torch.randint(0, c["V"], (h.shape[0],), generator=g, device=dev)
     return h, w, ids
 
@@ -665,14 +668,14 @@ def run_lmhead(args):
         dist.init_process_group("nccl", device_id=dev)
     rl.build()
     rl.load()
-    h, w, ids = lmhead_inputs_dev(dev, args.lmhead_rows)
+    h, w, ids = lmhead_inputs_dev(dev, args.lmhead_rows, args.lmhead_dim)
     R, D = h.shape
     V = w.shape[0]
     logp = torch.empty(R, device=dev)
     ent = torch.empty(R, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = torch.zeros(max(16, rl.rl_lmhead_workspace_size(R, V)), dtype=torch.uint8, device=dev)
-    n_sl, grid, _ = rl.rl_lmhead_plan(R, V, ws.numel())
+    n_sl, grid, _, group = rl.rl_lmhead_plan(R, V, ws.numel(), D=D)
     stream = torch.cuda.current_stream(dev)
 
     def launch(hh, out_lp, out_en):
@@ -747,11 +750,12 @@ def run_lmhead(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded)", "config": dict(lmhead_config(R, D, V),
                                                     parallelism="replicas" if world > 1 else "single GPU",
-                                                    split={"vocab_slices": n_sl, "ctas": grid}),
+                                                    split={"vocab_slices": n_sl, "ctas": grid,
+                                                           "row_tiles_per_group": group}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "traffic": (recorded_traffic(path=LMHEAD_TRAFFIC, src=LMHEAD_SRC)
-                                 if not args.lmhead_rows else None),
+                                 if not (args.lmhead_rows or args.lmhead_dim) else None),
                      "alg_flops_per_launch": flops, "kernel": "rl_lmhead_logprobs",
                      "kernel_ms": kern_ms},
         "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
@@ -816,6 +820,9 @@ def main():
                     help="time rl_lmhead_logprobs on the Qwen3-0.6B LM head instead")
     ap.add_argument("--lmhead-rows", type=int, default=0,
                     help="profiling only: rows of the LM-head leg (default 32768)")
+    ap.add_argument("--lmhead-dim", type=int, default=0,
+                    help="hidden size of the LM-head leg (default 1024, Qwen3-0.6B; "
+                         "2048, 2560, 4096 are the Qwen3-1.7B/4B/8B heads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

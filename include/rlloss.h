@@ -430,13 +430,15 @@ size_t rl_lmhead_workspace_size(long long R, long long V);
 /*
  * The work split rl_lmhead_logprobs would use with workspace_bytes of
  * workspace on a GPU of sm_count SMs (sm_count < 1: the current device):
- * vocabulary slices per 128-row tile, CTAs in the persistent grid and the
- * workspace bytes that split uses (0 when unsliced).  Any output pointer may
- * be NULL.  Host-only; with sm_count >= 1 it needs no GPU.  Errors:
- * RL_ERR_SHAPE (R < 1 or as rl_lmhead_logprobs), RL_ERR_CUDA.
+ * vocabulary slices per 128-row tile, CTAs in the persistent grid, row
+ * tiles per unit group (units run slice by slice inside a group, so the
+ * hidden tiles in use at one time stay in L2) and the workspace bytes that
+ * split uses (0 when unsliced).  Any output pointer may be NULL.  Host-only;
+ * with sm_count >= 1 it needs no GPU.  Errors: RL_ERR_SHAPE (R < 1 or as
+ * rl_lmhead_logprobs), RL_ERR_CUDA.
  */
-rl_status rl_lmhead_plan(long long R, long long V, size_t workspace_bytes, int sm_count,
-                         int* n_slices, int* grid, size_t* workspace_needed);
+rl_status rl_lmhead_plan(long long R, long long D, long long V, size_t workspace_bytes, int sm_count,
+                         int* n_slices, int* grid, int* group, size_t* workspace_needed);
 
 /*
  * The launch shape rl_policy_loss_fwd_bwd would use on the current device for

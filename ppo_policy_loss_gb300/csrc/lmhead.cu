@@ -68,6 +68,7 @@ struct LmSmem {
 struct LmArgs {
   long long R, D, V;
   int n_mt, n_nt, n_slices;
+  int group;              // row tiles per unit group
   unsigned int* tickets;  // [n_mt] (n_slices > 1)
   float4* partials;       // [n_slices][R]: (max, sum 2^x, sum 2^x x, sampled logit)
   const long long* ids;
@@ -136,6 +137,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // First vocabulary tile of slice vs when n_nt tiles are cut into n_sl slices.
 __device__ __forceinline__ int slice_begin(int vs, int n_nt, int n_sl) {
   return static_cast<int>(static_cast<long long>(vs) * n_nt / n_sl);
+}
+
+// Row tile and vocabulary slice of work unit u.  Units come in groups of g
+// row tiles; inside a group they run slice by slice, so the CTAs working at
+// one time share a slice of W and touch at most g hidden tiles (the host
+// sizes g so that those tiles stay in L2).
+__device__ __forceinline__ void unit_coords(int u, int n_mt, int n_sl, int g, int& mt, int& vs) {
+  const int per_group = g * n_sl;
+  const int grp = u / per_group;
+  const int base = grp * g;
+  const int gc = min(g, n_mt - base);
+  const int within = u - grp * per_group;
+  vs = within / gc;
+  mt = base + within % gc;
 }
 
 // v[j] through a tree of selects on the bits of j (constant register
@@ -222,7 +237,8 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
       uint32_t it = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const int mt = u % n_mt, vs = u / n_mt;
+        int mt, vs;
+        unit_coords(u, n_mt, n_sl, a.group, mt, vs);
         for (int nt = slice_begin(vs, n_nt, n_sl); nt < slice_begin(vs + 1, n_nt, n_sl) && !stop; ++nt) {
           for (int kb = 0; kb < n_kb; ++kb, ++it) {
             const uint32_t s = it % kStagesL, round = it / kStagesL;
@@ -247,7 +263,8 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
       uint32_t it = 0, acc_it = 0;
       bool stop = false, issued = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const int vs = u / n_mt;
+        int mt, vs;
+        unit_coords(u, n_mt, n_sl, a.group, mt, vs);
         for (int nt = slice_begin(vs, n_nt, n_sl); nt < slice_begin(vs + 1, n_nt, n_sl) && !stop; ++nt, ++acc_it) {
           const uint32_t buf = acc_it & 1, use = acc_it >> 1;
           if (use > 0 && !lm_wait<false>(smem_addr(&sm.acc_empty[buf]), (use - 1) & 1, abort_flag)) {
@@ -288,7 +305,8 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
     uint32_t acc_it = 0;
     bool stop = false;
     for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-      const int mt = u % n_mt, vs = u / n_mt;
+      int mt, vs;
+      unit_coords(u, n_mt, n_sl, a.group, mt, vs);
       const long long row = static_cast<long long>(mt) * kBM + r_in_tile;
       const long long y = row < a.R ? a.ids[row] : -1;
       float m = kFloor, zy = -INFINITY;
@@ -443,9 +461,13 @@ bool make_map(EncodeTiled enc, CUtensorMap* map, const void* base, long long row
 constexpr int kMaxSlices = 1024;
 
 struct LmPlan {
-  int n_mt, n_nt, n_slices, grid;
+  int n_mt, n_nt, n_slices, grid, group;
   size_t ws_bytes;
 };
+
+// Hidden tiles the CTAs working at one time may touch: about 40 MB of L2,
+// a third of it, leaving the rest to the weight slice being swept.
+constexpr long long kHiddenL2Budget = 40LL << 20;
 
 size_t ticket_bytes(long long n_mt) { return (static_cast<size_t>(n_mt) * 4 + 255) & ~size_t(255); }
 
@@ -454,7 +476,7 @@ size_t lm_ws_bytes(long long R, long long n_mt, int n_sl) {
   return ticket_bytes(n_mt) + static_cast<size_t>(n_sl) * static_cast<size_t>(R) * 16;
 }
 
-LmPlan lm_plan(long long R, long long V, int sms, size_t ws_cap) {
+LmPlan lm_plan(long long R, long long V, long long D, int sms, size_t ws_cap) {
   LmPlan p;
   p.n_mt = static_cast<int>((R + kBM - 1) / kBM);
   p.n_nt = static_cast<int>((V + kBN - 1) / kBN);
@@ -478,6 +500,9 @@ LmPlan lm_plan(long long R, long long V, int sms, size_t ws_cap) {
   const long long units = static_cast<long long>(p.n_mt) * best;
   p.grid = static_cast<int>(units < sms ? units : sms);
   p.ws_bytes = lm_ws_bytes(R, p.n_mt, best);
+  const long long tile_bytes = static_cast<long long>(kBM) * ((D + kBK - 1) / kBK) * kBK * 2;
+  const long long g = kHiddenL2Budget / tile_bytes;
+  p.group = static_cast<int>(g < 1 ? 1 : (g > p.n_mt ? p.n_mt : g));
   return p;
 }
 
@@ -498,18 +523,19 @@ extern "C" size_t rl_lmhead_workspace_size(long long R, long long V) {
   using namespace rl;
   int sms = 0;
   if (R < 1 || !lm_shape_ok(R, V) || device_sms(&sms) != RL_OK) return 0;
-  return lm_plan(R, V, sms, ~size_t(0)).ws_bytes;
+  return lm_plan(R, V, 1024, sms, ~size_t(0)).ws_bytes;
 }
 
-extern "C" rl_status rl_lmhead_plan(long long R, long long V, size_t workspace_bytes, int sm_count,
-                                    int* n_slices, int* grid, size_t* workspace_needed) {
+extern "C" rl_status rl_lmhead_plan(long long R, long long D, long long V, size_t workspace_bytes, int sm_count,
+                                    int* n_slices, int* grid, int* group, size_t* workspace_needed) {
   using namespace rl;
-  if (R < 1 || !lm_shape_ok(R, V)) return RL_ERR_SHAPE;
+  if (R < 1 || !lm_shape_ok(R, V) || D < 8 || D % 8 != 0) return RL_ERR_SHAPE;
   int sms = sm_count;
   if (sms < 1 && device_sms(&sms) != RL_OK) return RL_ERR_CUDA;
-  const LmPlan p = lm_plan(R, V, sms, workspace_bytes);
+  const LmPlan p = lm_plan(R, V, D, sms, workspace_bytes);
   if (n_slices) *n_slices = p.n_slices;
   if (grid) *grid = p.grid;
+  if (group) *group = p.group;
   if (workspace_needed) *workspace_needed = p.ws_bytes;
   return RL_OK;
 }
@@ -543,7 +569,7 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
       g_lm_attr_dev = dev;
     }
   }
-  const LmPlan plan = lm_plan(R, V, sms, workspace ? workspace_bytes : 0);
+  const LmPlan plan = lm_plan(R, V, D, sms, workspace ? workspace_bytes : 0);
   LmArgs args;
   args.R = R;
   args.D = D;
@@ -551,6 +577,7 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
   args.n_mt = plan.n_mt;
   args.n_nt = plan.n_nt;
   args.n_slices = plan.n_slices;
+  args.group = plan.group;
   args.tickets = plan.n_slices > 1 ? static_cast<unsigned int*>(workspace) : nullptr;
   args.partials = plan.n_slices > 1
                       ? reinterpret_cast<float4*>(static_cast<char*>(workspace) + ticket_bytes(plan.n_mt))

@@ -228,7 +228,8 @@ def test_lmhead_plan_balances_the_sms(lib, R, V):
     workspace the launch is unsliced."""
     sms = 152
     n_mt, n_nt = -(-R // 128), -(-V // 256)
-    ns, grid, need = rl.rl_lmhead_plan(R, V, 1 << 40, sms)
+    ns, grid, need, grp = rl.rl_lmhead_plan(R, V, 1 << 40, sms)
+    assert 1 <= grp <= n_mt
     assert 1 <= ns <= n_nt and grid == min(sms, n_mt * ns)
     if ns > 1:
         assert need >= ns * R * 16 + n_mt * 4
@@ -242,3 +243,13 @@ def test_lmhead_plan_balances_the_sms(lib, R, V):
         assert max(load) <= 1.06 * ideal, (ns, max(load), ideal)
     assert rl.rl_lmhead_plan(R, V, 0, sms)[0] == 1
     assert rl.rl_lmhead_plan(R, V, 0, sms)[2] == 0
+
+
+@pytest.mark.parametrize("D,expect", [(1024, 160), (2048, 80), (4096, 40), (200, 640)])
+def test_lmhead_plan_groups_row_tiles_to_fit_l2(lib, D, expect):
+    """Units are grouped so that the hidden tiles in use at one time (128 rows x D
+    bf16 each, D rounded up to 64) stay within a 40 MB share of L2."""
+    n_mt = 2000
+    grp = rl.rl_lmhead_plan(128 * n_mt, 151936, 1 << 40, 152, D=D)[3]
+    assert grp == min(expect, n_mt)
+    assert grp * 128 * (-(-D // 64) * 64) * 2 <= 40 << 20

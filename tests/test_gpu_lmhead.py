@@ -164,3 +164,35 @@ def test_lmhead_optional_outputs_and_empty():
     assert np.abs(logp.cpu().numpy() - ref[1]).max() <= LOGP_ATOL
     rl.rl_lmhead_logprobs(h, 64, w, 64, 0, 64, 500, i, logp, None, None, None)  # R = 0: no launch
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_lmhead_randomized(case):
+    """Seeded random shapes: R in [1, 3000], D a multiple of 8 in [8, 520]
+    (ragged K tails), V in [1, 5000], padded strides, logit spreads 0.5-12,
+    with and without a workspace."""
+    rng = np.random.default_rng(1000 + case)
+    R = int(rng.integers(1, 3001))
+    D = int(rng.integers(1, 66)) * 8
+    V = int(rng.integers(1, 5001))
+    ld_h = D + 8 * int(rng.integers(0, 3))
+    ld_w = D + 8 * int(rng.integers(0, 3))
+    sd = float(rng.uniform(0.5, 12.0))
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 2000 + case, sd, ld_h, ld_w)
+    got = run_gpu(hidden, weight, ids, D, V, sliced=bool(case % 2))
+    assert got[3] == 0
+    check(got[:3], oracle_rows(hidden, weight, ids, D))
+
+
+@pytest.mark.parametrize("sliced", [False, True])
+def test_lmhead_unit_groups(sliced):
+    """D = 4096 (the Qwen3-8B head's hidden size) puts 40 row tiles in a unit
+    group, so 45 row tiles make a full group and a 5-tile tail group."""
+    R, D, V = 128 * 45 - 3, 4096, 3000
+    ws_bytes = rl.rl_lmhead_workspace_size(R, V) if sliced else 0
+    plan = rl.rl_lmhead_plan(R, V, ws_bytes, D=D)
+    assert plan[3] == 40 and (plan[0] > 1) == sliced
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 12, 4.0)
+    got = run_gpu(hidden, weight, ids, D, V, sliced=sliced)
+    assert got[3] == 0
+    check(got[:3], oracle_rows(hidden, weight, ids, D))

@@ -392,6 +392,7 @@ def run_gpu(args):
                      "traffic": traffic, "alg_bytes_per_launch": bytes_launch,
                      "kernel": "rl_policy_loss_fwd_bwd", "kernel_ms": kern_ms},
         "e2e": e2e,
+        "aux_kernels": (time_aux(w, inp, dev, stream) if not args.no_aux else None),
         "gpu_launches": (3 if gm else 2) * args.steps,
         "clocks": clocks,
     }
@@ -403,6 +404,63 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def time_aux(w, inp, dev, stream, reps=50):
+    """Mean device time (CUDA events, `reps` back-to-back launches after a
+    warm-up) of the O(B*T) kernels beside the loss, at this workload's sizes:
+    group advantages, GAE, masked whitening, the critic loss and the token
+    count.  GRPO workloads get seeded values and per-token rewards for the
+    GAE and critic calls."""
+    import torch
+
+    import ppo_policy_loss_gb300 as rl
+    from ppo_policy_loss_gb300 import VALUE_STATS_BYTES
+
+    B, T, R = w.B, w.T, w.R
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    mask = inp["mask"]
+    values = (inp["values"] if "values" in inp else
+              0.5 * torch.randn((B, T), generator=g, device=dev)).contiguous()
+    rewards_t = (inp["rewards"] if w.advantage == "gae" else
+                 torch.randn((B, T), generator=g, device=dev)).contiguous()
+    lengths = (inp["lengths"] if "lengths" in inp else
+               mask.view(B, T).sum(1).to(torch.int32)).contiguous()
+    adv_seq = torch.empty(B, device=dev)
+    adv_tok, ret = torch.empty(R, device=dev), torch.empty(R, device=dev)
+    white = torch.empty(R, device=dev)
+    dval = torch.empty(R, device=dev)
+    vst = torch.zeros(VALUE_STATS_BYTES, dtype=torch.uint8, device=dev)
+    counts = torch.empty(2, dtype=torch.int64, device=dev)
+    rewards_seq = (inp["rewards"] if w.advantage != "gae" else
+                   torch.rand(B, generator=g, device=dev)).contiguous()
+    vold = (values + 0.1 * torch.randn((B, T), generator=g, device=dev)).contiguous()
+    G = w.group if w.group > 1 else (8 if B % 8 == 0 else B)  # PPO workloads: groups of 8
+    calls = {
+        "group_advantages": (lambda: rl.rl_group_advantages(rewards_seq, B // G, G, 1e-4, 1, adv_seq,
+                                                              stream), B * 8),
+        "gae_reverse_scan": (lambda: rl.rl_gae_reverse_scan(rewards_t, values, lengths, B, T, w.gamma,
+                                                              w.lam, adv_tok, ret, stream),
+                             R * 16 + B * 4),
+        "masked_whiten": (lambda: rl.rl_masked_whiten(adv_tok, mask, R, 1e-8, 1, white, stream),
+                          R * 9),
+        "value_loss": (lambda: rl.rl_value_loss_fwd_bwd(values, vold, ret, mask, R, 0.2, 1.0, dval,
+                                                        vst, stream), R * 17),
+        "count_tokens": (lambda: rl.rl_count_tokens(mask, B, T, counts, stream), R),
+    }
+    out = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        out[name] = {"us": round(us, 2), "bytes": nbytes, "GB_per_s": round(nbytes / us / 1e3, 1)}
+    return out
 
 
 def run_e2e(args, w, inp, dev, stream, step0):
@@ -812,6 +870,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-aux", action="store_true",
+                    help="skip timing the O(B*T) kernels beside the loss")
     ap.add_argument("--global-token-mean", action="store_true",
                     help="with N > 1: normalise by the token count summed over ranks")
     ap.add_argument("--seqs", type=int, default=0,

@@ -135,7 +135,7 @@ rl_status rl_group_advantages(const float* rewards, int n_groups, int group_size
  *   adv_out         : float[B*T], device, written.
  *   returns_out     : float[B*T], device, written; may be NULL.
  * Arithmetic in fp64 (a warp-parallel affine scan over the sequence),
- * result rounded to fp32.  One launch, one warp per sequence.
+ * result rounded to fp32.  One launch, one CTA per sequence.
  * Errors: RL_ERR_NULL, RL_ERR_SHAPE (B < 0, T < 0), RL_ERR_ARG (NaN gamma/lam).
  */
 rl_status rl_gae_reverse_scan(const float* rewards, const float* values, const int* lengths,
@@ -150,8 +150,9 @@ rl_status rl_gae_reverse_scan(const float* rewards, const float* values, const i
  *   out_t = (x_t - mu) / sqrt(var + eps)   (x_t / sqrt(var + eps) if !shift_mean)
  *   out_t = 0 where mask_t == 0.
  *   x, out : float[n], device (out may equal x);  mask : uint8[n].
- * fp64 reductions, one launch of one CTA.  Errors: RL_ERR_SHAPE (n < 0),
- * RL_ERR_NULL, RL_ERR_ARG (eps negative or NaN).  n == 0 launches nothing.
+ * fp32 per element, fp64 reductions in a fixed order, one launch of one
+ * CTA.  Errors: RL_ERR_SHAPE (n < 0), RL_ERR_NULL, RL_ERR_ARG (eps negative
+ * or NaN).  n == 0 launches nothing.
  */
 rl_status rl_masked_whiten(const float* x, const unsigned char* mask, long long n, double eps,
                            int shift_mean, float* out, void* stream);

@@ -4,8 +4,8 @@
 // paragraph after its benchmark table) for GRPO, the group-relative method of
 // the pitchhut.com listing ("Key Features" item 3), and advantage estimation
 // inside the PPO update (same article, "PPO 更新内核" bullet).  Both steps
-// touch O(B*T) bytes, so they are latency kernels: one warp per group or per
-// sequence, fp64 arithmetic (cheap at this size, and exact enough that the
+// touch O(B*T) bytes, so they are latency kernels: one warp per group, one
+// CTA per sequence, fp64 arithmetic (cheap at this size, and exact enough that the
 // result is the fp64 definition rounded once to fp32).
 #include <cmath>
 
@@ -48,26 +48,29 @@ group_advantages_kernel(const float* rewards, int n_groups, int G, double std_ep
   for (int j = lane; j < G; j += 32) a[j] = static_cast<float>((static_cast<double>(r[j]) - mean) * inv);
 }
 
-// One warp per sequence.  Lane l owns the contiguous time chunk
-// [l*cs, min(L, (l+1)*cs)).  Each lane folds its chunk into an affine map
-// A_start = P + Q * A_after_chunk (Q = c^len, c = gamma*lam); a suffix scan of
-// these maps across lanes (shuffles, composition from the high lanes down)
-// gives every chunk its incoming A; a second pass over the chunk writes A and
-// ret.  The terminal bootstrap is 0: delta_{L-1} = r_{L-1} - v_{L-1}.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+// One CTA of kThreadsG threads per sequence.  Thread k owns the contiguous
+// time chunk [k*cs, min(L, (k+1)*cs)).  Each thread folds its chunk into an
+// affine map A_start = P + Q * A_after_chunk (Q = c^len, c = gamma*lam); a
+// suffix composition of these maps (shuffles inside each warp, then the warp
+// totals in order) gives every chunk its incoming A; a second pass over the
+// chunk writes A and ret.  The terminal bootstrap is 0:
+// delta_{L-1} = r_{L-1} - v_{L-1}.
+constexpr int kThreadsG = 256;
+
+__global__ void __launch_bounds__(kThreadsG)
 gae_kernel(const float* __restrict__ rewards, const float* __restrict__ values,
            const int* __restrict__ lengths, int B, int T, double gamma, double lam, float* adv,
            float* ret) {
-  const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  __shared__ double s_p[kThreadsG / 32], s_q[kThreadsG / 32], s_in[kThreadsG / 32];
   allow_dependents();  // a following loss launch may start its set-up
-  const int lane = threadIdx.x & 31;
-  if (b >= B) return;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long base = static_cast<long long>(b) * T;
   int L = lengths[b];
   L = L < 0 ? 0 : (L > T ? T : L);
   const double c = gamma * lam;
-  const int cs = (L + 31) / 32;
-  const int t0 = min(L, lane * cs), t1 = min(L, t0 + cs);
+  const int cs = (L + kThreadsG - 1) / kThreadsG;
+  const int t0 = min(L, tid * cs), t1 = min(L, t0 + cs);
 
   auto delta = [&](int t) -> double {
     const double vn = (t + 1 < L) ? static_cast<double>(values[base + t + 1]) : 0.0;
@@ -79,7 +82,7 @@ gae_kernel(const float* __restrict__ rewards, const float* __restrict__ values,
     P = delta(t) + c * P;
     Q = c * Q;
   }
-  // inclusive suffix composition: lane l ends with F_l o F_{l+1} o ... o F_31
+  // inclusive suffix composition inside the warp: lane l ends with F_l o ... o F_31
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const double P2 = __shfl_down_sync(0xffffffffu, P, o);
@@ -89,16 +92,34 @@ gae_kernel(const float* __restrict__ rewards, const float* __restrict__ values,
       Q = Q * Q2;
     }
   }
-  double a_next = __shfl_down_sync(0xffffffffu, P, 1);  // A at the start of lane+1's chunk
-  if (lane == 31) a_next = 0.0;
+  if (lane == 0) {
+    s_p[warp] = P;
+    s_q[warp] = Q;
+  }
+  __syncthreads();
+  if (tid == 0) {  // A entering each warp's region from the warps after it
+    double a = 0.0;
+    for (int w = kThreadsG / 32 - 1; w >= 0; --w) {
+      s_in[w] = a;
+      a = s_p[w] + s_q[w] * a;
+    }
+  }
+  __syncthreads();
+  // A at the start of the next thread's chunk: lanes l+1..31 composed, applied
+  // to the A entering this warp's region from the warps after it
+  double Pn = __shfl_down_sync(0xffffffffu, P, 1), Qn = __shfl_down_sync(0xffffffffu, Q, 1);
+  if (lane == 31) {
+    Pn = 0.0;
+    Qn = 1.0;
+  }
   // second pass: outputs
-  double a = a_next;
+  double a = Pn + Qn * s_in[warp];
   for (int t = t1 - 1; t >= t0; --t) {
     a = delta(t) + c * a;
     adv[base + t] = static_cast<float>(a);
     if (ret) ret[base + t] = static_cast<float>(a + static_cast<double>(values[base + t]));
   }
-  for (int t = L + lane; t < T; t += 32) {
+  for (int t = L + tid; t < T; t += kThreadsG) {
     adv[base + t] = 0.f;
     if (ret) ret[base + t] = 0.f;
   }
@@ -130,8 +151,7 @@ extern "C" rl_status rl_gae_reverse_scan(const float* rewards, const float* valu
   if (!std::isfinite(gamma) || !std::isfinite(lam)) return RL_ERR_ARG;
   if (B == 0 || T == 0) return RL_OK;
   if (!rewards || !values || !lengths || !adv_out) return RL_ERR_NULL;
-  const int blocks = (B + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  gae_kernel<<<blocks, kWarpsPerBlock * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+  gae_kernel<<<B, kThreadsG, 0, static_cast<cudaStream_t>(stream)>>>(
       rewards, values, lengths, B, T, static_cast<double>(gamma), static_cast<double>(lam), adv_out,
       returns_out);
   return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
@@ -145,7 +165,13 @@ constexpr int kThreadsW = 1024;
 
 // One CTA: fp64 masked mean, unbiased variance, then (x - mu) / sqrt(var + eps)
 // (or x / sqrt(var + eps)); every element is read and written by the same
-// thread after the reductions, so out may alias x.
+// thread after the reductions, so out may alias x.  Each pass handles
+// kUnrollW elements per thread per step, loaded before any is used.  Per
+// element the arithmetic is fp32 (a step's 8 terms summed in fp32, the step
+// sums accumulated in fp64): fp64 units are scarce on this GPU, and one CTA
+// doing fp64 per element took ~100 us for 32K elements.
+constexpr int kUnrollW = 8;
+
 __global__ void __launch_bounds__(kThreadsW, 1)
 masked_whiten_kernel(const float* x, const unsigned char* __restrict__ mask, long long n,
                      double eps, int shift_mean, float* out) {
@@ -153,12 +179,28 @@ masked_whiten_kernel(const float* x, const unsigned char* __restrict__ mask, lon
   __shared__ double s_mu, s_inv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   allow_dependents();  // a following loss launch may start its set-up
+  constexpr long long kStep = static_cast<long long>(kThreadsW) * kUnrollW;
   double sum = 0.0, cnt = 0.0;
-  for (long long i = tid; i < n; i += kThreadsW)
-    if (mask[i]) {
-      sum += static_cast<double>(x[i]);
-      cnt += 1.0;
+  for (long long i0 = tid; i0 < n; i0 += kStep) {
+    float xv[kUnrollW];
+    bool mv[kUnrollW];
+#pragma unroll
+    for (int k = 0; k < kUnrollW; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsW;
+      mv[k] = i < n && mask[i] != 0;
+      xv[k] = i < n ? x[i] : 0.f;
     }
+    float s8 = 0.f;
+    int c8 = 0;
+#pragma unroll
+    for (int k = 0; k < kUnrollW; ++k)
+      if (mv[k]) {
+        s8 += xv[k];
+        ++c8;
+      }
+    sum += static_cast<double>(s8);
+    cnt += static_cast<double>(c8);
+  }
   sum = warp_sum(sum);
   cnt = warp_sum(cnt);
   if (lane == 0) {
@@ -177,12 +219,26 @@ masked_whiten_kernel(const float* x, const unsigned char* __restrict__ mask, lon
   }
   __syncthreads();
   const double mu = s_mu, N = s_inv;
+  const float mu_f = static_cast<float>(mu);
   double sq = 0.0;
-  for (long long i = tid; i < n; i += kThreadsW)
-    if (mask[i]) {
-      const double d = static_cast<double>(x[i]) - mu;
-      sq += d * d;
+  for (long long i0 = tid; i0 < n; i0 += kStep) {
+    float xv[kUnrollW];
+    bool mv[kUnrollW];
+#pragma unroll
+    for (int k = 0; k < kUnrollW; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsW;
+      mv[k] = i < n && mask[i] != 0;
+      xv[k] = i < n ? x[i] : 0.f;
     }
+    float q8 = 0.f;
+#pragma unroll
+    for (int k = 0; k < kUnrollW; ++k)
+      if (mv[k]) {
+        const float d = xv[k] - mu_f;
+        q8 = fmaf(d, d, q8);
+      }
+    sq += static_cast<double>(q8);
+  }
   sq = warp_sum(sq);
   __syncthreads();
   if (lane == 0) s_red[warp][0] = sq;
@@ -194,9 +250,22 @@ masked_whiten_kernel(const float* x, const unsigned char* __restrict__ mask, lon
     s_inv = 1.0 / sqrt(var + eps);
   }
   __syncthreads();
-  const double inv = s_inv, shift = shift_mean ? mu : 0.0;
-  for (long long i = tid; i < n; i += kThreadsW)
-    out[i] = mask[i] ? static_cast<float>((static_cast<double>(x[i]) - shift) * inv) : 0.f;
+  const float inv = static_cast<float>(s_inv), shift = shift_mean ? mu_f : 0.f;
+  for (long long i0 = tid; i0 < n; i0 += kStep) {
+    float xv[kUnrollW];
+    bool mv[kUnrollW];
+#pragma unroll
+    for (int k = 0; k < kUnrollW; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsW;
+      mv[k] = i < n && mask[i] != 0;
+      xv[k] = i < n ? x[i] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kUnrollW; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsW;
+      if (i < n) out[i] = mv[k] ? (xv[k] - shift) * inv : 0.f;
+    }
+  }
 }
 
 }  // namespace

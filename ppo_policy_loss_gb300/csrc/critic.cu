@@ -15,6 +15,7 @@ namespace {
 
 constexpr int kThreadsV = 1024;
 constexpr int kWarpsV = kThreadsV / 32;
+constexpr int kUnrollV = 8;
 
 template <typename T>
 __device__ __forceinline__ T warp_sum_t(T v) {
@@ -32,8 +33,21 @@ value_loss_kernel(const float* __restrict__ v, const float* __restrict__ vo,
   __shared__ long long s_clip[kWarpsV];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // Each step handles kUnrollV tokens per thread, all loaded before any is
+  // used; per token the arithmetic is fp32, and only the step sums are added
+  // in fp64 (fp64 units are scarce on this GPU).
+  constexpr long long kStep = static_cast<long long>(kThreadsV) * kUnrollV;
   long long cnt = 0;
-  for (long long i = tid; i < n; i += kThreadsV) cnt += mask[i] != 0;
+  for (long long i0 = tid; i0 < n; i0 += kStep) {
+    unsigned char mv[kUnrollV];
+#pragma unroll
+    for (int k = 0; k < kUnrollV; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsV;
+      mv[k] = i < n ? mask[i] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kUnrollV; ++k) cnt += mv[k] != 0;
+  }
   cnt = warp_sum_t(cnt);
   if (lane == 0) s_cnt[warp] = cnt;
   __syncthreads();
@@ -44,27 +58,46 @@ value_loss_kernel(const float* __restrict__ v, const float* __restrict__ vo,
 
   double sumL = 0.0, sumAbs = 0.0;
   long long nclip = 0;
-  for (long long i = tid; i < n; i += kThreadsV) {
-    if (!mask[i]) {
-      if (dv) dv[i] = 0.f;
-      continue;
+  for (long long i0 = tid; i0 < n; i0 += kStep) {
+    unsigned char mv[kUnrollV];
+    float vv[kUnrollV], rv[kUnrollV], ov[kUnrollV];
+#pragma unroll
+    for (int k = 0; k < kUnrollV; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsV;
+      const bool in = i < n;
+      mv[k] = in ? mask[i] : 0;
+      vv[k] = in ? v[i] : 0.f;
+      rv[k] = in ? ret[i] : 0.f;
+      ov[k] = in && use_clip ? vo[i] : 0.f;
     }
-    const float d = v[i] - ret[i];
-    const float u = d * d;
-    float g = d, L2 = u;
-    if (use_clip) {
-      const float delta = v[i] - vo[i];
-      const float dc = (vo[i] + fminf(fmaxf(delta, -clip), clip)) - ret[i];
-      const float c = dc * dc;
-      if (c > u) {  // the clipped square is the larger: its branch, flat outside the clip
-        g = fabsf(delta) <= clip ? dc : 0.f;
-        L2 = c;
-        ++nclip;
+    float l8 = 0.f, a8 = 0.f;  // this step's terms in fp32; the step sums go to fp64
+#pragma unroll
+    for (int k = 0; k < kUnrollV; ++k) {
+      const long long i = i0 + static_cast<long long>(k) * kThreadsV;
+      if (i >= n) continue;
+      if (!mv[k]) {
+        if (dv) dv[i] = 0.f;
+        continue;
       }
+      const float d = vv[k] - rv[k];
+      const float u = d * d;
+      float g = d, L2 = u;
+      if (use_clip) {
+        const float delta = vv[k] - ov[k];
+        const float dc = (ov[k] + fminf(fmaxf(delta, -clip), clip)) - rv[k];
+        const float c = dc * dc;
+        if (c > u) {  // the clipped square is the larger: its branch, flat outside the clip
+          g = fabsf(delta) <= clip ? dc : 0.f;
+          L2 = c;
+          ++nclip;
+        }
+      }
+      l8 += 0.5f * L2;
+      a8 += fabsf(d);
+      if (dv) dv[i] = scale * g;
     }
-    sumL += 0.5 * static_cast<double>(L2);
-    sumAbs += static_cast<double>(fabsf(d));
-    if (dv) dv[i] = scale * g;
+    sumL += static_cast<double>(l8);
+    sumAbs += static_cast<double>(a8);
   }
   sumL = warp_sum_t(sumL);
   sumAbs = warp_sum_t(sumAbs);

@@ -224,7 +224,8 @@ def test_group_advantages_shapes(G, ddof):
 
 
 @pytest.mark.parametrize("T,gamma,lam", [(512, 1.0, 0.95), (37, 0.99, 0.9), (1000, 1.0, 1.0),
-                                         (5, 0.5, 0.0), (1, 1.0, 0.95)])
+                                         (5, 0.5, 0.0), (1, 1.0, 0.95), (4096, 1.0, 0.95),
+                                         (300, 0.9, 0.99)])
 def test_gae_parity(T, gamma, lam):
     rng = np.random.default_rng(T)
     B = 70
@@ -475,6 +476,40 @@ def test_masked_whiten_ppo_advantages(shift):
     assert np.all(np.abs(got - ref) <= ADV_TOL * np.maximum(np.abs(ref), 1.0))
     torch_api.masked_whiten(d, to_dev(mask), 1e-8, shift, out=d)  # in place
     assert np.array_equal(d.cpu().numpy(), got)
+
+
+@pytest.mark.parametrize("n", [1, 7, 1000, 8192, 8193, 100003])
+def test_masked_whiten_sizes(n):
+    """Sizes around the kernel's 8192-element step (1024 threads x 8), a lone
+    element and a ragged large case."""
+    rng = np.random.default_rng(n)
+    x = rng.normal(0.3, 2.0, n).astype(np.float32)
+    mask = (rng.random(n) < 0.7).astype(np.uint8)
+    ref = oracle.masked_whiten(x, mask, 1e-8, True)
+    got = torch_api.masked_whiten(to_dev(x), to_dev(mask), 1e-8, True).cpu().numpy()
+    assert np.all(np.abs(got - ref) <= ADV_TOL * np.maximum(np.abs(ref), 1.0))
+
+
+@pytest.mark.parametrize("n", [1, 8193, 100003])
+def test_value_loss_sizes(n):
+    rng = np.random.default_rng(n + 1)
+    v = rng.normal(0, 1, n).astype(np.float32)
+    vo = (v + rng.normal(0, 0.3, n)).astype(np.float32)
+    ret = rng.normal(0, 1, n).astype(np.float32)
+    mask = (rng.random(n) < 0.6).astype(np.uint8)
+    N = int(mask.sum())
+    ref = oracle.value_loss(v, vo, ret, mask, 0.2, grad_scale=max(N, 1))
+    dv, st = torch_api.value_loss(to_dev(v), to_dev(ret), to_dev(mask), values_old=to_dev(vo),
+                                  clip_eps=0.2, grad_scale=float(max(N, 1)))
+    assert st["n_tokens"] == N
+    assert abs(st["loss"] - ref["loss"]) <= LOSS_RTOL * max(abs(ref["loss"]), 1e-3)
+    # tokens at a kink (clip boundary or equal squares) may take either branch
+    vd, vo64, r64 = v.astype(np.float64), vo.astype(np.float64), ret.astype(np.float64)
+    vc = vo64 + np.clip(vd - vo64, -0.2, 0.2)
+    kink = (np.abs(np.abs(vd - vo64) - 0.2) < 1e-5) | (np.abs((vc - r64) ** 2 - (vd - r64) ** 2) < 1e-5)
+    ok = ~kink
+    got = dv.cpu().numpy()
+    assert np.all(np.abs(got - ref["dvalues"])[ok] <= 1e-5 * np.maximum(np.abs(ref["dvalues"]), 1.0)[ok])
 
 
 # ----------------------------------------------------------------- randomized sweep

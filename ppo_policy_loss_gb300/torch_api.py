@@ -9,8 +9,8 @@ import torch
 
 from . import (AGGREGATIONS, DTYPES, RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN,
                STATS_BYTES, rl_gae_reverse_scan, rl_group_advantages, rl_policy_loss_desc_init,
-               VALUE_STATS_BYTES, rl_count_tokens, rl_masked_whiten, rl_policy_loss_fwd_bwd_ex,
-               rl_policy_loss_workspace_size,
+               VALUE_STATS_BYTES, rl_count_tokens, rl_lmhead_logprobs, rl_lmhead_workspace_size,
+               rl_masked_whiten, rl_policy_loss_fwd_bwd_ex, rl_policy_loss_workspace_size,
                rl_value_loss_fwd_bwd, stats_from_bytes, value_stats_from_bytes)
 
 _DT = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
@@ -160,3 +160,26 @@ def count_tokens(mask: torch.Tensor, B: int, T: int, out: torch.Tensor | None = 
     out = torch.empty(2, dtype=torch.int64, device=mask.device) if out is None else out
     rl_count_tokens(mask, B, T, out, stream)
     return out
+
+
+def lmhead_logprobs(hidden: torch.Tensor, weight: torch.Tensor, ids: torch.Tensor,
+                    want_entropy: bool = True, want_lse: bool = False, workspace="new",
+                    status: torch.Tensor | None = None, stream=None) -> dict:
+    """Per-row log-probs of the sampled ids (and entropy, lse) of hidden @ weight.T
+    without forming the logits (rl_lmhead_logprobs).  hidden [R, D] and weight
+    [V, D] are bf16 CUDA tensors with unit column stride.  ``workspace``: "new"
+    allocates the size the launch can use to balance the SMs, None runs
+    unsliced, a uint8 tensor is used as given (zero-filled before first use)."""
+    R, D = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    logp = torch.empty(R, dtype=torch.float32, device=dev)
+    ent = torch.empty(R, dtype=torch.float32, device=dev) if want_entropy else None
+    lse = torch.empty(R, dtype=torch.float32, device=dev) if want_lse else None
+    if isinstance(workspace, str):
+        nb = rl_lmhead_workspace_size(R, V)
+        workspace = torch.zeros(nb, dtype=torch.uint8, device=dev) if nb else None
+    rl_lmhead_logprobs(hidden, hidden.stride(0), weight, weight.stride(0), R, D, V, ids, logp, ent,
+                       lse, status, workspace, workspace.numel() if workspace is not None else 0,
+                       stream)
+    return dict(logp=logp, entropy=ent, lse=lse, workspace=workspace)

@@ -196,3 +196,31 @@ def test_lmhead_unit_groups(sliced):
     got = run_gpu(hidden, weight, ids, D, V, sliced=sliced)
     assert got[3] == 0
     check(got[:3], oracle_rows(hidden, weight, ids, D))
+
+
+def test_lmhead_torch_api_and_cuda_graph():
+    """torch_api.lmhead_logprobs matches the oracle, and the launch captured in a
+    CUDA graph replays to the same bits (the tensor maps travel as launch
+    parameters; the workspace tickets are left at zero by every launch)."""
+    from ppo_policy_loss_gb300 import torch_api
+    R, D, V = 1000, 256, 20000
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 21, 3.0)
+    dev = torch.device("cuda:0")
+    h, w, i = hidden.to(dev), weight.to(dev), ids.to(dev)
+    out = torch_api.lmhead_logprobs(h, w, i, want_lse=True)
+    torch.cuda.synchronize()
+    check((out["lse"].cpu().numpy(), out["logp"].cpu().numpy(), out["entropy"].cpu().numpy()),
+          oracle_rows(hidden, weight, ids, D))
+    ws = out["workspace"]
+    lp = torch.empty(R, device=dev)
+    s = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            rl.rl_lmhead_logprobs(h, D, w, D, R, D, V, i, lp, None, None, None, ws,
+                                  ws.numel() if ws is not None else 0, s)
+    for _ in range(3):
+        lp.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(lp, out["logp"])

@@ -602,3 +602,39 @@ def test_global_counts_split_batch(agg):
     assert parts[0]["n_tokens"] + parts[1]["n_tokens"] == st["n_tokens"]
     cat = torch.cat([x["dlogits"] for x in halves])
     assert torch.equal(cat.view(torch.int16), full["dlogits"].view(torch.int16))
+
+
+def test_loss_waits_for_the_kernel_before_it():
+    """The loss launch may start while the kernel before it in the stream still
+    runs (programmatic dependent launch); it must still read that kernel's
+    output.  A single-CTA whitening over a long buffer (the advantages plus
+    four million masked-out elements, ~1 ms) rewrites the per-token
+    advantages in place, and the loss is launched right after it with no host
+    synchronisation: the loss must match the oracle on the WHITENED
+    advantages."""
+    w = W["ppo_gae"].scaled(n_prompts=8)
+    small = synth.small_inputs(w)
+    logits = synth.logits(w, device="cuda")
+    V, R = w.V, w.R
+    mask, ids = small["mask"], small["ids"]
+    A, _ = oracle.gae(small["rewards"], small["values"], small["lengths"], w.gamma, w.lam)
+    A = A.astype(np.float32).reshape(-1)
+    extra = 4 << 20
+    buf = np.concatenate([A, np.full(extra, 123.0, np.float32)])
+    wmask = np.concatenate([mask, np.zeros(extra, np.uint8)])
+    A_w = oracle.masked_whiten(A, mask, 1e-8, True).astype(np.float32)
+    lse, logp, ent = oracle_stats_chunked(logits, w.dtype, V, ids, mask)
+    lo, _ = composed_old_ref(logp, small, mask, R)
+    ref = oracle.loss_from_stats(logp, ent, mask, A_w.astype(np.float64), lo, None, w.eps, 0.0,
+                                 w.c_ent)
+    band = band_mask(ref, w.eps) & (mask != 0)
+    d_buf, d_wmask = to_dev(buf), to_dev(wmask)
+    d_ids, d_mask, d_lo = to_dev(ids), to_dev(mask), to_dev(lo)
+    torch.cuda.synchronize()
+    torch_api.masked_whiten(d_buf, d_wmask, 1e-8, True, out=d_buf)  # in place, ~1 ms
+    out = torch_api.policy_loss(logits, d_ids, d_mask, d_buf[:R], w.B, w.T, logp_old=d_lo,
+                                eps=w.eps, beta=0.0, c_ent=w.c_ent, grad_scale=1.0,
+                                dlogits=None)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(d_buf[:R].cpu().numpy() - A_w) <= ADV_TOL * np.maximum(np.abs(A_w), 1.0))
+    assert_stats_match(torch_api.read_stats(out["stats"]), ref, int(band.sum()))

@@ -733,7 +733,7 @@ def run_lmhead(args):
     ent = torch.empty(R, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = torch.zeros(max(16, rl.rl_lmhead_workspace_size(R, V)), dtype=torch.uint8, device=dev)
-    n_sl, grid, _, group = rl.rl_lmhead_plan(R, V, ws.numel(), D=D)
+    n_sl, grid, group, _ = rl.rl_lmhead_plan(R, D, V, ws.numel())
     stream = torch.cuda.current_stream(dev)
 
     def launch(hh, out_lp, out_en):

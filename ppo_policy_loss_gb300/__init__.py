@@ -245,15 +245,15 @@ def rl_lmhead_workspace_size(R, V) -> int:
     return int(load().rl_lmhead_workspace_size(R, V))
 
 
-def rl_lmhead_plan(R, V, workspace_bytes, sm_count=0, D=1024):
-    """(vocabulary slices per row tile, CTAs, workspace bytes used, row tiles per
-    unit group) of the launch on a GPU of ``sm_count`` SMs (0: the current
-    device)."""
+def rl_lmhead_plan(R, D, V, workspace_bytes, sm_count=0):
+    """(vocabulary slices per row tile, CTAs, row tiles per unit group, workspace
+    bytes used) of the launch on a GPU of ``sm_count`` SMs (0: the current
+    device); the C call's outputs in their order."""
     ns, grid, grp, need = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
     _check(load().rl_lmhead_plan(R, D, V, workspace_bytes, sm_count, ctypes.byref(ns),
                                  ctypes.byref(grid), ctypes.byref(grp), ctypes.byref(need)),
            "rl_lmhead_plan")
-    return ns.value, grid.value, need.value, grp.value
+    return ns.value, grid.value, grp.value, need.value
 
 
 def rl_policy_loss_launch_shape(dtype, V, n_rows):

@@ -215,9 +215,9 @@ def test_lmhead_host_errors(lib, over, expect):
 
 def test_lmhead_plan_rejects_bad_shapes(lib):
     with pytest.raises(rl.RlLossError):
-        rl.rl_lmhead_plan(0, 1000, 0, 152)
+        rl.rl_lmhead_plan(0, 1024, 1000, 0, 152)
     with pytest.raises(rl.RlLossError):
-        rl.rl_lmhead_plan(128, 0, 0, 152)
+        rl.rl_lmhead_plan(128, 1024, 0, 0, 152)
 
 
 @pytest.mark.parametrize("R,V", [(32768, 151936), (65536, 151936), (1024, 151936), (128, 151936),
@@ -228,7 +228,7 @@ def test_lmhead_plan_balances_the_sms(lib, R, V):
     workspace the launch is unsliced."""
     sms = 152
     n_mt, n_nt = -(-R // 128), -(-V // 256)
-    ns, grid, need, grp = rl.rl_lmhead_plan(R, V, 1 << 40, sms)
+    ns, grid, grp, need = rl.rl_lmhead_plan(R, 1024, V, 1 << 40, sms)
     assert 1 <= grp <= n_mt
     assert 1 <= ns <= n_nt and grid == min(sms, n_mt * ns)
     if ns > 1:
@@ -241,8 +241,8 @@ def test_lmhead_plan_balances_the_sms(lib, R, V):
     ideal = n_mt * n_nt / sms
     if ideal >= 8:
         assert max(load) <= 1.06 * ideal, (ns, max(load), ideal)
-    assert rl.rl_lmhead_plan(R, V, 0, sms)[0] == 1
-    assert rl.rl_lmhead_plan(R, V, 0, sms)[2] == 0
+    assert rl.rl_lmhead_plan(R, 1024, V, 0, sms)[0] == 1
+    assert rl.rl_lmhead_plan(R, 1024, V, 0, sms)[3] == 0
 
 
 @pytest.mark.parametrize("D,expect", [(1024, 160), (2048, 80), (4096, 40), (200, 640)])
@@ -250,6 +250,6 @@ def test_lmhead_plan_groups_row_tiles_to_fit_l2(lib, D, expect):
     """Units are grouped so that the hidden tiles in use at one time (128 rows x D
     bf16 each, D rounded up to 64) stay within a 40 MB share of L2."""
     n_mt = 2000
-    grp = rl.rl_lmhead_plan(128 * n_mt, 151936, 1 << 40, 152, D=D)[3]
+    grp = rl.rl_lmhead_plan(128 * n_mt, D, 151936, 1 << 40, 152)[2]
     assert grp == min(expect, n_mt)
     assert grp * 128 * (-(-D // 64) * 64) * 2 <= 40 << 20

@@ -46,7 +46,7 @@ def run_gpu(hidden, weight, ids, D, V, status=None, sliced=True, ws_bytes=None, 
     rl.rl_lmhead_logprobs(h, h.stride(0), w, w.stride(0), R, D, V, i, logp, ent, lse, st,
                           ws, ws.numel() if ws is not None else 0)
     torch.cuda.synchronize()
-    if ws is not None and rl.rl_lmhead_plan(R, V, ws.numel())[0] > 1:
+    if ws is not None and rl.rl_lmhead_plan(R, D, V, ws.numel())[0] > 1:
         n_mt = -(-R // 128)
         assert int(ws[: n_mt * 4].view(torch.int32).abs().sum()) == 0, "tickets not reset"
     return lse.cpu().numpy(), logp.cpu().numpy(), ent.cpu().numpy(), int(st.item())
@@ -110,7 +110,7 @@ def test_lmhead_slice_counts_agree():
     seen = set()
     for k in (1, 2, 3, None):
         nb = None if k is None else ((n_mt * 4 + 255) // 256 * 256 + k * R * 16 if k > 1 else 0)
-        ns = rl.rl_lmhead_plan(R, V, rl.rl_lmhead_workspace_size(R, V) if nb is None else nb)[0]
+        ns = rl.rl_lmhead_plan(R, D, V, rl.rl_lmhead_workspace_size(R, V) if nb is None else nb)[0]
         seen.add(ns)
         got = run_gpu(None, None, None, D, V, ws_bytes=nb, dev_inputs=dev_in)
         assert got[3] == 0
@@ -126,7 +126,7 @@ def test_lmhead_qwen3_shape_sampled_rows():
     oracle recomputes 96 sampled rows, including the first and last."""
     R, D, V = 32 * 1024, 1024, 151936
     hidden, weight, ids = synth.lmhead_inputs(R, D, V, 8, 3.0)
-    assert rl.rl_lmhead_plan(R, V, rl.rl_lmhead_workspace_size(R, V))[0] > 1
+    assert rl.rl_lmhead_plan(R, D, V, rl.rl_lmhead_workspace_size(R, V))[0] > 1
     lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V)
     assert st == 0
     assert np.isfinite(lse).all() and np.isfinite(logp).all() and np.isfinite(ent).all()
@@ -190,8 +190,8 @@ def test_lmhead_unit_groups(sliced):
     group, so 45 row tiles make a full group and a 5-tile tail group."""
     R, D, V = 128 * 45 - 3, 4096, 3000
     ws_bytes = rl.rl_lmhead_workspace_size(R, V) if sliced else 0
-    plan = rl.rl_lmhead_plan(R, V, ws_bytes, D=D)
-    assert plan[3] == 40 and (plan[0] > 1) == sliced
+    plan = rl.rl_lmhead_plan(R, D, V, ws_bytes)
+    assert plan[2] == 40 and (plan[0] > 1) == sliced
     hidden, weight, ids = synth.lmhead_inputs(R, D, V, 12, 4.0)
     got = run_gpu(hidden, weight, ids, D, V, sliced=sliced)
     assert got[3] == 0

@@ -2,9 +2,10 @@
 
 Small cases compare every output element by element (loss and statistics,
 per-token logp and entropy, every dlogits element at grad_scale 1 and N);
-they are sized to span several 16 KB chunks, both row layouts (rows held
-on chip for both passes, and rows streamed twice through the ring, up to
-256 chunks per row), ragged vocabulary tails and padded rows.  The
+they are sized to span several 32 KB chunks, both row layouts (rows of at
+most two chunks held on chip for both passes, longer rows streamed twice
+through the ring, up to 128 chunks per row, including a row whose last
+chunk is 16 bytes), ragged vocabulary tails and padded rows.  The
 full-size workloads run in the launch configuration the benchmark times and
 are compared on the scalar loss and statistics (all rows), on logp/entropy
 (all rows), on sampled dlogits rows, and on properties that hold at any size
@@ -92,14 +93,20 @@ SMALL = {
                                                      lengths=("uniform", 0, 16), c_ent=0.05),
     "f16_v7_tiny": W["long_seq_grpo"].scaled(n_prompts=2, group=4, T=8, V=7,
                                              lengths=("uniform", 1, 8), beta=0.1),
-    "bf16_single_chunk": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=8192,
+    "bf16_single_chunk": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=16384,
                                                      lengths=("uniform", 1, 8)),
+    "bf16_half_chunk": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=8192,
+                                                   lengths=("uniform", 1, 8)),
     "f32_v1M_stream": W["tiny_grpo"].scaled(n_prompts=1, group=2, T=4, V=1 << 20,
                                             lengths=("uniform", 1, 4)),
     "bf16_v300001_stream": W["large_grpo"].scaled(n_prompts=1, group=4, T=4, V=300001,
                                                   lengths=("uniform", 1, 4), c_ent=0.01),
-    "f16_v49152_resident": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=49152,
-                                                     lengths=("uniform", 2, 8)),
+    "f16_v32768_resident_max": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=32768,
+                                                         lengths=("uniform", 2, 8)),
+    "f16_v32776_stream_min": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=32776,
+                                                       lengths=("uniform", 2, 8), c_ent=0.02),
+    "f16_v49152_stream": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=49152,
+                                                   lengths=("uniform", 2, 8)),
 }
 PADDED_LD = {"f32_v12345_ragged": 12348, "bf16_v1001_ragged": 1008, "f16_v7_tiny": 8,
              "bf16_v300001_stream": 300008}

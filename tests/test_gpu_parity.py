@@ -645,3 +645,58 @@ def test_loss_waits_for_the_kernel_before_it():
     torch.cuda.synchronize()
     assert np.all(np.abs(d_buf[:R].cpu().numpy() - A_w) <= ADV_TOL * np.maximum(np.abs(A_w), 1.0))
     assert_stats_match(torch_api.read_stats(out["stats"]), ref, int(band.sum()))
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 151936), ("f16", 32000), ("f32", 5000)])
+def test_minus_infinity_and_extreme_logits(dtype, V):
+    """Padded-vocabulary rows: the last 267 entries of every row are -inf (as
+    when a 151,669-token vocabulary is padded to 151,936), 1% of the other
+    entries are -inf, and a few rows carry extreme logits (+3e4 and -3e4 in
+    16-bit formats, 1e6 in fp32: a max far from the bulk, exponents that
+    underflow; one row scaled by 10).  Sampled ids
+    are finite entries.  With the entropy bonus and the KL term on, every
+    output must match the oracle, which takes 0 log 0 = 0."""
+    base = W["qwen3_0p6b_grpo"] if dtype == "bf16" else W["long_seq_grpo"]
+    w = base.scaled(dtype=dtype, V=V, n_prompts=2, group=4, T=6, lengths=("uniform", 1, 6),
+                    c_ent=0.02, beta=0.05, seed=77)
+    small = synth.small_inputs(w)
+    logits = synth.logits(w, device="cuda")
+    R = w.R
+    g = torch.Generator(device="cuda").manual_seed(5)
+    hole = torch.rand((R, V), generator=g, device="cuda") < 0.01
+    hole[:, V - 267:] = True
+    logits[hole] = float("-inf")
+    big = 3e4 if dtype != "f32" else 1e6
+    logits[1, 10] = big
+    logits[2, 11] = -big
+    logits[3, ::7] = logits[3, ::7] * 10.0
+    host = storage_np(logits)
+    zf = oracle.decode(host, dtype)
+    ids = small["ids"].copy()
+    for r in range(R):  # a sampled token has a finite logit
+        while not np.isfinite(zf[r, ids[r]]):
+            ids[r] = (ids[r] + 1) % (V - 267)
+    # row 1 samples its dominant entry (logp ~ 0); a sampled logp near -3e4 would leave fp32
+    # too few bits for the ratio exp(logp - logp_old), in any implementation
+    ids[1] = 10
+    mask = small["mask"]
+    arow, adv = adv_rows(w, small)
+    lse, logp, ent = oracle.row_stats(host, dtype, V, ids, mask)
+    lo, rf = composed_old_ref(logp, small, mask, R)
+    ref = oracle.loss_from_stats(logp, ent, mask, arow, lo, rf, w.eps, w.beta, w.c_ent)
+    band = band_mask(ref, w.eps) & (mask != 0)
+    N = ref["n_tokens"]
+    out = torch_api.policy_loss(logits, to_dev(ids), to_dev(mask), to_dev(adv.astype(np.float32)),
+                                w.B, w.T, logp_old=to_dev(lo), ref_logp=to_dev(rf), eps=w.eps,
+                                beta=w.beta, c_ent=w.c_ent, grad_scale=float(N))
+    torch.cuda.synchronize()
+    st = torch_api.read_stats(out["stats"])
+    assert_stats_match(st, ref, int(band.sum()))
+    assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
+    rows = np.array([r for r in range(R) if not band[r]])
+    scale = np.where(mask[rows] != 0, 1.0, 0.0)  # grad_scale N times the 1/N of the token mean
+    d_ref = oracle.dlogits_rows(host[rows], dtype, V, ids[rows], np.arange(rows.size), lse[rows],
+                                ent[rows], ref["g"][rows], scale, w.c_ent, dtype)
+    d_gpu = storage_np(out["dlogits"].index_select(0, to_dev(rows)))
+    assert_dlogits_close(d_gpu, d_ref, dtype, where=f"{dtype} V={V}")
+    assert not torch.isnan(out["dlogits"].float()).any()

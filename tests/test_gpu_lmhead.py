@@ -224,3 +224,19 @@ def test_lmhead_torch_api_and_cuda_graph():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(lp, out["logp"])
+
+
+def test_lmhead_zero_hidden_rows_are_uniform():
+    """A zero hidden state gives all-zero logits: lse = entropy = ln V and
+    logp = -ln V exactly in closed form (the uniform distribution)."""
+    R, D, V = 300, 128, 151936
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 23, 3.0)
+    zero = np.arange(0, R, 7)
+    hidden[zero] = 0
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V)
+    assert st == 0
+    lnV = np.log(V)
+    assert np.abs(lse[zero] - lnV).max() <= LOGP_ATOL
+    assert np.abs(ent[zero] - lnV).max() <= LOGP_ATOL
+    assert np.abs(logp[zero] + lnV).max() <= LOGP_ATOL
+    check((lse, logp, ent), oracle_rows(hidden, weight, ids, D))

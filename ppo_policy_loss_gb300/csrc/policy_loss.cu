@@ -26,6 +26,9 @@
 //     resident row, statistics exchanged through distributed shared memory)
 //     is kept for comparison builds; it costs a cluster-wide exchange per row
 //     and loses to streaming on GB300.
+//   * A zero warp writes the all-zero gradient of masked rows (their logits
+//     are never read), paced to within a row of the consumers, so masked
+//     rows' stores overlap the valid rows' arithmetic.
 //   * Sixteen consumer warps.  Pass 1: per-thread online (max, sum 2^x,
 //     sum 2^x * x) in packed fp32x2 with independent accumulator chains.
 //     Each warp shuffle-merges its lanes and publishes one partial; the
@@ -78,7 +81,7 @@ constexpr int kChunkBytes = 32768;
 constexpr int kSlots = RL_RING_SLOTS;
 constexpr int kConsumerWarps = RL_CONSUMER_WARPS;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kThreads = kConsumerThreads + 64;  // + the producer warp and the zero warp
 constexpr int kMaxCluster = 8;
 constexpr int kVecsPerChunk = kChunkBytes / 16;
 constexpr int kVecsPerThread = kVecsPerChunk / kConsumerThreads;
@@ -86,6 +89,7 @@ static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly ov
 static_assert(kConsumerWarps * kMaxCluster <= 128, "partials of one row fit 4 per lane");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kConsumerBarrier = 1;  // named barrier id (0 is __syncthreads)
+constexpr long long kZeroLead = 1;        // rows the zero warp may run ahead of the consumers
 
 struct LossSmem {
   alignas(128) unsigned char ring[kSlots][kChunkBytes];
@@ -98,6 +102,7 @@ struct LossSmem {
   double wred[kConsumerWarps][5];
   int abort;
   int is_last;
+  long long pace;  // row the consumers are on (the zero warp keeps within a few rows of it)
 };
 
 struct LossArgs {
@@ -409,13 +414,12 @@ __device__ __forceinline__ void grad_vec(uint4 w, float cL, float a0, float a1, 
   }
 }
 
+// All-zero gradient slice of a masked row, written by the 32 lanes of one warp.
 template <class E>
-__device__ __forceinline__ void zero_slice(unsigned char* drow, long long nelem, int tid) {
+__device__ __forceinline__ void zero_slice(unsigned char* drow, long long nelem, int lane) {
   const long long nvec = nelem / E::kVec;
-  for (long long j = tid; j < nvec; j += kConsumerThreads)
-    st_global_cs_v4(drow + j * 16, make_uint4(0u, 0u, 0u, 0u));
-  for (long long e = nvec * E::kVec + tid; e < nelem; e += kConsumerThreads)
-    E::store1(drow + e * E::kBytes, 0.f);
+  for (long long j = lane; j < nvec; j += 32) st_global_cs_v4(drow + j * 16, make_uint4(0u, 0u, 0u, 0u));
+  for (long long e = nvec * E::kVec + lane; e < nelem; e += 32) E::store1(drow + e * E::kBytes, 0.f);
 }
 
 // Wait for a bulk copy to land regardless of the abort flag (used to drain).
@@ -532,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     mbar_init(smem_addr(&sm.xbar[1]), n_parts);
     sm.abort = 0;
     sm.is_last = 0;
+    sm.pace = -1;
     fence_mbar_init();
   }
   __syncthreads();
@@ -585,6 +590,27 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       if (stop) {  // let every copy already issued land before this CTA can exit
         for (uint32_t k = it > kSlots ? it - kSlots : 0; k < it; ++k)
           drain_wait(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1);
+      }
+    }
+  } else if (warp == kConsumerWarps + 1) {
+    // ---------------------------------------------------------------- zero warp
+    // Masked rows need no logits, only an all-zero gradient slice: this warp
+    // writes them while the consumers work on the valid rows, so the masked
+    // rows' stores overlap the valid rows' arithmetic.  It keeps within
+    // kZeroLead rows of the consumers, so the writes stay spread over the
+    // launch instead of arriving as one burst at its start.
+    const volatile long long* pace = &sm.pace;
+    for (long long row = cid; row < a.R; row += ncl) {
+      if (a.mask[row] != 0) continue;
+      if (*pace < row - kZeroLead * static_cast<long long>(ncl)) {  // bounded wait, then go on
+        const uint64_t t0 = global_ns();
+        while (*pace < row - kZeroLead * static_cast<long long>(ncl) && global_ns() - t0 < kWaitLimitNs)
+          __nanosleep(500);
+      }
+      if (a.dlogits) zero_slice<E>(a.dlogits + row * a.row_bytes + lo * E::kBytes, nelem, lane);
+      if (rank == 0 && lane == 0) {
+        if (a.logp_out) a.logp_out[row] = 0.f;
+        if (a.entropy_out) a.entropy_out[row] = 0.f;
       }
     }
   } else {
@@ -641,17 +667,11 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     bool aborted = false;
 
     for (long long row = cid; row < a.R; row += ncl) {
+      if (tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = row;
       const RowScalars rs = cur;
       cur = load_row(a, row + ncl);  // next row's scalars, in flight during this row
       unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes + lo * E::kBytes : nullptr;
-      if (!rs.valid) {
-        if (drow) zero_slice<E>(drow, nelem, tid);
-        if (rank == 0 && tid == 0) {
-          if (a.logp_out) a.logp_out[row] = 0.f;
-          if (a.entropy_out) a.entropy_out[row] = 0.f;
-        }
-        continue;
-      }
+      if (!rs.valid) continue;  // the zero warp writes masked rows
       if (*abort_flag) {
         aborted = true;
         break;
@@ -882,6 +902,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       }
       ++vrow;
     }
+    if (tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = a.R + 1;  // release the zero warp
 
     // ---- per-CTA partial, then the last CTA reduces all partials in CTA order
     if (tid == 0) {

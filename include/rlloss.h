@@ -457,6 +457,22 @@ rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, long long n_r
  */
 rl_status rl_read_device_status(const void* workspace, void* stream);
 
+/*
+ * Self-test of failure detection, without a fault: every wait on an on-chip
+ * barrier in this library's kernels is bounded, and a wait that runs out
+ * raises RL_DEVERR_TIMEOUT and lets the kernel return normally, so the CUDA
+ * context stays usable.  This call runs that same bounded wait, for
+ * limit_ns nanoseconds, on a barrier that nothing completes: one thread of
+ * one CTA waits, gives up, ORs RL_DEVERR_TIMEOUT into *status_dev (one
+ * unsigned int in device memory) and writes the nanoseconds it waited to
+ * *waited_ns_dev (device, may be NULL).  The pages have no counterpart; it
+ * exists so that tests can check the timeout path on a GPU.
+ * Errors: RL_ERR_NULL (status_dev), RL_ERR_ARG (limit_ns outside
+ * [1 us, 10 s]), RL_ERR_CUDA.
+ */
+rl_status rl_selftest_wait_timeout(unsigned long long limit_ns, unsigned int* status_dev,
+                                   unsigned long long* waited_ns_dev, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* rl_status_string(rl_status status);
 

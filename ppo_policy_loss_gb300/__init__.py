@@ -35,7 +35,7 @@ __all__ = [
     "rl_policy_loss_desc", "rl_policy_loss_fwd_bwd_noalloc", "rl_policy_loss_launch_shape",
     "rl_read_device_status", "rl_masked_whiten", "rl_count_tokens", "rl_value_loss_fwd_bwd",
     "rl_value_stats", "value_stats_from_bytes", "rl_lmhead_logprobs",
-    "rl_lmhead_workspace_size", "rl_lmhead_plan",
+    "rl_lmhead_workspace_size", "rl_lmhead_plan", "rl_selftest_wait_timeout",
     "rl_status_string", "rl_loss_stats", "RlLossError", "build", "load", "stats_from_bytes",
 ]
 
@@ -116,6 +116,8 @@ def load(path: str | None = None):
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
     lib.rl_read_device_status.argtypes = [P, P]
+    lib.rl_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, P, P, P]
+    lib.rl_selftest_wait_timeout.restype = I
     lib.rl_status_string.argtypes = [I]
     lib.rl_status_string.restype = ctypes.c_char_p
     for fn in ("rl_group_advantages", "rl_gae_reverse_scan", "rl_policy_loss_fwd_bwd",
@@ -262,6 +264,11 @@ def rl_policy_loss_launch_shape(dtype, V, n_rows):
                                               ctypes.byref(n), ctypes.byref(s)),
            "rl_policy_loss_launch_shape")
     return c.value, n.value, s.value
+
+
+def rl_selftest_wait_timeout(limit_ns, status_dev, waited_ns_dev=None, stream=None):
+    _check(load().rl_selftest_wait_timeout(int(limit_ns), _ptr(status_dev), _ptr(waited_ns_dev),
+                                           _stream(stream)), "rl_selftest_wait_timeout")
 
 
 def rl_read_device_status(workspace, stream=None) -> int:

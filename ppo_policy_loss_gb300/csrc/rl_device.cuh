@@ -200,10 +200,11 @@ __device__ __forceinline__ void allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Spin on an mbarrier phase for at most kWaitLimitNs.  Returns false on
-// timeout (after raising `*abort`) or immediately if `*abort` is already set.
+// Spin on an mbarrier phase for at most limit_ns.  Returns false on timeout
+// (after raising `*abort`) or immediately if `*abort` is already set.
 template <bool kClusterScope>
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool wait_bounded_for(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                 uint64_t limit_ns) {
   bool ok = kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   if (ok) return true;
   uint64_t t0 = global_ns();
@@ -211,11 +212,15 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     if (*abort) return false;
     ok = kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     if (ok) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
   }
+}
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return wait_bounded_for<kClusterScope>(bar, parity, abort, kWaitLimitNs);
 }
 
 }  // namespace rl

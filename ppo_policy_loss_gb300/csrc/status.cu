@@ -31,3 +31,36 @@ extern "C" rl_status rl_read_device_status(const void* workspace, void* stream) 
   if (word & RL_DEVERR_TIMEOUT) return RL_ERR_TIMEOUT;
   return RL_OK;
 }
+
+// ------------------------------------------------------------------ wait self-test
+namespace rl {
+namespace {
+
+// One thread waits on a shared-memory barrier that nothing ever completes,
+// through the same bounded wait the kernels use, then reports.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, unsigned int* status,
+                                     unsigned long long* waited_ns) {
+  __shared__ unsigned long long bar;
+  __shared__ int abort;
+  if (threadIdx.x != 0) return;
+  abort = 0;
+  mbar_init(smem_addr(&bar), 1);
+  fence_mbar_init();
+  const uint64_t t0 = global_ns();
+  const bool ok = wait_bounded_for<false>(smem_addr(&bar), 0, &abort, limit_ns);
+  const uint64_t t1 = global_ns();
+  if (!ok) atomicOr(status, RL_DEVERR_TIMEOUT);
+  if (waited_ns) *waited_ns = t1 - t0;
+}
+
+}  // namespace
+}  // namespace rl
+
+extern "C" rl_status rl_selftest_wait_timeout(unsigned long long limit_ns, unsigned int* status_dev,
+                                              unsigned long long* waited_ns_dev, void* stream) {
+  if (!status_dev) return RL_ERR_NULL;
+  if (limit_ns < 1000ull || limit_ns > 10ull * 1000ull * 1000ull * 1000ull) return RL_ERR_ARG;
+  rl::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, status_dev,
+                                                                           waited_ns_dev);
+  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}

@@ -253,3 +253,9 @@ def test_lmhead_plan_groups_row_tiles_to_fit_l2(lib, D, expect):
     grp = rl.rl_lmhead_plan(128 * n_mt, D, 151936, 1 << 40, 152)[2]
     assert grp == min(expect, n_mt)
     assert grp * 128 * (-(-D // 64) * 64) * 2 <= 40 << 20
+
+
+def test_selftest_wait_timeout_host_errors(lib):
+    assert lib.rl_selftest_wait_timeout(1000000, None, None, None) == rl.RL_ERR_NULL
+    assert lib.rl_selftest_wait_timeout(10, FAKE, None, None) == rl.RL_ERR_ARG
+    assert lib.rl_selftest_wait_timeout(11 * 10**9, FAKE, None, None) == rl.RL_ERR_ARG

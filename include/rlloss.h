@@ -192,10 +192,10 @@ size_t rl_policy_loss_workspace_size(long long n_rows);
  *                 Base address 16-byte aligned; ld * sizeof(dtype) a multiple
  *                 of 16 (pad rows if V is odd); ld >= V.
  *   dtype       : RL_F32, RL_BF16 or RL_F16 (for logits and dlogits alike).
- *   B, T, V, ld : B >= 0, T >= 0, V >= 1.  V up to the on-chip row limit of
- *                 the device (every valid row is held on chip across a
- *                 cluster of up to 8 CTAs: about 1.6 MB per row; larger
- *                 rows return RL_ERR_SHAPE).
+ *   B, T, V, ld : B >= 0, T >= 0, 1 <= V <= 2^30.  Rows of at most 64 KB
+ *                 stay on chip for both passes; longer rows are streamed
+ *                 through shared memory twice, the second time from L2.
+ *                 Larger V returns RL_ERR_SHAPE.
  *   ids         : int64[R], the sampled token of each row.  An id outside
  *                 [0, V) on a valid row sets RL_DEVERR_ID_RANGE and makes
  *                 that row's logp, entropy, loss and gradient NaN.
@@ -213,6 +213,9 @@ size_t rl_policy_loss_workspace_size(long long n_rows);
  *                 zero-filled before its first use (see above).
  * Deterministic: the same inputs on the same device give bitwise identical
  * outputs (fixed-order fp64 reductions, no floating-point atomics).
+ * The launch allows programmatic dependent launch: it may be scheduled while
+ * the kernel before it on `stream` is still running, and reads no argument
+ * before that kernel has completed.
  */
 rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype,
                                  long long B, long long T, long long V, long long ld,

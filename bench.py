@@ -737,7 +737,7 @@ def run_lmhead(args):
     stream = torch.cuda.current_stream(dev)
 
     def launch(hh, out_lp, out_en):
-        rl.rl_lmhead_logprobs(hh, D, w, D, R, D, V, ids, out_lp, out_en, None, status, ws,
+        rl.rl_lmhead_logprobs(hh, D, w, D, "bf16", R, D, V, ids, out_lp, out_en, None, status, ws,
                               ws.numel(), stream)
 
     for _ in range(args.warmup):
@@ -791,7 +791,7 @@ def run_lmhead(args):
         for _ in range(steps):
             dh.copy_(hh, non_blocking=True)
             dids.copy_(hid, non_blocking=True)
-            rl.rl_lmhead_logprobs(dh, D, w, D, R, D, V, dids, logp, ent, None, status, ws,
+            rl.rl_lmhead_logprobs(dh, D, w, D, "bf16", R, D, V, dids, logp, ent, None, status, ws,
                                   ws.numel(), stream)
             o_lp.copy_(logp, non_blocking=True)
             o_en.copy_(ent, non_blocking=True)

@@ -392,12 +392,16 @@ rl_status rl_value_loss_fwd_bwd(const float* values, const float* values_old,
  * "技术深度解析", actor network with custom matrix multiplication); the
  * behaviour- and reference-policy log-probs the loss takes are these rows'
  * log pi(y_r | .).  For each row r < R, with z_r = hidden_r . W^T (fp32
- * accumulation of the exact bf16 products):
+ * accumulation of the exact products of the 16-bit inputs; the pages' FP16
+ * inputs with FP32 accumulation, pitchhut.com RL.cu listing, "Key Features"
+ * item 1):
  *   lse_out[r]     = log sum_v exp z_rv
  *   logp_out[r]    = z_r,ids[r] - lse_out[r]     (NaN when ids[r] is outside [0, V))
  *   entropy_out[r] = -sum_v p_rv log p_rv,  p_r = softmax(z_r)
- *   hidden : bf16 [R, D] device, row stride ld_h elements (ld_h >= D), read only;
- *   weight : bf16 [V, D] device, row stride ld_w elements (ld_w >= D), read only;
+ *   hidden : [R, D] of `dtype` (RL_BF16 or RL_F16), device, row stride ld_h
+ *            elements (ld_h >= D), read only;
+ *   weight : [V, D] of `dtype`, device, row stride ld_w elements (ld_w >= D),
+ *            read only;
  *            both 16-byte aligned, row strides multiples of 8 elements, D a
  *            multiple of 8;
  *   ids    : int64 [R] device;
@@ -414,12 +418,14 @@ rl_status rl_value_loss_fwd_bwd(const float* values, const float* values_old,
  *            results up to fp32 rounding order.  Calls sharing a workspace
  *            must not overlap on the GPU.
  * One launch of a persistent tensor-core kernel (tcgen05, TMA, tensor memory).
- * Allocates nothing; stream-ordered.  Errors: RL_ERR_SHAPE (R < 0, R >= 2^31,
+ * Allocates nothing; stream-ordered.  Errors: RL_ERR_DTYPE (not RL_BF16 or
+ * RL_F16), RL_ERR_SHAPE (R < 0, R >= 2^31,
  * V < 1, V > 2^31, D < 8, D not a multiple of 8, a stride below D),
  * RL_ERR_NULL, RL_ERR_ALIGN, RL_ERR_CUDA.  R == 0 launches nothing.
  */
 rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
-                             long long R, long long D, long long V, const long long* ids,
+                             rl_dtype dtype, long long R, long long D, long long V,
+                             const long long* ids,
                              float* logp_out, float* entropy_out, float* lse_out,
                              unsigned int* status_dev, void* workspace, size_t workspace_bytes,
                              void* stream);

@@ -104,7 +104,7 @@ def load(path: str | None = None):
     lib.rl_value_loss_fwd_bwd.argtypes = [P, P, P, P, LL, F, F, P, P, P]
     lib.rl_masked_whiten.argtypes = [P, P, LL, D, I, P, P]
     lib.rl_count_tokens.argtypes = [P, LL, LL, P, P]
-    lib.rl_lmhead_logprobs.argtypes = [P, LL, P, LL, LL, LL, LL, P, P, P, P, P, P, SZ, P]
+    lib.rl_lmhead_logprobs.argtypes = [P, LL, P, LL, I, LL, LL, LL, P, P, P, P, P, P, SZ, P]
     lib.rl_lmhead_workspace_size.argtypes = [LL, LL]
     lib.rl_lmhead_workspace_size.restype = SZ
     lib.rl_lmhead_plan.argtypes = [LL, LL, LL, SZ, I, ctypes.POINTER(I), ctypes.POINTER(I),
@@ -233,12 +233,12 @@ def value_stats_from_bytes(raw: bytes) -> dict:
     return {name: getattr(st, name) for name, _ in rl_value_stats._fields_}
 
 
-def rl_lmhead_logprobs(hidden, ld_h, weight, ld_w, R, D, V, ids, logp_out, entropy_out, lse_out,
-                       status_dev=None, workspace=None, workspace_bytes=0, stream=None):
+def rl_lmhead_logprobs(hidden, ld_h, weight, ld_w, dtype, R, D, V, ids, logp_out, entropy_out,
+                       lse_out, status_dev=None, workspace=None, workspace_bytes=0, stream=None):
     if workspace is not None and hasattr(workspace, "numel") and not workspace_bytes:
         workspace_bytes = workspace.numel() * workspace.element_size()
-    _check(load().rl_lmhead_logprobs(_ptr(hidden), ld_h, _ptr(weight), ld_w, R, D, V, _ptr(ids),
-                                     _ptr(logp_out), _ptr(entropy_out), _ptr(lse_out),
+    _check(load().rl_lmhead_logprobs(_ptr(hidden), ld_h, _ptr(weight), ld_w, _dtype(dtype), R, D, V,
+                                     _ptr(ids), _ptr(logp_out), _ptr(entropy_out), _ptr(lse_out),
                                      _ptr(status_dev), _ptr(workspace), workspace_bytes,
                                      _stream(stream)), "rl_lmhead_logprobs")
 

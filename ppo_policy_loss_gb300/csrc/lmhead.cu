@@ -67,6 +67,7 @@ struct LmSmem {
 
 struct LmArgs {
   long long R, D, V;
+  uint32_t idesc;         // tcgen05 instruction descriptor (operand format)
   int n_mt, n_nt, n_slices;
   int group;              // row tiles per unit group
   unsigned int* tickets;  // [n_mt] (n_slices > 1)
@@ -180,9 +181,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: fp32 D, bf16 A and B, both K-major, M x N.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+// Instruction descriptor: fp32 D, A and B both bf16 (format 1) or both fp16
+// (format 0), both K-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+}
 
 template <bool kDrain>
 __device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -284,7 +288,7 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
               umma_bf16(d_tmem, smem_desc_sw128(a_base + k * kUmmaK * 2), smem_desc_sw128(b_base + k * kUmmaK * 2),
-                        kIdesc, (kb | k) != 0);
+                        a.idesc, (kb | k) != 0);
             issued = true;
             umma_commit(smem_addr(&sm.empty[s]));  // the stage is free once these MMAs have read it
           }
@@ -444,13 +448,14 @@ rl_status encode_fn(EncodeTiled* out) {
 }
 
 // 2-D bf16 tensor map [rows, cols] (row stride ld elements), box box_rows x 64, 128B swizzle.
-bool make_map(EncodeTiled enc, CUtensorMap* map, const void* base, long long rows, long long cols, long long ld,
+bool make_map(EncodeTiled enc, CUtensorMap* map, CUtensorMapDataType dt, const void* base, long long rows,
+              long long cols, long long ld,
               uint32_t box_rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -541,11 +546,13 @@ extern "C" rl_status rl_lmhead_plan(long long R, long long D, long long V, size_
 }
 
 extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
-                                        long long R, long long D, long long V, const long long* ids,
+                                        rl_dtype dtype, long long R, long long D, long long V,
+                                        const long long* ids,
                                         float* logp_out, float* entropy_out, float* lse_out,
                                         unsigned int* status_dev, void* workspace, size_t workspace_bytes,
                                         void* stream) {
   using namespace rl;
+  if (dtype != RL_BF16 && dtype != RL_F16) return RL_ERR_DTYPE;
   if (!lm_shape_ok(R, V) || D < 8 || D % 8 != 0 || ld_h < D || ld_w < D) return RL_ERR_SHAPE;
   if (R == 0) return RL_OK;
   if (!hidden || !weight || !ids) return RL_ERR_NULL;
@@ -555,7 +562,9 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
   EncodeTiled enc = nullptr;
   if (encode_fn(&enc) != RL_OK) return RL_ERR_CUDA;
   CUtensorMap mh, mw;
-  if (!make_map(enc, &mh, hidden, R, D, ld_h, kBM) || !make_map(enc, &mw, weight, V, D, ld_w, kBN))
+  const CUtensorMapDataType tdt =
+      dtype == RL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!make_map(enc, &mh, tdt, hidden, R, D, ld_h, kBM) || !make_map(enc, &mw, tdt, weight, V, D, ld_w, kBN))
     return RL_ERR_CUDA;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || device_sms(&sms) != RL_OK) return RL_ERR_CUDA;
@@ -574,6 +583,7 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
   args.R = R;
   args.D = D;
   args.V = V;
+  args.idesc = make_idesc(dtype == RL_BF16);
   args.n_mt = plan.n_mt;
   args.n_nt = plan.n_nt;
   args.n_slices = plan.n_slices;

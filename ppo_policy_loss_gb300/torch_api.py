@@ -167,7 +167,7 @@ def lmhead_logprobs(hidden: torch.Tensor, weight: torch.Tensor, ids: torch.Tenso
                     status: torch.Tensor | None = None, stream=None) -> dict:
     """Per-row log-probs of the sampled ids (and entropy, lse) of hidden @ weight.T
     without forming the logits (rl_lmhead_logprobs).  hidden [R, D] and weight
-    [V, D] are bf16 CUDA tensors with unit column stride.  ``workspace``: "new"
+    [V, D] are bf16 or fp16 CUDA tensors (the same type) with unit column stride.  ``workspace``: "new"
     allocates the size the launch can use to balance the SMs, None runs
     unsliced, a uint8 tensor is used as given (zero-filled before first use)."""
     R, D = hidden.shape
@@ -179,7 +179,8 @@ def lmhead_logprobs(hidden: torch.Tensor, weight: torch.Tensor, ids: torch.Tenso
     if isinstance(workspace, str):
         nb = rl_lmhead_workspace_size(R, V)
         workspace = torch.zeros(nb, dtype=torch.uint8, device=dev) if nb else None
-    rl_lmhead_logprobs(hidden, hidden.stride(0), weight, weight.stride(0), R, D, V, ids, logp, ent,
+    rl_lmhead_logprobs(hidden, hidden.stride(0), weight, weight.stride(0), dtype_name(hidden), R, D, V,
+                       ids, logp, ent,
                        lse, status, workspace, workspace.numel() if workspace is not None else 0,
                        stream)
     return dict(logp=logp, entropy=ent, lse=lse, workspace=workspace)

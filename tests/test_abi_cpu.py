@@ -182,17 +182,20 @@ def test_fixed_form_rejects_group_rewards_layout(lib):
 
 
 def call_lmhead(lib, **over):
-    a = dict(hidden=FAKE, ld_h=1024, weight=FAKE + 0x1000000, ld_w=1024, R=256, D=1024, V=151936,
+    a = dict(hidden=FAKE, ld_h=1024, weight=FAKE + 0x1000000, ld_w=1024, dtype=rl.RL_BF16, R=256,
+             D=1024, V=151936,
              ids=FAKE + 0x2000000, logp=FAKE + 0x3000000, ent=None, lse=None, status=None,
              ws=None, ws_bytes=0, stream=None)
     a.update(over)
-    return lib.rl_lmhead_logprobs(a["hidden"], a["ld_h"], a["weight"], a["ld_w"], a["R"], a["D"],
+    return lib.rl_lmhead_logprobs(a["hidden"], a["ld_h"], a["weight"], a["ld_w"], a["dtype"], a["R"], a["D"],
                                   a["V"], a["ids"], a["logp"], a["ent"], a["lse"], a["status"],
                                   a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("over,expect", [
     (dict(R=-1), rl.RL_ERR_SHAPE),
+    (dict(dtype=rl.RL_F32), rl.RL_ERR_DTYPE),
+    (dict(dtype=7), rl.RL_ERR_DTYPE),
     (dict(D=0), rl.RL_ERR_SHAPE),
     (dict(D=1020, ld_h=1020, ld_w=1020), rl.RL_ERR_SHAPE),    # D not a multiple of 8
     (dict(V=0), rl.RL_ERR_SHAPE),

@@ -35,6 +35,7 @@ def run_gpu(hidden, weight, ids, D, V, status=None, sliced=True, ws_bytes=None, 
     dev = torch.device("cuda:0")
     h, w, i = dev_inputs if dev_inputs is not None else (hidden.to(dev), weight.to(dev), ids.to(dev))
     R = h.shape[0]
+    dtype = "f16" if h.dtype == torch.float16 else "bf16"
     lse = torch.full((R,), 7.0, device=dev)
     logp = torch.full((R,), 7.0, device=dev)
     ent = torch.full((R,), 7.0, device=dev)
@@ -43,7 +44,7 @@ def run_gpu(hidden, weight, ids, D, V, status=None, sliced=True, ws_bytes=None, 
     if sliced:
         nb = rl.rl_lmhead_workspace_size(R, V) if ws_bytes is None else ws_bytes
         ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=dev)
-    rl.rl_lmhead_logprobs(h, h.stride(0), w, w.stride(0), R, D, V, i, logp, ent, lse, st,
+    rl.rl_lmhead_logprobs(h, h.stride(0), w, w.stride(0), dtype, R, D, V, i, logp, ent, lse, st,
                           ws, ws.numel() if ws is not None else 0)
     torch.cuda.synchronize()
     if ws is not None and rl.rl_lmhead_plan(R, D, V, ws.numel())[0] > 1:
@@ -58,7 +59,7 @@ def oracle_rows(hidden, weight, ids, D, rows=None):
     idn = ids.numpy()
     if rows is not None:
         h, idn = h[rows], idn[rows]
-    return oracle.lmhead_row_stats(h, w, idn, "bf16")
+    return oracle.lmhead_row_stats(h, w, idn, "f16" if hidden.dtype == torch.float16 else "bf16")
 
 
 def check(got, ref, rows=slice(None)):
@@ -158,11 +159,11 @@ def test_lmhead_optional_outputs_and_empty():
     dev = torch.device("cuda:0")
     h, w, i = hidden.to(dev), weight.to(dev), ids.to(dev)
     logp = torch.empty(200, device=dev)
-    rl.rl_lmhead_logprobs(h, 64, w, 64, 200, 64, 500, i, logp, None, None, None)
+    rl.rl_lmhead_logprobs(h, 64, w, 64, "bf16", 200, 64, 500, i, logp, None, None, None)
     torch.cuda.synchronize()
     ref = oracle_rows(hidden, weight, ids, 64)
     assert np.abs(logp.cpu().numpy() - ref[1]).max() <= LOGP_ATOL
-    rl.rl_lmhead_logprobs(h, 64, w, 64, 0, 64, 500, i, logp, None, None, None)  # R = 0: no launch
+    rl.rl_lmhead_logprobs(h, 64, w, 64, "bf16", 0, 64, 500, i, logp, None, None, None)  # R = 0: no launch
     torch.cuda.synchronize()
 
 
@@ -217,7 +218,7 @@ def test_lmhead_torch_api_and_cuda_graph():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            rl.rl_lmhead_logprobs(h, D, w, D, R, D, V, i, lp, None, None, None, ws,
+            rl.rl_lmhead_logprobs(h, D, w, D, "bf16", R, D, V, i, lp, None, None, None, ws,
                                   ws.numel() if ws is not None else 0, s)
     for _ in range(3):
         lp.fill_(7.0)
@@ -239,4 +240,15 @@ def test_lmhead_zero_hidden_rows_are_uniform():
     assert np.abs(lse[zero] - lnV).max() <= LOGP_ATOL
     assert np.abs(ent[zero] - lnV).max() <= LOGP_ATOL
     assert np.abs(logp[zero] + lnV).max() <= LOGP_ATOL
+    check((lse, logp, ent), oracle_rows(hidden, weight, ids, D))
+
+
+@pytest.mark.parametrize("R,D,V,sliced", [(300, 200, 1000, False), (1000, 1024, 30000, True)])
+def test_lmhead_fp16_inputs(R, D, V, sliced):
+    """fp16 hidden states and weight (the pages' FP16 inputs with FP32
+    accumulation): the same kernel with fp16 tensor-core operands."""
+    hidden, weight, ids = synth.lmhead_inputs(R, D, V, 31 + R, 3.0)
+    hidden, weight = hidden.float().half(), weight.float().half()  # bf16 values are exact in fp16 here
+    lse, logp, ent, st = run_gpu(hidden, weight, ids, D, V, sliced=sliced)
+    assert st == 0
     check((lse, logp, ent), oracle_rows(hidden, weight, ids, D))

@@ -281,6 +281,26 @@ typedef struct {
    * ent_term and clip_frac are this rank's share of the global means (their
    * sum over ranks is the global value); n_tokens stays this rank's count. */
   const long long* global_counts;
+  /* Vocabulary parallelism (the LM head split over ranks by vocabulary
+   * columns): this call's logits are the columns [vocab_offset,
+   * vocab_offset + V) of a vocabulary of vocab_total columns (0 = V), and
+   * ids are global.  A row's softmax needs the statistics of every shard, so
+   * a step takes two launches per shard with one exchange between them:
+   *   1. partials_out != NULL: pass 1 only.  For each valid row, writes
+   *      float[4] = (max z, sum 2^((z - max) log2 e), sum 2^(..) (z - max) log2 e,
+   *      z_y or -inf when y is not in this shard) at partials_out[4 * row];
+   *      nothing else is written (dlogits, logp_out, entropy_out ignored).
+   *   2. After gathering the n_shards partial arrays of the shards in order
+   *      (shard k at shard_partials[4 * (k * B * T + row)]), shard_partials != NULL:
+   *      merges them in shard order, then computes the loss, logp, entropy and
+   *      this shard's dlogits columns.  Every shard reports the same loss and
+   *      statistics.
+   * Both NULL: the ordinary single-shard launch. */
+  long long vocab_offset;        /* default 0 */
+  long long vocab_total;         /* default 0 (= V) */
+  float* partials_out;           /* launch 1: float[4 * B * T], device */
+  const float* shard_partials;   /* launch 2: float[4 * n_shards * B * T], device */
+  int n_shards;                  /* launch 2: >= 1 */
 } rl_policy_loss_desc;
 
 /*

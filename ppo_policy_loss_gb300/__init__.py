@@ -65,7 +65,10 @@ class rl_policy_loss_desc(ctypes.Structure):
                 ("agg", ctypes.c_int), ("agg_norm", ctypes.c_double), ("dlogits", ctypes.c_void_p),
                 ("logp_out", ctypes.c_void_p), ("entropy_out", ctypes.c_void_p),
                 ("stats_dev", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("global_counts", ctypes.c_void_p)]
+                ("workspace_bytes", ctypes.c_size_t), ("global_counts", ctypes.c_void_p),
+                ("vocab_offset", ctypes.c_longlong), ("vocab_total", ctypes.c_longlong),
+                ("partials_out", ctypes.c_void_p), ("shard_partials", ctypes.c_void_p),
+                ("n_shards", ctypes.c_int)]
 
 
 class rl_value_stats(ctypes.Structure):

@@ -129,6 +129,11 @@ struct LossArgs {
   int agg;              // rl_loss_agg
   double agg_w;         // RL_AGG_TOKEN_SUM_NORM: 1 / agg_norm
   const long long* global_counts;  // device [N, B'] over all ranks, or null (local counts)
+  long long v_offset;              // global id of local column 0 (vocabulary shards)
+  long long v_total;               // vocabulary size for the id range check
+  float4* partials_out;            // shard partials, pass-1 launch
+  const float4* shard_partials;    // [n_shards][R] gathered partials, merge launch
+  int n_shards;
 };
 
 // ------------------------------------------------------------------ element formats
@@ -511,7 +516,10 @@ __device__ __forceinline__ float warp_group_advantage(const LossArgs& a, long lo
 // ------------------------------------------------------------------ the kernel
 // kStream: rows are streamed twice through the ring (second pass from L2);
 // otherwise each CTA's slice of a row stays in the ring for both passes.
-template <int DT, bool kStream>
+// kMode: 0 the whole loss; 1 (vocabulary shard) pass 1 only, writing each
+// row's partial statistics; 2 (vocabulary shard) merge the gathered shard
+// partials instead of pass 1, then the loss and this shard's gradient.
+template <int DT, bool kStream, int kMode>
 __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kernel(const LossArgs a) {
   using E = Elem<DT>;
   constexpr int kVec = E::kVec;
@@ -565,8 +573,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         valid_next = row + ncl < a.R ? a.mask[row + ncl] != 0 : false;  // one row ahead
         if (!valid || nchunks == 0) continue;
         const unsigned char* src = a.logits + row * a.row_bytes + lo * E::kBytes;
-        for (int pass = 0; pass < (kStream ? 2 : 1) && !stop; ++pass) {
-          const uint64_t pol = (kStream && pass == 0) ? pol_last : pol_first;
+        constexpr int kPasses = (kStream && kMode == 0) ? 2 : 1;
+        for (int pass = 0; pass < kPasses && !stop; ++pass) {
+          const uint64_t pol = (kPasses == 2 && pass == 0) ? pol_last : pol_first;
           for (int c = 0; c < nchunks; ++c, ++it) {
             const uint32_t slot = it % kSlots, round = it / kSlots;
             if (round > 0 &&
@@ -697,95 +706,128 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
       // Where the sampled id sits in this CTA's slice: chunk cy, vector jy of
       // the chunk (owned by thread ty as its vector qy), element iy.
       int cy = -1, jy = 0, iy = 0, ty = -1;
-      if (y >= lo && y < hi) {
-        const int off = static_cast<int>(y - lo);
+      const long long yl = y - a.v_offset;  // column of y in this shard
+      if (yl >= lo && yl < hi) {
+        const int off = static_cast<int>(yl - lo);
         cy = off / kChunkElems;
         jy = (off % kChunkElems) / kVec;
         iy = off % kVec;
         ty = jy % kConsumerThreads;
       }
 
-      // ---- pass 1: online statistics of this thread's share of the slice
-      ThreadStats st;
-      stats_init(st);
-      float zy = -INFINITY;
       const uint32_t base = it;
-      for (int c = 0; c < nchunks; ++c) {
-        const uint32_t k = it++, slot = k % kSlots;
-        wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
-        const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
-        const int c0 = c * kChunkElems;
-        if (c0 + kChunkElems <= nelem) {
-          accumulate_chunk<E>(buf, st);
-        } else {
-#pragma unroll
-          for (int q = 0; q < kVecsPerThread; ++q) {
-            const int e0 = c0 + (tid + q * kConsumerThreads) * kVec;
-            const int nv = max(0, min(kVec, nelem - e0));
-            const uint4 w = nv > 0 ? ld_shared_v4(buf + q * kConsumerThreads * 16) : make_uint4(0u, 0u, 0u, 0u);
-            accumulate_tail<E>(w, nv, st, q);
+      float M = -INFINITY, S = 0.f, Tt = 0.f, zyr = -INFINITY;
+      if constexpr (kMode != 2) {
+        // ---- pass 1: online statistics of this thread's share of the slice
+        ThreadStats st;
+        stats_init(st);
+        float zy = -INFINITY;
+        for (int c = 0; c < nchunks; ++c) {
+          const uint32_t k = it++, slot = k % kSlots;
+          wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
+          const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
+          const int c0 = c * kChunkElems;
+          if (c0 + kChunkElems <= nelem) {
+            accumulate_chunk<E>(buf, st);
+          } else {
+  #pragma unroll
+            for (int q = 0; q < kVecsPerThread; ++q) {
+              const int e0 = c0 + (tid + q * kConsumerThreads) * kVec;
+              const int nv = max(0, min(kVec, nelem - e0));
+              const uint4 w = nv > 0 ? ld_shared_v4(buf + q * kConsumerThreads * 16) : make_uint4(0u, 0u, 0u, 0u);
+              accumulate_tail<E>(w, nv, st, q);
+            }
+          }
+          if (c == cy && tid == ty) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + jy * 16), iy);
+          if (kStream || kMode == 1) {  // re-read from L2 in pass 2 (or no pass 2): free it now
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
           }
         }
-        if (c == cy && tid == ty) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + jy * 16), iy);
-        if (kStream) {  // this chunk is re-read from L2 in pass 2: free it now
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+
+        // ---- one partial per warp; the C * 16 partials meet through xbar[b]
+        float m = st.m, s = 0.f, t = 0.f;
+  #pragma unroll
+        for (int q = 0; q < kVecsPerThread; ++q) {
+          s += st.s[q].x + st.s[q].y;
+          t += st.t[q].x + st.t[q].y;
         }
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+          const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
+          merge_stats(m, s, t, m2, s2, t2);
+          zy = max_nan(zy, __shfl_xor_sync(0xffffffffu, zy, o));
+        }
+        const uint32_t b = vrow & 1;
+        if (csize == 1) {  // one CTA per row: CTA-scope publish and wait
+          if (lane == 0) {
+            sm.xpart[b][warp] = make_float4(m, s, t, zy);
+            mbar_arrive(smem_addr(&sm.xbar[b]));
+          }
+          wait_bounded<false>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
+        } else {  // cluster: every rank gets every warp's partial through DSMEM
+          if (lane == 0) {
+            const float4 P = make_float4(m, s, t, zy);
+            const uint32_t xa = smem_addr(&sm.xpart[b][rank * kConsumerWarps + warp]);
+            const uint32_t ba = smem_addr(&sm.xbar[b]);
+            for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
+            for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
+          }
+          wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
+        }
+        for (int p = lane; p < n_parts; p += 32) {
+          const float4 P = sm.xpart[b][p];
+          merge_stats(M, S, Tt, P.x, P.y, P.z);
+          zyr = max_nan(zyr, P.w);
+        }
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+          const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
+          merge_stats(M, S, Tt, m2, s2, t2);
+          zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
+        }
+        // every lane of every warp uses lane 0's bits
+        M = __shfl_sync(0xffffffffu, M, 0);
+        S = __shfl_sync(0xffffffffu, S, 0);
+        Tt = __shfl_sync(0xffffffffu, Tt, 0);
+        zyr = __shfl_sync(0xffffffffu, zyr, 0);
+      } else {
+        // ---- the gathered shard partials stand in for pass 1
+        if (!kStream) {  // the row's chunks stay in the ring for pass 2
+          for (int c = 0; c < nchunks; ++c) {
+            const uint32_t k = it++;
+            wait_bounded<false>(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1, abort_flag);
+          }
+        }
+        for (int k = lane; k < a.n_shards; k += 32) {  // shard order, then a fixed shuffle tree
+          const float4 P = __ldg(&a.shard_partials[static_cast<long long>(k) * a.R + row]);
+          merge_stats(M, S, Tt, P.x, P.y, P.z);
+          zyr = max_nan(zyr, P.w);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+          const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
+          merge_stats(M, S, Tt, m2, s2, t2);
+          zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
+        }
+        M = __shfl_sync(0xffffffffu, M, 0);
+        S = __shfl_sync(0xffffffffu, S, 0);
+        Tt = __shfl_sync(0xffffffffu, Tt, 0);
+        zyr = __shfl_sync(0xffffffffu, zyr, 0);
+      }
+      if constexpr (kMode == 1) {  // this shard's statistics of the row, for the exchange
+        if (rank == 0 && tid == 0) a.partials_out[row] = make_float4(M, S, Tt, zyr);
+        ++vrow;
+        continue;
       }
 
-      // ---- one partial per warp; the C * 16 partials meet through xbar[b]
-      float m = st.m, s = 0.f, t = 0.f;
-#pragma unroll
-      for (int q = 0; q < kVecsPerThread; ++q) {
-        s += st.s[q].x + st.s[q].y;
-        t += st.t[q].x + st.t[q].y;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
-        merge_stats(m, s, t, m2, s2, t2);
-        zy = max_nan(zy, __shfl_xor_sync(0xffffffffu, zy, o));
-      }
-      const uint32_t b = vrow & 1;
-      if (csize == 1) {  // one CTA per row: CTA-scope publish and wait
-        if (lane == 0) {
-          sm.xpart[b][warp] = make_float4(m, s, t, zy);
-          mbar_arrive(smem_addr(&sm.xbar[b]));
-        }
-        wait_bounded<false>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
-      } else {  // cluster: every rank gets every warp's partial through DSMEM
-        if (lane == 0) {
-          const float4 P = make_float4(m, s, t, zy);
-          const uint32_t xa = smem_addr(&sm.xpart[b][rank * kConsumerWarps + warp]);
-          const uint32_t ba = smem_addr(&sm.xbar[b]);
-          for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
-          for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
-        }
-        wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
-      }
-      float M = -INFINITY, S = 0.f, Tt = 0.f, zyr = -INFINITY;
-      for (int p = lane; p < n_parts; p += 32) {
-        const float4 P = sm.xpart[b][p];
-        merge_stats(M, S, Tt, P.x, P.y, P.z);
-        zyr = max_nan(zyr, P.w);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-        const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
-        merge_stats(M, S, Tt, m2, s2, t2);
-        zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
-      }
-      // every lane of every warp uses lane 0's bits
-      M = __shfl_sync(0xffffffffu, M, 0);
-      S = __shfl_sync(0xffffffffu, S, 0);
-      Tt = __shfl_sync(0xffffffffu, Tt, 0);
-      zyr = __shfl_sync(0xffffffffu, zyr, 0);
-
-      const bool y_ok = (y >= 0) && (y < a.V);
+      const bool y_ok = (y >= 0) && (y < a.v_total);
       const float zv = y_ok ? zyr : __int_as_float(0x7fc00000);
       const float log2S = log2f(S);
       const float lse = fmaf(log2S, kLn2, M);
@@ -995,36 +1037,44 @@ bool choose_layout(int es, long long V, Plan* p) {
   return false;
 }
 
-template <int DT, bool S>
-void* kernel_ptr() {
-  return reinterpret_cast<void*>(&policy_loss_kernel<DT, S>);
+template <int DT, int M>
+void* kernel_ptr(bool stream) {
+  return stream ? reinterpret_cast<void*>(&policy_loss_kernel<DT, true, M>)
+                : reinterpret_cast<void*>(&policy_loss_kernel<DT, false, M>);
 }
 
-void* kernel_for(rl_dtype dt, bool stream) {
+template <int M>
+void* kernel_for_mode(rl_dtype dt, bool stream) {
   switch (dt) {
-    case RL_F32: return stream ? kernel_ptr<RL_F32, true>() : kernel_ptr<RL_F32, false>();
-    case RL_BF16: return stream ? kernel_ptr<RL_BF16, true>() : kernel_ptr<RL_BF16, false>();
-    case RL_F16: return stream ? kernel_ptr<RL_F16, true>() : kernel_ptr<RL_F16, false>();
+    case RL_F32: return kernel_ptr<RL_F32, M>(stream);
+    case RL_BF16: return kernel_ptr<RL_BF16, M>(stream);
+    case RL_F16: return kernel_ptr<RL_F16, M>(stream);
   }
   return nullptr;
+}
+
+void* kernel_for(rl_dtype dt, bool stream, int mode) {
+  return mode == 1 ? kernel_for_mode<1>(dt, stream)
+       : mode == 2 ? kernel_for_mode<2>(dt, stream)
+                   : kernel_for_mode<0>(dt, stream);
 }
 
 // Per (device, kernel, cluster size): attributes set once and the number of
 // co-resident clusters.
 std::mutex g_occ_mu;
-std::map<std::tuple<int, int, int, int>, int> g_occ;
+std::map<std::tuple<int, int, int, int, int>, int> g_occ;
 
-rl_status max_clusters(rl_dtype dt, bool stream, int cluster, int* out) {
+rl_status max_clusters(rl_dtype dt, bool stream, int cluster, int mode, int* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
-  const auto key = std::make_tuple(dev, static_cast<int>(dt), static_cast<int>(stream), cluster);
+  const auto key = std::make_tuple(dev, static_cast<int>(dt), static_cast<int>(stream), cluster, mode);
   std::lock_guard<std::mutex> lock(g_occ_mu);
   auto found = g_occ.find(key);
   if (found != g_occ.end()) {
     *out = found->second;
     return RL_OK;
   }
-  void* fn = kernel_for(dt, stream);
+  void* fn = kernel_for(dt, stream, mode);
   const int smem = static_cast<int>(sizeof(LossSmem));
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return RL_ERR_CUDA;
@@ -1046,13 +1096,13 @@ rl_status max_clusters(rl_dtype dt, bool stream, int cluster, int* out) {
   return RL_OK;
 }
 
-rl_status plan(rl_dtype dt, long long V, long long R, Plan* p) {
+rl_status plan(rl_dtype dt, long long V, long long R, Plan* p, int mode = 0) {
   const int es = elem_bytes(dt);
   if (es == 0) return RL_ERR_DTYPE;
   if (V < 1 || R < 0) return RL_ERR_SHAPE;
   if (!choose_layout(es, V, p)) return RL_ERR_SHAPE;
   int occ = 0;
-  const rl_status st = max_clusters(dt, p->stream, p->cluster, &occ);
+  const rl_status st = max_clusters(dt, p->stream, p->cluster, mode, &occ);
   if (st != RL_OK) return st;
   long long n = occ;
   if (n > R) n = R > 0 ? R : 1;
@@ -1118,6 +1168,20 @@ extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, lo
   return RL_OK;
 }
 
+namespace {
+template <int DT, bool S>
+cudaError_t launch_one(cudaLaunchConfig_t* cfg, int mode, const LossArgs& args) {
+  return mode == 1 ? cudaLaunchKernelEx(cfg, policy_loss_kernel<DT, S, 1>, args)
+       : mode == 2 ? cudaLaunchKernelEx(cfg, policy_loss_kernel<DT, S, 2>, args)
+                   : cudaLaunchKernelEx(cfg, policy_loss_kernel<DT, S, 0>, args);
+}
+
+template <int DT>
+cudaError_t launch_mode(cudaLaunchConfig_t* cfg, bool stream, int mode, const LossArgs& args) {
+  return stream ? launch_one<DT, true>(cfg, mode, args) : launch_one<DT, false>(cfg, mode, args);
+}
+}  // namespace
+
 extern "C" void rl_policy_loss_desc_init(rl_policy_loss_desc* d) {
   if (!d) return;
   std::memset(d, 0, sizeof(*d));
@@ -1161,6 +1225,15 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   }
   if (d->agg == RL_AGG_TOKEN_SUM_NORM && !(d->agg_norm > 0.0 && std::isfinite(d->agg_norm)))
     return RL_ERR_ARG;
+  // vocabulary shards
+  const int mode = d->partials_out ? 1 : d->shard_partials ? 2 : 0;
+  const long long v_total = d->vocab_total > 0 ? d->vocab_total : V;
+  if (d->partials_out && d->shard_partials) return RL_ERR_ARG;
+  if (d->vocab_offset < 0 || d->vocab_total < 0 || d->vocab_offset + V > v_total) return RL_ERR_SHAPE;
+  if (mode == 2 && d->n_shards < 1) return RL_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(d->partials_out) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(d->shard_partials) & 15) != 0)
+    return RL_ERR_ALIGN;
   const long long row_bytes = ld * es;
   if ((row_bytes & 15) != 0) return RL_ERR_ALIGN;
   if ((reinterpret_cast<uintptr_t>(d->logits) & 15) != 0) return RL_ERR_ALIGN;
@@ -1174,7 +1247,7 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   }
 
   Plan pl;
-  const rl_status st = plan(d->dtype, V, R, &pl);
+  const rl_status st = plan(d->dtype, V, R, &pl, mode);
   if (st != RL_OK) return st;
 
   LossArgs args;
@@ -1208,6 +1281,16 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   args.agg = d->agg;
   args.agg_w = d->agg == RL_AGG_TOKEN_SUM_NORM ? 1.0 / d->agg_norm : 0.0;
   args.global_counts = d->global_counts;
+  args.v_offset = d->vocab_offset;
+  args.v_total = v_total;
+  args.partials_out = reinterpret_cast<float4*>(d->partials_out);
+  args.shard_partials = reinterpret_cast<const float4*>(d->shard_partials);
+  args.n_shards = mode == 2 ? d->n_shards : 0;
+  if (mode == 1) {  // statistics only
+    args.dlogits = nullptr;
+    args.logp_out = nullptr;
+    args.entropy_out = nullptr;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -1225,18 +1308,9 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   cfg.numAttrs = 2;
   cudaError_t e = cudaErrorInvalidValue;
   switch (d->dtype) {
-    case RL_F32:
-      e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32, true>, args)
-                    : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F32, false>, args);
-      break;
-    case RL_BF16:
-      e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_BF16, true>, args)
-                    : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_BF16, false>, args);
-      break;
-    case RL_F16:
-      e = pl.stream ? cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16, true>, args)
-                    : cudaLaunchKernelEx(&cfg, policy_loss_kernel<RL_F16, false>, args);
-      break;
+    case RL_F32: e = launch_mode<RL_F32>(&cfg, pl.stream, mode, args); break;
+    case RL_BF16: e = launch_mode<RL_BF16>(&cfg, pl.stream, mode, args); break;
+    case RL_F16: e = launch_mode<RL_F16>(&cfg, pl.stream, mode, args); break;
   }
   return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }

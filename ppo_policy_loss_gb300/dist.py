@@ -44,3 +44,36 @@ def policy_loss_data_parallel(logits, ids, mask, adv, B, T, group=None, count_fn
     out["global_counts"] = counts
     out["loss"] = share
     return out
+
+
+def _default_partials(logits, ids, mask, adv, B, T, vocab_offset, vocab_total, **kw):
+    R = B * T
+    part = torch.empty((R, 4), dtype=torch.float32, device=logits.device)
+    torch_api.policy_loss(logits, ids, mask, adv, B, T, vocab_offset=vocab_offset,
+                          vocab_total=vocab_total, partials_out=part, **kw)
+    return part
+
+
+def _default_merge(logits, ids, mask, adv, B, T, vocab_offset, vocab_total, gathered, **kw):
+    return torch_api.policy_loss(logits, ids, mask, adv, B, T, vocab_offset=vocab_offset,
+                                 vocab_total=vocab_total, shard_partials=gathered, **kw)
+
+
+def policy_loss_vocab_parallel(logits, ids, mask, adv, B, T, vocab_offset, vocab_total,
+                               group=None, partials_fn=None, merge_fn=None, **kw) -> dict:
+    """Fused loss with the vocabulary split over the ranks of ``group`` (each
+    holds the logits columns [vocab_offset, vocab_offset + V) of every row; ids
+    are global).  One launch per rank writes each row's shard statistics
+    (max, sum of exponentials, their weighted sum, the sampled logit or -inf),
+    an all-gather assembles them in rank order (B*T*16 bytes per rank), and a
+    second launch merges them and writes the loss, logp, entropy and this
+    rank's gradient columns.  Every rank reports the same loss."""
+    partials_fn = partials_fn or _default_partials
+    merge_fn = merge_fn or _default_merge
+    part = partials_fn(logits, ids, mask, adv, B, T, vocab_offset, vocab_total, **kw)
+    world = dist.get_world_size(group)
+    flat = torch.empty((world * part.shape[0],) + tuple(part.shape[1:]), dtype=part.dtype,
+                       device=part.device)
+    dist.all_gather_into_tensor(flat, part.contiguous(), group=group)
+    gathered = flat.view((world,) + tuple(part.shape))
+    return merge_fn(logits, ids, mask, adv, B, T, vocab_offset, vocab_total, gathered, **kw)

@@ -56,7 +56,9 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
                 dlogits="new", logp_out="new", entropy_out="new", workspace=None, stats=None,
                 stream=None, eps_high: float | None = None, agg: str = "token_mean",
                 agg_norm: float = 1.0, group_size: int | None = None, ddof: int = 1,
-                std_eps: float = 1e-4, global_counts: torch.Tensor | None = None) -> dict:
+                std_eps: float = 1e-4, global_counts: torch.Tensor | None = None,
+                vocab_offset: int = 0, vocab_total: int = 0, partials_out=None,
+                shard_partials=None) -> dict:
     """Run the fused loss on [B*T, ld] logits (rl_policy_loss_fwd_bwd_ex).
 
     ``dlogits`` / ``logp_out`` / ``entropy_out``: "new" allocates, None skips,
@@ -67,13 +69,28 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
     (token_mean, seq_mean_token_mean, seq_mean_token_sum, token_sum_norm).
     Returns the output tensors and the (device) stats record; call
     ``read_stats`` for the scalars.
+
+    Vocabulary shards: ``logits`` holds columns [vocab_offset, vocab_offset + V)
+    of a ``vocab_total``-column vocabulary.  With ``partials_out`` (float32
+    [B*T, 4]) the launch only writes each row's shard statistics; with
+    ``shard_partials`` (float32 [n_shards, B*T, 4], every shard's partials in
+    shard order) it merges them and computes the loss and this shard's
+    gradient columns.
     """
     dev = logits.device
     R = B * T
+    if partials_out is not None:  # this launch writes the shard partials only
+        dlogits = logp_out = entropy_out = None
     ld = logits.stride(0) if logits.dim() == 2 and R > 0 else logits.shape[-1]
     V = logits.shape[-1] if V is None else V
-    if isinstance(dlogits, str):
-        dlogits = torch.empty_like(logits)
+    if isinstance(dlogits, str):  # same row stride as the logits (the C call takes one ld)
+        if logits.dim() == 2 and logits.stride(0) != logits.shape[1]:
+            dlogits = torch.empty((logits.shape[0], ld), dtype=logits.dtype, device=dev)
+            dlogits = dlogits[:, :logits.shape[1]]
+        else:
+            dlogits = torch.empty_like(logits)
+    elif dlogits is not None and R > 0 and dlogits.stride(0) != ld:
+        raise ValueError(f"dlogits row stride {dlogits.stride(0)} != logits row stride {ld}")
     if isinstance(logp_out, str):
         logp_out = torch.empty(R, dtype=torch.float32, device=dev)
     if isinstance(entropy_out, str):
@@ -97,6 +114,9 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
     d.dlogits, d.logp_out, d.entropy_out = p(dlogits), p(logp_out), p(entropy_out)
     d.stats_dev, d.workspace, d.workspace_bytes = p(stats), p(workspace), workspace.numel()
     d.global_counts = p(global_counts)
+    d.vocab_offset, d.vocab_total = vocab_offset, vocab_total
+    d.partials_out, d.shard_partials = p(partials_out), p(shard_partials)
+    d.n_shards = shard_partials.shape[0] if shard_partials is not None else 0
     rl_policy_loss_fwd_bwd_ex(d, stream)
     return dict(dlogits=dlogits, logp=logp_out, entropy=entropy_out, stats=stats,
                 workspace=workspace)

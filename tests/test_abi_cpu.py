@@ -168,6 +168,12 @@ def test_desc_defaults(lib):
     (dict(adv_layout=rl.RL_ADV_GROUP_REWARDS, group_size=2, std_eps=-1.0), rl.RL_ERR_ARG),
     (dict(eps_high=float("inf")), rl.RL_ERR_ARG),
     (dict(stats_dev=None), rl.RL_ERR_NULL),
+    # vocabulary shards
+    (dict(partials_out=FAKE + 0x700000, shard_partials=FAKE + 0x800000, n_shards=2), rl.RL_ERR_ARG),
+    (dict(shard_partials=FAKE + 0x800000, n_shards=0), rl.RL_ERR_ARG),
+    (dict(vocab_offset=8, vocab_total=1024), rl.RL_ERR_SHAPE),      # shard runs past the vocabulary
+    (dict(vocab_offset=-8, vocab_total=4096), rl.RL_ERR_SHAPE),
+    (dict(partials_out=FAKE + 0x700008), rl.RL_ERR_ALIGN),
 ])
 def test_desc_argument_errors(lib, over, status):
     assert lib.rl_policy_loss_fwd_bwd_ex(ctypes.byref(_desc(**over)), None) == status

@@ -79,3 +79,45 @@ def test_two_ranks_reproduce_the_single_process_loss(agg):
     for rank, loss, counts in res:
         assert counts == [int(mask.sum()), 5]
         assert abs(loss - whole["loss"]) < 1e-12, (rank, loss, whole["loss"])
+
+
+def _vp_rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    R = 5
+
+    def partials_fn(logits, ids, mask, adv, b, t, off, total, **kw):
+        # stand-in for the first launch: each row's entry tags the shard and the row
+        return torch.tensor([[float(rank), float(r), float(off), float(total)] for r in range(R)])
+
+    def merge_fn(logits, ids, mask, adv, b, t, off, total, gathered, **kw):
+        return {"gathered": gathered.clone()}
+
+    off = [0, 7, 11][rank]
+    out = rldist.policy_loss_vocab_parallel(None, None, None, None, 1, R, off, 13,
+                                            partials_fn=partials_fn, merge_fn=merge_fn)
+    q.put((rank, out["gathered"].tolist()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_vocab_parallel_exchange_orders_the_shards():
+    """Three gloo ranks: the all-gather between the two launches hands every
+    rank every shard's partials, in rank (shard) order, row by row."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _port()
+    procs = [ctx.Process(target=_vp_rank_main, args=(r, 3, port, q)) for r in range(3)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, g in res:
+        assert len(g) == 3
+        for k, shard in enumerate(g):
+            assert [row[0] for row in shard] == [float(k)] * 5
+            assert [row[1] for row in shard] == [0.0, 1.0, 2.0, 3.0, 4.0]
+            assert shard[0][2] == [0, 7, 11][k] and shard[0][3] == 13

@@ -100,6 +100,7 @@ struct LossSmem {
   long long wcount[kConsumerWarps];
   long long wseq[kConsumerWarps];
   double wred[kConsumerWarps][5];
+  double acc[5];  // this CTA's J, pg, kl, H, clipped sums (kept by thread 0 of rank 0)
   int abort;
   int is_last;
   long long pace;  // row the consumers are on (the zero warp keeps within a few rows of it)
@@ -149,6 +150,7 @@ struct Elem;
 template <>
 struct Elem<RL_F32> {
   static constexpr int kBytes = 4, kVec = 4;
+  static constexpr uint32_t kFloorWord = 0xF149F2CAu;  // kFloor
   __device__ static void clamp(uint4& w) {
     w.x = __float_as_uint(max_nan(__uint_as_float(w.x), kFloor));
     w.y = __float_as_uint(max_nan(__uint_as_float(w.y), kFloor));
@@ -188,6 +190,7 @@ template <>
 struct Elem<RL_BF16> {
   static constexpr int kBytes = 2, kVec = 8;
   static constexpr uint32_t kFloor2 = 0xF149F149u;  // (-9.98e29, -9.98e29) in bf16
+  static constexpr uint32_t kFloorWord = kFloor2;
   __device__ static void clamp(uint4& w) {
     w.x = max_nan_bf16x2(w.x, kFloor2);
     w.y = max_nan_bf16x2(w.y, kFloor2);
@@ -224,6 +227,7 @@ template <>
 struct Elem<RL_F16> {
   static constexpr int kBytes = 2, kVec = 8;
   static constexpr uint32_t kFloor2 = 0xFBFFFBFFu;  // (-65504, -65504) in fp16
+  static constexpr uint32_t kFloorWord = kFloor2;
   __device__ static void clamp(uint4& w) {
     w.x = max_nan_f16x2(w.x, kFloor2);
     w.y = max_nan_f16x2(w.y, kFloor2);
@@ -343,47 +347,60 @@ __device__ __forceinline__ void accumulate_chunk(uint32_t buf, ThreadStats& a) {
   }
 }
 
-// Pass-1 update with one full 16-byte vector into chain q (whole warp).
+// Elements nv .. kVec-1 of a vector set to the format's floor: past the end
+// of a row they can never raise the running maximum.
 template <class E>
-__device__ __forceinline__ void accumulate_full(uint4 w, ThreadStats& a, int q) {
-  E::clamp(w);
-  raise_max(E::vmax(w), a);
-  float z[E::kVec];
-  E::unpack(w, z);
-  const float2 L2 = make_float2(kLog2e, kLog2e);
-  const float2 nmL = make_float2(a.nmL, a.nmL);
-  float2 s = a.s[q], t = a.t[q];
+__device__ __forceinline__ void fill_floor(uint4& w, int nv) {
+  uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  constexpr int kPerWord = E::kVec / 4;  // elements per 32-bit word: 1 or 2
 #pragma unroll
-  for (int i = 0; i < E::kVec; i += 2) {
-    const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, nmL);
-    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-    s = __fadd2_rn(s, e);
-    t = __ffma2_rn(e, x, t);
+  for (int k = 0; k < 4; ++k) {
+    if (kPerWord * k >= nv)
+      u[k] = E::kFloorWord;
+    else if (kPerWord == 2 && 2 * k + 1 >= nv)
+      u[k] = (u[k] & 0xffffu) | (E::kFloorWord & 0xffff0000u);
   }
-  a.s[q] = s;
-  a.t[q] = t;
+  w = make_uint4(u[0], u[1], u[2], u[3]);
 }
 
-// Pass-1 update with the first nv (0..kVec) elements of a vector (row tail;
-// whole warp, lanes past the end pass nv = 0).
+// Pass-1 update with a row's last, partly filled chunk (whole warp).  Element
+// e0 = first + q * kConsumerThreads * kVec starts this thread's vector q; the
+// row ends at element nelem.  The same packed chains as a full chunk, with
+// the exponentials of elements past the end set to 0 (so they add exactly 0
+// to s and t), and vector positions that no lane of the warp holds skipped.
 template <class E>
-__device__ __forceinline__ void accumulate_tail(uint4 w, int nv, ThreadStats& a, int q) {
-  E::clamp(w);
-  float z[E::kVec];
-  E::unpack(w, z);
+__device__ __forceinline__ void accumulate_chunk_tail(uint32_t buf, int first, int nelem,
+                                                      ThreadStats& a) {
+  const int rem = nelem - first;  // elements from this thread's vector 0 to the row's end
+  uint4 w[kVecsPerThread];
   float vm = kFloor;
 #pragma unroll
-  for (int i = 0; i < E::kVec; ++i)
-    if (i < nv) vm = max_nan(vm, z[i]);
+  for (int q = 0; q < kVecsPerThread; ++q) {
+    const int nv = max(0, min(E::kVec, rem - q * kConsumerThreads * E::kVec));
+    w[q] = nv > 0 ? ld_shared_v4(buf + q * kConsumerThreads * 16) : make_uint4(0u, 0u, 0u, 0u);
+    if (nv < E::kVec) fill_floor<E>(w[q], nv);
+    E::clamp(w[q]);
+    vm = max_nan(vm, E::vmax(w[q]));
+  }
   raise_max(vm, a);
+  const float2 L2 = make_float2(kLog2e, kLog2e);
+  const float2 nmL = make_float2(a.nmL, a.nmL);
 #pragma unroll
-  for (int i = 0; i < E::kVec; ++i) {
-    if (i < nv) {
-      const float x = fmaf(z[i], kLog2e, a.nmL);
-      const float e = ex2_approx(x);
-      a.s[q].x += e;
-      a.t[q].x = fmaf(e, x, a.t[q].x);
+  for (int q = 0; q < kVecsPerThread; ++q) {
+    const int nv = max(0, min(E::kVec, rem - q * kConsumerThreads * E::kVec));
+    if (!__any_sync(0xffffffffu, nv > 0)) continue;  // warp-uniform
+    float z[E::kVec];
+    E::unpack(w[q], z);
+    float2 s = a.s[q], t = a.t[q];
+#pragma unroll
+    for (int i = 0; i < E::kVec; i += 2) {
+      const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, nmL);
+      const float2 e = make_float2(i < nv ? ex2_approx(x.x) : 0.f, i + 1 < nv ? ex2_approx(x.y) : 0.f);
+      s = __fadd2_rn(s, e);
+      t = __ffma2_rn(e, x, t);
     }
+    a.s[q] = s;
+    a.t[q] = t;
   }
 }
 
@@ -474,6 +491,31 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   return v;
 }
 
+// A CTA's rows are first, first + stride, first + 2 stride, ... (below R).
+// A warp walks the ones whose mask byte is nonzero (kValid) or zero
+// (!kValid) a window of 32 at a time: lane k reads the byte of row
+// base + k * stride and one ballot gives the window's rows, so a run of
+// skipped rows costs one load latency per 32 rows instead of one per row.
+// next() returns the next such row, or R after the last; whole warp.
+template <bool kValid>
+struct RowWalk {
+  long long base;
+  uint32_t bits;
+  __device__ RowWalk(long long first, long long stride) : base(first - 32 * stride), bits(0u) {}
+  __device__ __forceinline__ long long next(const unsigned char* mask, long long stride, long long R,
+                                            int lane) {
+    while (bits == 0u) {
+      if (base >= R) return R;
+      base += 32 * stride;
+      const long long r = base + lane * stride;
+      bits = __ballot_sync(0xffffffffu, r < R && ((mask[r] != 0) == kValid));
+    }
+    const int k = __ffs(bits) - 1;
+    bits &= bits - 1u;
+    return base + k * stride;
+  }
+};
+
 // Nonzero bytes of mask[begin, begin + n), counted by one warp (every lane
 // gets the count).
 __device__ __forceinline__ int warp_count_mask(const unsigned char* m, long long n, int lane) {
@@ -545,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     sm.abort = 0;
     sm.is_last = 0;
     sm.pace = -1;
+    for (int k = 0; k < 5; ++k) sm.acc[k] = 0.0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -562,16 +605,14 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol_last = RL_STREAM_KEEP_L2 ? policy_evict_last() : policy_evict_normal();
-      const uint64_t pol_first = policy_evict_first();
-      uint32_t it = 0;
-      bool stop = false;
-      bool valid_next = cid < a.R ? a.mask[cid] != 0 : false;
-      for (long long row = cid; row < a.R && !stop; row += ncl) {
-        const bool valid = valid_next;
-        valid_next = row + ncl < a.R ? a.mask[row + ncl] != 0 : false;  // one row ahead
-        if (!valid || nchunks == 0) continue;
+    // The warp walks the valid rows; lane 0 issues their copies.
+    const uint64_t pol_last = RL_STREAM_KEEP_L2 ? policy_evict_last() : policy_evict_normal();
+    const uint64_t pol_first = policy_evict_first();
+    uint32_t it = 0;
+    bool stop = nchunks == 0;
+    RowWalk<true> walk(cid, ncl);
+    for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R && !stop; row = walk.next(a.mask, ncl, a.R, lane)) {
+      if (lane == 0) {
         const unsigned char* src = a.logits + row * a.row_bytes + lo * E::kBytes;
         constexpr int kPasses = (kStream && kMode == 0) ? 2 : 1;
         for (int pass = 0; pass < kPasses && !stop; ++pass) {
@@ -596,10 +637,11 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
           }
         }
       }
-      if (stop) {  // let every copy already issued land before this CTA can exit
-        for (uint32_t k = it > kSlots ? it - kSlots : 0; k < it; ++k)
-          drain_wait(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1);
-      }
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+    }
+    if (lane == 0 && stop && nchunks > 0) {  // let every copy already issued land before this CTA can exit
+      for (uint32_t k = it > kSlots ? it - kSlots : 0; k < it; ++k)
+        drain_wait(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1);
     }
   } else if (warp == kConsumerWarps + 1) {
     // ---------------------------------------------------------------- zero warp
@@ -609,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     // kZeroLead rows of the consumers, so the writes stay spread over the
     // launch instead of arriving as one burst at its start.
     const volatile long long* pace = &sm.pace;
-    for (long long row = cid; row < a.R; row += ncl) {
-      if (a.mask[row] != 0) continue;
+    RowWalk<false> walk(cid, ncl);
+    for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R; row = walk.next(a.mask, ncl, a.R, lane)) {
       if (*pace < row - kZeroLead * static_cast<long long>(ncl)) {  // bounded wait, then go on
         const uint64_t t0 = global_ns();
         while (*pace < row - kZeroLead * static_cast<long long>(ncl) && global_ns() - t0 < kWaitLimitNs)
@@ -624,7 +666,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    RowScalars cur = load_row(a, cid);  // in flight while the mask is counted
+    RowWalk<true> walk(cid, ncl);  // the valid rows of this CTA
+    long long nrow = walk.next(a.mask, ncl, a.R, lane);
+    RowScalars cur = load_row(a, nrow);  // in flight while the mask is counted
 
     // N = number of valid tokens; every CTA counts the whole mask.
     long long cnt = 0;
@@ -670,17 +714,16 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     int cache_L = 0;
     float cache_A = 0.f;
 
-    double acc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // J, pg, kl, H, clipped (rank 0, thread 0)
     unsigned int err = 0;
     uint32_t it = 0, vrow = 0;
     bool aborted = false;
 
-    for (long long row = cid; row < a.R; row += ncl) {
+    for (long long row = nrow; row < a.R; row = nrow) {  // masked rows: the zero warp
       if (tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = row;
+      nrow = walk.next(a.mask, ncl, a.R, lane);
       const RowScalars rs = cur;
-      cur = load_row(a, row + ncl);  // next row's scalars, in flight during this row
+      cur = load_row(a, nrow);  // next row's scalars, in flight during this row
       unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes + lo * E::kBytes : nullptr;
-      if (!rs.valid) continue;  // the zero warp writes masked rows
       if (*abort_flag) {
         aborted = true;
         break;
@@ -727,17 +770,10 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
           wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
           const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
           const int c0 = c * kChunkElems;
-          if (c0 + kChunkElems <= nelem) {
+          if (c0 + kChunkElems <= nelem)
             accumulate_chunk<E>(buf, st);
-          } else {
-  #pragma unroll
-            for (int q = 0; q < kVecsPerThread; ++q) {
-              const int e0 = c0 + (tid + q * kConsumerThreads) * kVec;
-              const int nv = max(0, min(kVec, nelem - e0));
-              const uint4 w = nv > 0 ? ld_shared_v4(buf + q * kConsumerThreads * 16) : make_uint4(0u, 0u, 0u, 0u);
-              accumulate_tail<E>(w, nv, st, q);
-            }
-          }
+          else
+            accumulate_chunk_tail<E>(buf, c0 + tid * kVec, nelem, st);
           if (c == cy && tid == ty) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + jy * 16), iy);
           if (kStream || kMode == 1) {  // re-read from L2 in pass 2 (or no pass 2): free it now
             __syncwarp();
@@ -854,11 +890,11 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         g = logp;
       }
       if (rank == 0 && tid == 0) {
-        acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(J) : w_row * J;
-        acc[1] += pg;
-        acc[2] += kl;
-        acc[3] += H;
-        acc[4] += clipped ? 1.0 : 0.0;
+        sm.acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(J) : w_row * J;
+        sm.acc[1] += pg;
+        sm.acc[2] += kl;
+        sm.acc[3] += H;
+        sm.acc[4] += clipped ? 1.0 : 0.0;
         if (!y_ok) err |= RL_DEVERR_ID_RANGE;
         if (a.logp_out) a.logp_out[row] = logp;
         if (a.entropy_out) a.entropy_out[row] = H;
@@ -949,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     // ---- per-CTA partial, then the last CTA reduces all partials in CTA order
     if (tid == 0) {
       WsPartial& P = a.partials[blockIdx.x];
-      for (int k = 0; k < 5; ++k) P.v[k] = acc[k];
+      for (int k = 0; k < 5; ++k) P.v[k] = sm.acc[k];
       if (aborted || *abort_flag) err |= RL_DEVERR_TIMEOUT;
       if (err) atomicOr(&a.ws->status, err);
       __threadfence();

@@ -27,8 +27,11 @@
 //     is kept for comparison builds; it costs a cluster-wide exchange per row
 //     and loses to streaming on GB300.
 //   * A zero warp writes the all-zero gradient of masked rows (their logits
-//     are never read), paced to within a row of the consumers, so masked
-//     rows' stores overlap the valid rows' arithmetic.
+//     are never read) as bulk copies of a zeroed shared-memory block, kept
+//     within eight rows of the consumers, so masked rows' stores overlap the
+//     valid rows' arithmetic without taking the consumers' store path.
+//   * Each row loop reads the mask bytes of 32 of its rows with one ballot
+//     and jumps to the next row it handles.
 //   * Sixteen consumer warps.  Pass 1: per-thread online (max, sum 2^x,
 //     sum 2^x * x) in packed fp32x2 with independent accumulator chains.
 //     Each warp shuffle-merges its lanes and publishes one partial; the
@@ -89,10 +92,12 @@ static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly ov
 static_assert(kConsumerWarps * kMaxCluster <= 128, "partials of one row fit 4 per lane");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kConsumerBarrier = 1;  // named barrier id (0 is __syncthreads)
-constexpr long long kZeroLead = 1;        // rows the zero warp may run ahead of the consumers
+constexpr int kZeroBytes = 16384;         // zero block the masked rows are copied from
+constexpr long long kZeroLead = 8;        // rows the zero warp may run ahead of the consumers
 
 struct LossSmem {
   alignas(128) unsigned char ring[kSlots][kChunkBytes];
+  alignas(128) unsigned char zeros[kZeroBytes];  // source of the masked rows' bulk stores
   unsigned long long full[kSlots];
   unsigned long long empty[kSlots];
   unsigned long long xbar[2];
@@ -436,14 +441,6 @@ __device__ __forceinline__ void grad_vec(uint4 w, float cL, float a0, float a1, 
   }
 }
 
-// All-zero gradient slice of a masked row, written by the 32 lanes of one warp.
-template <class E>
-__device__ __forceinline__ void zero_slice(unsigned char* drow, long long nelem, int lane) {
-  const long long nvec = nelem / E::kVec;
-  for (long long j = lane; j < nvec; j += 32) st_global_cs_v4(drow + j * 16, make_uint4(0u, 0u, 0u, 0u));
-  for (long long e = nvec * E::kVec + lane; e < nelem; e += 32) E::store1(drow + e * E::kBytes, 0.f);
-}
-
 // Wait for a bulk copy to land regardless of the abort flag (used to drain).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -650,6 +647,15 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
     // rows' stores overlap the valid rows' arithmetic.  It keeps within
     // kZeroLead rows of the consumers, so the writes stay spread over the
     // launch instead of arriving as one burst at its start.
+    // The writes are bulk copies of a zeroed shared-memory block: they go
+    // through the copy engine, not the load/store path that the consumers'
+    // gradient stores keep busy.
+    for (int i = lane; i < kZeroBytes / 16; i += 32)
+      reinterpret_cast<uint4*>(sm.zeros)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_shared();
+    __syncwarp();
+    const uint64_t pol = policy_evict_first();
+    const long long nb16 = static_cast<long long>(nelem) * E::kBytes & ~15LL;  // bulk part of a slice
     const volatile long long* pace = &sm.pace;
     RowWalk<false> walk(cid, ncl);
     for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R; row = walk.next(a.mask, ncl, a.R, lane)) {
@@ -658,12 +664,22 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         while (*pace < row - kZeroLead * static_cast<long long>(ncl) && global_ns() - t0 < kWaitLimitNs)
           __nanosleep(500);
       }
-      if (a.dlogits) zero_slice<E>(a.dlogits + row * a.row_bytes + lo * E::kBytes, nelem, lane);
+      if (a.dlogits) {
+        unsigned char* d = a.dlogits + row * a.row_bytes + lo * E::kBytes;
+        if (lane == 0) {
+          for (long long off = 0; off < nb16; off += kZeroBytes)
+            bulk_store(d + off, smem_addr(sm.zeros),
+                       static_cast<uint32_t>(min(static_cast<long long>(kZeroBytes), nb16 - off)), pol);
+          bulk_commit();
+        }
+        for (long long e = nb16 / E::kBytes + lane; e < nelem; e += 32) E::store1(d + e * E::kBytes, 0.f);
+      }
       if (rank == 0 && lane == 0) {
         if (a.logp_out) a.logp_out[row] = 0.f;
         if (a.entropy_out) a.entropy_out[row] = 0.f;
       }
     }
+    if (lane == 0) bulk_wait_all();  // the block is read until the last copy is done
   } else {
     // ---------------------------------------------------------------- consumers
     RowWalk<true> walk(cid, ncl);  // the valid rows of this CTA

@@ -17,6 +17,10 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "librlloss.so")
 SOURCES = ["policy_loss.cu", "advantages.cu", "critic.cu", "status.cu", "lmhead.cu"]
+# (object, source, extra flags): policy_loss.cu builds a second time with the
+# short-row configuration of the loss kernel.
+UNITS = [(src.replace(".cu", ".o"), src, []) for src in SOURCES] + [
+    ("policy_loss_short_rows.o", "policy_loss.cu", ["-DRL_SHORT_ROWS"])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I" + INCLUDE]
@@ -54,9 +58,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(OBJ_DIR, exist_ok=True)
     procs, objs = [], []
-    for src in SOURCES:
-        obj = os.path.join(OBJ_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    for name, src, extra in UNITS:
+        obj = os.path.join(OBJ_DIR, name)
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

@@ -60,7 +60,29 @@
 namespace rl {
 namespace {
 
+// The source builds twice.  The default build is the configuration for long
+// rows: 16 consumer warps, one CTA per SM, 32 KB chunks.  With RL_SHORT_ROWS
+// it builds the one for rows of at most kShortRowBytes: 8 consumer warps,
+// two CTAs per SM and 16 KB chunks, so that each SM has two rows in flight
+// and one row's per-row latencies (the exchange, the row's scalar math)
+// overlap the other's streaming.  The C entry points, compiled in the
+// default build only, pick one per call from the row length.
+#define RL_INTERNAL __attribute__((visibility("hidden")))  // shared by the two builds only
+#ifdef RL_SHORT_ROWS
+#define RL_CONSUMER_WARPS 8
+#define RL_MIN_CTAS_PER_SM 2
+#define RL_CHUNK_BYTES 16384
+#define RL_LOSS_KERNEL policy_loss_short_rows_kernel
+#define RL_ROWS_NS rl_short_rows
+#else
+#define RL_LOSS_KERNEL policy_loss_kernel
+#define RL_ROWS_NS rl_long_rows
+#endif
+
 // Tuning knobs (compile-time; the defaults are the shipped configuration).
+#ifndef RL_CHUNK_BYTES
+#define RL_CHUNK_BYTES 32768
+#endif
 #ifndef RL_CONSUMER_WARPS
 #define RL_CONSUMER_WARPS 16
 #endif
@@ -80,7 +102,7 @@ namespace {
 #define RL_STREAM_KEEP_L2 1
 #endif
 
-constexpr int kChunkBytes = 32768;
+constexpr int kChunkBytes = RL_CHUNK_BYTES;
 constexpr int kSlots = RL_RING_SLOTS;
 constexpr int kConsumerWarps = RL_CONSUMER_WARPS;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
@@ -92,7 +114,7 @@ static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly ov
 static_assert(kConsumerWarps * kMaxCluster <= 128, "partials of one row fit 4 per lane");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kConsumerBarrier = 1;  // named barrier id (0 is __syncthreads)
-constexpr int kZeroBytes = 16384;         // zero block the masked rows are copied from
+constexpr int kZeroBytes = kChunkBytes / 2;  // zero block the masked rows are copied from
 constexpr long long kZeroLead = 8;        // rows the zero warp may run ahead of the consumers
 
 struct LossSmem {
@@ -462,20 +484,30 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
 
 // Per-row scalars, loaded one row ahead of their use.
 struct RowScalars {
-  long long y;
+  long long y, b;  // sampled id; sequence of the row
   float A, lpo, rf;
   bool valid;
 };
+
+// row / T: a 32-bit division when both fit (the 64-bit one is a long
+// software sequence, and every consumer thread needs it once per row).
+__device__ __forceinline__ long long seq_of(long long row, long long T) {
+  if (((row | T) >> 32) == 0)
+    return static_cast<long long>(static_cast<uint32_t>(row) / static_cast<uint32_t>(T));
+  return row / T;
+}
 
 __device__ __forceinline__ RowScalars load_row(const LossArgs& a, long long row) {
   RowScalars r;
   r.valid = false;
   r.y = 0;
+  r.b = 0;
   r.A = r.lpo = r.rf = 0.f;
   if (row < a.R) {
     r.valid = a.mask[row] != 0;
     r.y = a.ids[row];
-    if (a.adv_mode != RL_ADV_GROUP_REWARDS) r.A = a.adv[a.adv_mode == RL_ADV_PER_TOKEN ? row : row / a.T];
+    r.b = seq_of(row, a.T);
+    if (a.adv_mode != RL_ADV_GROUP_REWARDS) r.A = a.adv[a.adv_mode == RL_ADV_PER_TOKEN ? row : r.b];
     r.lpo = a.logp_old ? a.logp_old[row] : 0.f;
     r.rf = a.ref_logp ? a.ref_logp[row] : 0.f;
   }
@@ -559,7 +591,7 @@ __device__ __forceinline__ float warp_group_advantage(const LossArgs& a, long lo
 // row's partial statistics; 2 (vocabulary shard) merge the gathered shard
 // partials instead of pass 1, then the loss and this shard's gradient.
 template <int DT, bool kStream, int kMode>
-__global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kernel(const LossArgs a) {
+__global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(const LossArgs a) {
   using E = Elem<DT>;
   constexpr int kVec = E::kVec;
   constexpr int kChunkElems = kChunkBytes / E::kBytes;
@@ -745,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) policy_loss_kern
         break;
       }
       // Per-sequence quantities, recomputed by each warp when the sequence changes.
-      const long long bseq = row / a.T;
+      const long long bseq = rs.b;
       if (bseq != cache_b) {
         cache_b = bseq;
         if (a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN)
@@ -1091,8 +1123,8 @@ bool choose_layout(int es, long long V, Plan* p) {
 
 template <int DT, int M>
 void* kernel_ptr(bool stream) {
-  return stream ? reinterpret_cast<void*>(&policy_loss_kernel<DT, true, M>)
-                : reinterpret_cast<void*>(&policy_loss_kernel<DT, false, M>);
+  return stream ? reinterpret_cast<void*>(&RL_LOSS_KERNEL<DT, true, M>)
+                : reinterpret_cast<void*>(&RL_LOSS_KERNEL<DT, false, M>);
 }
 
 template <int M>
@@ -1171,46 +1203,25 @@ bool finite(float x) { return std::isfinite(x); }
 using namespace rl;
 
 // ------------------------------------------------------------------ no-allocation variant
-// Scratch for rl_policy_loss_fwd_bwd_noalloc: the workspace a caller would
-// otherwise allocate (status header + one partial per CTA, kWorkspaceBytes =
-// 131,328 bytes), held in a file-scope device array instead.  Every GPU that
-// loads the library holds it until the process exits.
-static __device__ __align__(256) unsigned char g_loss_scratch[kWorkspaceBytes];
-
 namespace {
-std::mutex g_scratch_mu;
-std::map<int, void*> g_scratch_addr;  // device ordinal -> device address of g_loss_scratch
+template <int DT, bool S>
+cudaError_t launch_one(cudaLaunchConfig_t* cfg, int mode, const LossArgs& args) {
+  return mode == 1 ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 1>, args)
+       : mode == 2 ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 2>, args)
+                   : cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 0>, args);
+}
 
-// In host code g_loss_scratch names a host-side stand-in, not device memory:
-// the device address must come from cudaGetSymbolAddress, once per device,
-// with that device current.
-rl_status loss_scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  auto found = g_scratch_addr.find(dev);
-  if (found != g_scratch_addr.end()) {
-    *out = found->second;
-    return RL_OK;
-  }
-  void* ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_loss_scratch) != cudaSuccess || ptr == nullptr)
-    return RL_ERR_CUDA;
-  g_scratch_addr[dev] = ptr;
-  *out = ptr;
-  return RL_OK;
+template <int DT>
+cudaError_t launch_mode(cudaLaunchConfig_t* cfg, bool stream, int mode, const LossArgs& args) {
+  return stream ? launch_one<DT, true>(cfg, mode, args) : launch_one<DT, false>(cfg, mode, args);
 }
 }  // namespace
 
-extern "C" size_t rl_policy_loss_workspace_size(long long n_rows) {
-  (void)n_rows;
-  return kWorkspaceBytes;
-}
+// ------------------------------------------------------------------ this build's entry
+namespace RL_ROWS_NS {
 
-extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, long long n_rows,
-                                                 int* cluster_size, int* n_clusters,
-                                                 int* smem_bytes) {
-  if (!cluster_size || !n_clusters || !smem_bytes) return RL_ERR_NULL;
+RL_INTERNAL rl_status launch_shape(rl_dtype dtype, long long V, long long n_rows, int* cluster_size,
+                                   int* n_clusters, int* smem_bytes) {
   Plan p;
   const rl_status st = plan(dtype, V, n_rows, &p);
   if (st != RL_OK) return st;
@@ -1220,37 +1231,7 @@ extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, lo
   return RL_OK;
 }
 
-namespace {
-template <int DT, bool S>
-cudaError_t launch_one(cudaLaunchConfig_t* cfg, int mode, const LossArgs& args) {
-  return mode == 1 ? cudaLaunchKernelEx(cfg, policy_loss_kernel<DT, S, 1>, args)
-       : mode == 2 ? cudaLaunchKernelEx(cfg, policy_loss_kernel<DT, S, 2>, args)
-                   : cudaLaunchKernelEx(cfg, policy_loss_kernel<DT, S, 0>, args);
-}
-
-template <int DT>
-cudaError_t launch_mode(cudaLaunchConfig_t* cfg, bool stream, int mode, const LossArgs& args) {
-  return stream ? launch_one<DT, true>(cfg, mode, args) : launch_one<DT, false>(cfg, mode, args);
-}
-}  // namespace
-
-extern "C" void rl_policy_loss_desc_init(rl_policy_loss_desc* d) {
-  if (!d) return;
-  std::memset(d, 0, sizeof(*d));
-  d->dtype = RL_BF16;
-  d->adv_layout = RL_ADV_PER_SEQ;
-  d->group_size = 1;
-  d->ddof = 1;
-  d->std_eps = 1e-4;
-  d->eps = 0.2f;
-  d->eps_high = -1.f;
-  d->grad_scale = 1.f;
-  d->agg = RL_AGG_TOKEN_MEAN;
-  d->agg_norm = 1.0;
-}
-
-extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, void* stream) {
-  if (!d) return RL_ERR_NULL;
+RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream) {
   const int es = elem_bytes(d->dtype);
   if (es == 0) return RL_ERR_DTYPE;
   if (d->adv_layout != RL_ADV_PER_SEQ && d->adv_layout != RL_ADV_PER_TOKEN &&
@@ -1264,7 +1245,7 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   if (B > 0 && T > (1LL << 40) / B) return RL_ERR_SHAPE;
   const long long R = B * T;
   if (!d->stats_dev) return RL_ERR_NULL;
-  if (!d->workspace || d->workspace_bytes < rl_policy_loss_workspace_size(R)) return RL_ERR_WORKSPACE;
+  if (!d->workspace || d->workspace_bytes < kWorkspaceBytes) return RL_ERR_WORKSPACE;
   if (R > 0 && (!d->logits || !d->ids || !d->mask || !d->adv)) return RL_ERR_NULL;
   if (d->beta != 0.f && !d->ref_logp) return RL_ERR_NULL;
   if (!finite(d->eps) || d->eps < 0.f || !finite(d->eps_high) || !finite(d->beta) ||
@@ -1367,6 +1348,92 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, voi
   return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
 
+}  // namespace RL_ROWS_NS
+
+#ifndef RL_SHORT_ROWS
+// ------------------------------------------------------------------ C entry points
+namespace rl_short_rows {
+RL_INTERNAL rl_status launch_shape(rl_dtype dtype, long long V, long long n_rows, int* cluster_size,
+                                   int* n_clusters, int* smem_bytes);
+RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream);
+}  // namespace rl_short_rows
+
+namespace {
+// Rows (this call's columns) of at most this many bytes take the short-row
+// build: two CTAs per SM measured faster up to 100 KB rows (V = 50,000
+// bf16) and slower from 128 KB on when most rows are masked.
+constexpr long long kShortRowBytes = 102400;
+
+bool short_rows(rl_dtype dtype, long long V) {
+  const int es = elem_bytes(dtype);
+  return es > 0 && V >= 1 && V <= kShortRowBytes / es;
+}
+}  // namespace
+
+// Scratch for rl_policy_loss_fwd_bwd_noalloc: the workspace a caller would
+// otherwise allocate (status header + one partial per CTA, kWorkspaceBytes =
+// 131,328 bytes), held in a file-scope device array instead.  Every GPU that
+// loads the library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_loss_scratch[kWorkspaceBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+std::map<int, void*> g_scratch_addr;  // device ordinal -> device address of g_loss_scratch
+
+// In host code g_loss_scratch names a host-side stand-in, not device memory:
+// the device address must come from cudaGetSymbolAddress, once per device,
+// with that device current.
+rl_status loss_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  auto found = g_scratch_addr.find(dev);
+  if (found != g_scratch_addr.end()) {
+    *out = found->second;
+    return RL_OK;
+  }
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_loss_scratch) != cudaSuccess || ptr == nullptr)
+    return RL_ERR_CUDA;
+  g_scratch_addr[dev] = ptr;
+  *out = ptr;
+  return RL_OK;
+}
+}  // namespace
+
+extern "C" size_t rl_policy_loss_workspace_size(long long n_rows) {
+  (void)n_rows;
+  return kWorkspaceBytes;
+}
+
+extern "C" rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, long long n_rows,
+                                                 int* cluster_size, int* n_clusters,
+                                                 int* smem_bytes) {
+  if (!cluster_size || !n_clusters || !smem_bytes) return RL_ERR_NULL;
+  return short_rows(dtype, V) ? rl_short_rows::launch_shape(dtype, V, n_rows, cluster_size, n_clusters, smem_bytes)
+                              : rl_long_rows::launch_shape(dtype, V, n_rows, cluster_size, n_clusters, smem_bytes);
+}
+
+extern "C" void rl_policy_loss_desc_init(rl_policy_loss_desc* d) {
+  if (!d) return;
+  std::memset(d, 0, sizeof(*d));
+  d->dtype = RL_BF16;
+  d->adv_layout = RL_ADV_PER_SEQ;
+  d->group_size = 1;
+  d->ddof = 1;
+  d->std_eps = 1e-4;
+  d->eps = 0.2f;
+  d->eps_high = -1.f;
+  d->grad_scale = 1.f;
+  d->agg = RL_AGG_TOKEN_MEAN;
+  d->agg_norm = 1.0;
+}
+
+extern "C" rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* d, void* stream) {
+  if (!d) return RL_ERR_NULL;
+  return short_rows(d->dtype, d->V) ? rl_short_rows::fwd_bwd(d, stream) : rl_long_rows::fwd_bwd(d, stream);
+}
+
 extern "C" rl_status rl_policy_loss_fwd_bwd(const void* logits, rl_dtype dtype, long long B,
                                             long long T, long long V, long long ld,
                                             const long long* ids, const float* logp_old,
@@ -1426,3 +1493,4 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_noalloc(
                                 adv_layout, eps, beta, c_ent, grad_scale, dlogits, logp_out,
                                 entropy_out, stats_dev, scratch, sizeof(g_loss_scratch), stream);
 }
+#endif  // !RL_SHORT_ROWS

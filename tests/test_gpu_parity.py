@@ -126,6 +126,12 @@ def test_launch_shape():
         c, n, smem = rl.rl_policy_loss_launch_shape(dt, V, 32768)
         assert c == 1 and 1 <= n <= 2048 and smem <= 227 * 1024, (dt, V, c, n, smem)
     assert rl.rl_policy_loss_launch_shape("bf16", 151936, 5)[1] == 5  # no more CTAs than rows
+    # rows of at most 100 KB take the short-row build: two CTAs per SM
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert rl.rl_policy_loss_launch_shape("f16", 32000, 1 << 20)[1] == 2 * sms
+    assert rl.rl_policy_loss_launch_shape("bf16", 51200, 1 << 20)[1] == 2 * sms
+    assert rl.rl_policy_loss_launch_shape("bf16", 51208, 1 << 20)[1] == sms
+    assert rl.rl_policy_loss_launch_shape("bf16", 151936, 1 << 20)[1] == sms
     with pytest.raises(rl.RlLossError):
         rl.rl_policy_loss_launch_shape("bf16", (1 << 30) + 8, 10)  # beyond 32-bit row offsets
 

@@ -590,7 +590,7 @@ __device__ __forceinline__ float warp_group_advantage(const LossArgs& a, long lo
 // kMode: 0 the whole loss; 1 (vocabulary shard) pass 1 only, writing each
 // row's partial statistics; 2 (vocabulary shard) merge the gathered shard
 // partials instead of pass 1, then the loss and this shard's gradient.
-template <int DT, bool kStream, int kMode>
+template <int DT, bool kStream, int kMode, bool kEnt>
 __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(const LossArgs a) {
   using E = Elem<DT>;
   constexpr int kVec = E::kVec;
@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
     // Data parallel over ranks: the means run over every rank's tokens.
     const long long N = a.global_counts ? a.global_counts[0] : N_local;
     const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
-    const bool with_entropy = a.c_ent != 0.f;
+    constexpr bool with_entropy = kEnt;  // c_ent != 0: the entropy term is in the gradient
     const bool seq_agg = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN || a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM;
     long long Bp = 0;  // sequences with at least one valid token
     if (seq_agg && a.global_counts) {
@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
           zy = max_nan(zy, __shfl_xor_sync(0xffffffffu, zy, o));
         }
         const uint32_t b = vrow & 1;
-        if (csize == 1) {  // one CTA per row: CTA-scope publish and wait
+        if (!RL_CLUSTER_RESIDENT || csize == 1) {  // one CTA per row: CTA-scope publish and wait
           if (lane == 0) {
             sm.xpart[b][warp] = make_float4(m, s, t, zy);
             mbar_arrive(smem_addr(&sm.xbar[b]));
@@ -1121,26 +1121,28 @@ bool choose_layout(int es, long long V, Plan* p) {
   return false;
 }
 
-template <int DT, int M>
+// The entropy term is a template argument (c_ent != 0); the statistics-only
+// mode has no gradient and is built without it.
+template <int DT, int M, bool E>
 void* kernel_ptr(bool stream) {
-  return stream ? reinterpret_cast<void*>(&RL_LOSS_KERNEL<DT, true, M>)
-                : reinterpret_cast<void*>(&RL_LOSS_KERNEL<DT, false, M>);
+  return stream ? reinterpret_cast<void*>(&RL_LOSS_KERNEL<DT, true, M, E>)
+                : reinterpret_cast<void*>(&RL_LOSS_KERNEL<DT, false, M, E>);
 }
 
-template <int M>
+template <int M, bool E>
 void* kernel_for_mode(rl_dtype dt, bool stream) {
   switch (dt) {
-    case RL_F32: return kernel_ptr<RL_F32, M>(stream);
-    case RL_BF16: return kernel_ptr<RL_BF16, M>(stream);
-    case RL_F16: return kernel_ptr<RL_F16, M>(stream);
+    case RL_F32: return kernel_ptr<RL_F32, M, E>(stream);
+    case RL_BF16: return kernel_ptr<RL_BF16, M, E>(stream);
+    case RL_F16: return kernel_ptr<RL_F16, M, E>(stream);
   }
   return nullptr;
 }
 
-void* kernel_for(rl_dtype dt, bool stream, int mode) {
-  return mode == 1 ? kernel_for_mode<1>(dt, stream)
-       : mode == 2 ? kernel_for_mode<2>(dt, stream)
-                   : kernel_for_mode<0>(dt, stream);
+void* kernel_for(rl_dtype dt, bool stream, int mode, bool ent) {
+  if (mode == 1) return kernel_for_mode<1, false>(dt, stream);
+  if (mode == 2) return ent ? kernel_for_mode<2, true>(dt, stream) : kernel_for_mode<2, false>(dt, stream);
+  return ent ? kernel_for_mode<0, true>(dt, stream) : kernel_for_mode<0, false>(dt, stream);
 }
 
 // Per (device, kernel, cluster size): attributes set once and the number of
@@ -1158,9 +1160,12 @@ rl_status max_clusters(rl_dtype dt, bool stream, int cluster, int mode, int* out
     *out = found->second;
     return RL_OK;
   }
-  void* fn = kernel_for(dt, stream, mode);
+  // both entropy variants get the shared-memory attribute; they have the same occupancy
+  void* fn = kernel_for(dt, stream, mode, false);
+  void* fn_ent = kernel_for(dt, stream, mode, true);
   const int smem = static_cast<int>(sizeof(LossSmem));
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(fn_ent, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return RL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -1202,18 +1207,21 @@ bool finite(float x) { return std::isfinite(x); }
 
 using namespace rl;
 
-// ------------------------------------------------------------------ no-allocation variant
+// ------------------------------------------------------------------ launch
 namespace {
 template <int DT, bool S>
-cudaError_t launch_one(cudaLaunchConfig_t* cfg, int mode, const LossArgs& args) {
-  return mode == 1 ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 1>, args)
-       : mode == 2 ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 2>, args)
-                   : cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 0>, args);
+cudaError_t launch_one(cudaLaunchConfig_t* cfg, int mode, bool ent, const LossArgs& args) {
+  if (mode == 1) return cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 1, false>, args);
+  if (mode == 2)
+    return ent ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 2, true>, args)
+               : cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 2, false>, args);
+  return ent ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 0, true>, args)
+             : cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 0, false>, args);
 }
 
 template <int DT>
-cudaError_t launch_mode(cudaLaunchConfig_t* cfg, bool stream, int mode, const LossArgs& args) {
-  return stream ? launch_one<DT, true>(cfg, mode, args) : launch_one<DT, false>(cfg, mode, args);
+cudaError_t launch_mode(cudaLaunchConfig_t* cfg, bool stream, int mode, bool ent, const LossArgs& args) {
+  return stream ? launch_one<DT, true>(cfg, mode, ent, args) : launch_one<DT, false>(cfg, mode, ent, args);
 }
 }  // namespace
 
@@ -1341,9 +1349,9 @@ RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream) {
   cfg.numAttrs = 2;
   cudaError_t e = cudaErrorInvalidValue;
   switch (d->dtype) {
-    case RL_F32: e = launch_mode<RL_F32>(&cfg, pl.stream, mode, args); break;
-    case RL_BF16: e = launch_mode<RL_BF16>(&cfg, pl.stream, mode, args); break;
-    case RL_F16: e = launch_mode<RL_F16>(&cfg, pl.stream, mode, args); break;
+    case RL_F32: e = launch_mode<RL_F32>(&cfg, pl.stream, mode, d->c_ent != 0.f, args); break;
+    case RL_BF16: e = launch_mode<RL_BF16>(&cfg, pl.stream, mode, d->c_ent != 0.f, args); break;
+    case RL_F16: e = launch_mode<RL_F16>(&cfg, pl.stream, mode, d->c_ent != 0.f, args); break;
   }
   return e == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }

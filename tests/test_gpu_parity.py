@@ -101,12 +101,21 @@ SMALL = {
                                             lengths=("uniform", 1, 4)),
     "bf16_v300001_stream": W["large_grpo"].scaled(n_prompts=1, group=4, T=4, V=300001,
                                                   lengths=("uniform", 1, 4), c_ent=0.01),
-    "f16_v32768_resident_max": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=32768,
-                                                         lengths=("uniform", 2, 8)),
-    "f16_v32776_stream_min": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=32776,
-                                                       lengths=("uniform", 2, 8), c_ent=0.02),
+    "f16_v32768": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=32768,
+                                            lengths=("uniform", 2, 8)),
+    "f16_v32776": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=32776,
+                                            lengths=("uniform", 2, 8), c_ent=0.02),
     "f16_v49152_stream": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=49152,
                                                    lengths=("uniform", 2, 8)),
+    # the two builds of the loss kernel: rows of at most 100 KB take the short-row one
+    # (16 KB chunks: rows of up to 32 KB stay on chip), longer rows the long-row one
+    "bf16_v16392_short_stream_min": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8,
+                                                                V=16392, lengths=("uniform", 1, 8),
+                                                                c_ent=0.01),
+    "bf16_v51200_short_max": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=51200,
+                                                         lengths=("uniform", 1, 8), c_ent=0.01),
+    "bf16_v51208_long_min": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=51208,
+                                                        lengths=("uniform", 1, 8), c_ent=0.01),
 }
 PADDED_LD = {"f32_v12345_ragged": 12348, "bf16_v1001_ragged": 1008, "f16_v7_tiny": 8,
              "bf16_v300001_stream": 300008}

@@ -7,7 +7,11 @@
 // paragraph after its benchmark table, in one launch to avoid global-memory
 // round trips.  This kernel is that step for GB300, designed around HBM:
 //
-//   * Persistent grid, one CTA per SM; CTA q takes rows q, q + Q, ...
+//   * Persistent grid; CTA q takes rows q, q + Q, ...  Two builds of this
+//     source (see RL_SHORT_ROWS below): one CTA per SM with 16 consumer
+//     warps and 32 KB chunks for rows longer than 100 KB, two CTAs per SM
+//     with 8 consumer warps and 16 KB chunks for shorter rows.  The figures
+//     in the rest of this comment are the long-row build's.
 //   * One producer warp streams the valid rows with 1-D bulk copies
 //     (cp.async.bulk) into a ring of 6 x 32 KB shared-memory chunks guarded
 //     by full/empty mbarriers.  It runs ahead of the consumers by up to the
@@ -32,12 +36,13 @@
 //     valid rows' arithmetic without taking the consumers' store path.
 //   * Each row loop reads the mask bytes of 32 of its rows with one ballot
 //     and jumps to the next row it handles.
-//   * Sixteen consumer warps.  Pass 1: per-thread online (max, sum 2^x,
+//   * Consumer warps.  Pass 1: per-thread online (max, sum 2^x,
 //     sum 2^x * x) in packed fp32x2 with independent accumulator chains.
 //     Each warp shuffle-merges its lanes and publishes one partial; the
 //     partials meet through one mbarrier (no CTA-wide barrier per row), and
 //     every warp merges them with shuffles.  Pass 2: the gradient, written
-//     with 16-byte streaming stores.
+//     with 16-byte streaming stores.  The entropy term is a template
+//     argument, so each launch runs only the pass-2 code it needs.
 //   * Masked rows: all-zero gradient stores only, their logits are not read.
 //   * N (valid tokens) is counted by every CTA at start (R bytes from L2);
 //     the loss is reduced in fp64: per-CTA partials in a fixed row order,

@@ -87,6 +87,16 @@ def bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def bf16_sustained_peak():
+    """The bf16 GEMM rate held for seconds under the power cap, or None."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -818,6 +828,10 @@ def run_lmhead(args):
                      "kernel_ms": kern_ms},
         "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
     }
+    sust = bf16_sustained_peak()
+    if sust:  # back-to-back launches run under the power cap: the sustained figure beside the burst one
+        out["roofline"]["peak_sustained"] = sust
+        out["roofline"]["frac_of_sustained"] = achieved / sust
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = lmhead_cpu(h, w, ids, args.cpu_seconds)
     if world > 1:

@@ -314,7 +314,21 @@ def workload_for(args):
     if args.seqs:  # a slice of the workload (profiling captures): same T, V and distributions
         w = (w.scaled(n_prompts=max(1, args.seqs // w.group)) if args.seqs >= w.group
              else w.scaled(n_prompts=1, group=max(2, args.seqs)))
+    # other shapes of the same workload (profiling captures and sweeps)
+    if getattr(args, "vocab", 0):
+        w = w.scaled(V=args.vocab)
+    if getattr(args, "dtype", None):
+        w = w.scaled(dtype=args.dtype)
+    if getattr(args, "seq_len", 0):
+        w = w.scaled(T=args.seq_len)
+    if getattr(args, "all_valid", False):
+        w = w.scaled(lengths=("full",))
     return w
+
+
+def reshaped(args) -> bool:
+    return bool(args.seqs or getattr(args, "vocab", 0) or getattr(args, "dtype", None)
+                or getattr(args, "seq_len", 0) or getattr(args, "all_valid", False))
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -376,7 +390,7 @@ def run_gpu(args):
     bytes_launch = alg_bytes(w, n_valid)
     peak, peak_kind = hbm_peak()
     achieved = bytes_launch / (kern_ms / 1e3) / 1e9
-    traffic = recorded_traffic(args.workload) if not args.seqs else None
+    traffic = recorded_traffic(args.workload) if not reshaped(args) else None
 
     # ---- end to end through the C ABI with pinned host buffers
     e2e = run_e2e(args, w, inp, dev, stream, step) if args.e2e_steps > 0 else None
@@ -388,7 +402,8 @@ def run_gpu(args):
         "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": {"workload": f"{args.workload}: {DESCRIBE.get(args.workload, '')}",
                    "B": w.B, "T": w.T, "V": w.V, "rows": w.R, "valid_tokens": n_valid,
-                   "slice": (f"profiling slice: first {w.B} sequences" if args.seqs else None),
+                   "slice": (f"profiling shape: {w.B} sequences x T={w.T}, V={w.V} {w.dtype}, "
+                             f"lengths {w.lengths[0]}" if reshaped(args) else None),
                    "valid_tokens_per_s": world * n_valid / (ms_step / 1e3),
                    "l2": (f"inputs ({w.R * w.V * w.elem_bytes / 1e9:.1f} GB logits) vs 129 MB "
                           "L2; no flush"),
@@ -890,6 +905,12 @@ def main():
                     help="with N > 1: normalise by the token count summed over ranks")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profiling only: keep the first SEQS sequences")
+    ap.add_argument("--vocab", type=int, default=0, help="profiling only: another V")
+    ap.add_argument("--dtype", choices=["f32", "bf16", "f16"], default=None,
+                    help="profiling only: another logits dtype")
+    ap.add_argument("--seq-len", type=int, default=0, help="profiling only: another T")
+    ap.add_argument("--all-valid", action="store_true",
+                    help="profiling only: every position valid (no masked rows)")
     ap.add_argument("--lmhead", action="store_true",
                     help="time rl_lmhead_logprobs on the Qwen3-0.6B LM head instead")
     ap.add_argument("--lmhead-rows", type=int, default=0,

@@ -85,3 +85,18 @@ def test_traffic_record_ignored_when_kernel_changed(tmp_path):
 def test_alg_bytes_ppo_counts_per_token_advantages_and_no_reference():
     w = synth.WORKLOADS["ppo_gae"]
     assert bench.alg_bytes(w, w.R) == 2 * w.R * w.V * 2 + w.R * 21 + w.R * 4
+
+
+def test_profiling_shape_options_reshape_the_workload():
+    import argparse
+    base = dict(workload="long_seq_grpo", seqs=0, vocab=0, dtype=None, seq_len=0,
+                all_valid=False)
+    a = argparse.Namespace(**base)
+    assert bench.workload_for(a) == synth.WORKLOADS["long_seq_grpo"] and not bench.reshaped(a)
+    b = argparse.Namespace(**dict(base, seqs=8, vocab=50000, dtype="bf16", seq_len=1024,
+                                  all_valid=True))
+    w = bench.workload_for(b)
+    assert (w.B, w.T, w.V, w.dtype, w.lengths) == (8, 1024, 50000, "bf16", ("full",))
+    assert bench.reshaped(b)
+    mask = synth.small_inputs(w)["mask"]
+    assert mask.size == w.R and int(mask.sum()) == w.R  # every position valid

@@ -249,6 +249,12 @@ def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent, 
     branch is strictly the smaller one, i.e. (A > 0 and r > 1 + eps) or
     (A < 0 and r < 1 - eps); kl' = 1 - exp(d); so g = pg' + beta (exp(d) - 1).
     Masked tokens give zeros everywhere.
+
+    Also returned: both one-sided derivatives of the surrogate at every token,
+    g_unclipped (pg' = r A) and g_clipped (pg' = 0), each with the same KL
+    term.  At a token whose ratio lies on a clip boundary the surrogate has a
+    kink; there each of the two is a valid gradient, and an implementation
+    that evaluates r in lower precision may take either side.
     """
     m = np.asarray(mask).astype(bool)
     logp = np.where(m, logp, 0.0)
@@ -267,7 +273,8 @@ def token_objective(logp, ent, mask, adv, logp_old, ref_logp, eps, beta, c_ent, 
     J = pg - beta * kl + c_ent * H
     g = dpg + beta * dkl
     z = lambda x: np.where(m, x, 0.0)
-    return dict(r=z(r), pg=z(pg), kl=z(kl), H=H, J=z(J), g=z(g), clipped=m & clipped)
+    return dict(r=z(r), pg=z(pg), kl=z(kl), H=H, J=z(J), g=z(g), clipped=m & clipped,
+                g_unclipped=z(r * A + beta * dkl), g_clipped=z(beta * dkl))
 
 
 AGGREGATIONS = ("token_mean", "seq_mean_token_mean", "seq_mean_token_sum", "token_sum_norm")

@@ -298,6 +298,48 @@ def test_surrogate_brute_force_derivative():
             assert abs(oracle.surrogate(r, A, eps)[1] - fd) < 1e-6
 
 
+def test_one_sided_derivatives_at_the_clip_kink():
+    # With the ratio exactly on a clip boundary the surrogate has a kink: the
+    # derivative of J in logp from one side is the unclipped branch (r A +
+    # KL term), from the other the clipped one (KL term only).  Which side is
+    # which depends on the sign of A.  One-sided differences of the oracle's
+    # own J pin g_unclipped and g_clipped; away from the kink g is one of them.
+    eps, beta, h = 0.2, 0.3, 1e-7
+    lo_ref = -1.3
+    for A, r_b in ((0.9, 1 + eps), (-0.7, 1 - eps), (1.4, 1 - eps), (-2.0, 1 + eps)):
+        lo = -2.0
+        l0 = lo + math.log(r_b)
+        m = np.ones(1, np.uint8)
+
+        def J(l):
+            return oracle.token_objective(np.array([l]), np.zeros(1), m, np.array([A]),
+                                          np.array([lo]), np.array([lo_ref]), eps, beta, 0.0)["J"][0]
+
+        o = oracle.token_objective(np.array([l0]), np.zeros(1), m, np.array([A]), np.array([lo]),
+                                   np.array([lo_ref]), eps, beta, 0.0)
+        right = (J(l0 + h) - J(l0)) / h
+        left = (J(l0) - J(l0 - h)) / h
+        # r grows with logp.  The clip binds above 1 + eps when A > 0 and below
+        # 1 - eps when A < 0; at the other boundary there is no kink.
+        if A > 0 and r_b > 1:
+            free_side, clipped_side = left, right
+        elif A < 0 and r_b < 1:
+            free_side, clipped_side = right, left
+        else:
+            free_side, clipped_side = left, None
+            assert abs(right - o["g_unclipped"][0]) < 1e-5, (A, r_b)
+        assert abs(free_side - o["g_unclipped"][0]) < 1e-5, (A, r_b)
+        if clipped_side is not None:
+            assert abs(clipped_side - o["g_clipped"][0]) < 1e-5, (A, r_b)
+        # at the boundary itself the gradient flows (inclusive clip): g is the unclipped branch
+        assert o["g"][0] == o["g_unclipped"][0]
+    z, ids, mask, adv, n_old, n_ref = _problem(29, R=40)
+    _, logp, H = oracle.row_stats(z, "f64", z.shape[1], ids, mask, threads=1)
+    o = oracle.token_objective(logp, H, mask, 3 * adv, logp + 3 * n_old, logp + n_ref, 0.05, 0.2, 0.0)
+    assert o["clipped"].any() and (~o["clipped"] & (mask != 0)).any()
+    assert np.array_equal(o["g"], np.where(o["clipped"], o["g_clipped"], o["g_unclipped"]))
+
+
 def test_kl_k3_zero_at_reference_and_quadratic_small():
     logp = np.array([-3.0, -1.0, -0.5])
     m = np.ones(3, np.uint8)

@@ -59,6 +59,11 @@ def oracle_stats_chunked(logits_t, dtype, V, ids, mask, chunk=2048):
     return lse, logp, ent
 
 
+def ref_rows(ref, rows):
+    """The oracle's per-token gradient coefficients of the listed rows."""
+    return {k: ref[k][rows] for k in ("g", "g_unclipped", "g_clipped")}
+
+
 def band_mask(o, eps):
     r = o["r"]
     return (np.abs(r - (1 + eps)) < CLIP_BAND) | (np.abs(r - (1 - eps)) < CLIP_BAND)
@@ -104,6 +109,78 @@ def assert_dlogits_close(gpu_store, ref_store, dtype, where=""):
         raise AssertionError(f"{where} dlogits: {int(bad.sum())} elements out of tolerance; first at "
                              f"{tuple(i)}: gpu {g[tuple(i)]!r} oracle {r[tuple(i)]!r} tol {tol[tuple(i)]!r}")
     return float((err / np.maximum(oracle.ulp(r, dtype), 1e-300)).max()) if err.size else 0.0
+
+
+_FMT = {"f32": (24, -126), "bf16": (8, -126), "f16": (11, -14)}
+
+
+def _widen(t: torch.Tensor, dtype) -> torch.Tensor:
+    """Elements of a bf16/f16/f32 tensor (or of its uint16/int16 storage) as fp64."""
+    if dtype in ("bf16", "f16") and t.dtype in (torch.int16, torch.uint16):
+        t = t.view(torch.int16).view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.float().double()
+
+
+def _ulp_dev(r: torch.Tensor, dtype) -> torch.Tensor:
+    """oracle.ulp on the device: the spacing of ``dtype`` at |r| (r holds values
+    of that format), built from the fp32 exponent field so that it is exact."""
+    p, emin = _FMT[dtype]
+    bits = r.abs().float().view(torch.int32)
+    e = ((bits >> 23) & 0xFF).to(torch.int64) - 127      # -127 for 0 and fp32 subnormals
+    u = torch.clamp(e, min=emin) - (p - 1)
+    return ((u + 1023) << 52).view(torch.float64)
+
+
+def rows_within(gpu_rows: torch.Tensor, ref_store: np.ndarray, dtype):
+    """Per row: True when every element of the GPU's gradient row lies within
+    the dlogits tolerance of the oracle's rounded value.  Compared on the
+    device (the full-size workloads hold tens of GB of gradient).  Returns
+    (per-row bool array, max error in units of the oracle value's ulp)."""
+    dev = gpu_rows.device
+    ref = torch.from_numpy(np.ascontiguousarray(ref_store))
+    if dtype in ("bf16", "f16"):
+        ref = ref.view(torch.int16)
+    r = _widen(ref.to(dev), dtype)
+    g = _widen(gpu_rows, dtype)
+    u = _ulp_dev(r, dtype)
+    tol = u + DLOGIT_ATOL
+    if dtype == "f32":
+        tol = tol + DLOGIT_F32_RTOL * r.abs()
+    err = (g - r).abs()
+    ok = (err <= tol).all(dim=1)          # NaN compares false
+    worst = float((err / u).max()) if err.numel() else 0.0
+    return ok.cpu().numpy(), worst
+
+
+def check_dlogits_rows(gpu_rows, host, dtype, V, ids, rows, lse, ent, ref, band, scale, c_ent,
+                       where=""):
+    """Every listed row of the GPU's gradient against the oracle.
+
+    ``host`` holds the logits storage that ``rows`` index (with ``ids``);
+    ``lse``, ``ent``, ``scale`` and ``band`` are per listed row, ``ref`` is the
+    oracle's loss_from_stats output indexed by the same listed rows.  A row
+    in the clip band (its ratio within CLIP_BAND of a clip boundary, where
+    the kernel's fp32 ratio may fall on the other side) must match the
+    gradient of one of the surrogate's two branches; every other row must
+    match the oracle's own gradient.  Returns the max error in ulps."""
+    main = oracle.dlogits_rows(host, dtype, V, ids, rows, lse, ent, ref["g"], scale, c_ent, dtype)
+    ok, worst = rows_within(gpu_rows, main, dtype)
+    for i in np.nonzero(~ok & band)[0]:  # a band row may take the other branch
+        for key in ("g_unclipped", "g_clipped"):
+            alt = oracle.dlogits_rows(host, dtype, V, ids, rows[i:i + 1], lse[i:i + 1],
+                                      ent[i:i + 1], ref[key][i:i + 1], scale[i:i + 1], c_ent, dtype)
+            if rows_within(gpu_rows[i:i + 1], alt, dtype)[0][0]:
+                ok[i] = True
+                break
+    if not ok.all():
+        i = int(np.nonzero(~ok)[0][0])
+        g = _widen(gpu_rows[i:i + 1], dtype).cpu().numpy()[0]
+        r = oracle.decode(main[i], dtype)
+        j = int(np.argmax(np.abs(g - r)))
+        raise AssertionError(f"{where} dlogits: {int((~ok).sum())} of {ok.size} rows out of "
+                             f"tolerance; first: listed row {i} (band {bool(band[i])}), element "
+                             f"{j}: gpu {g[j]!r} oracle {r[j]!r}")
+    return worst
 
 
 def build_case(w, device="cuda", ld=None, n_rows=None):

@@ -7,9 +7,10 @@ most two chunks held on chip for both passes, longer rows streamed twice
 through the ring, up to 128 chunks per row, including a row whose last
 chunk is 16 bytes), ragged vocabulary tails and padded rows.  The
 full-size workloads run in the launch configuration the benchmark times and
-are compared on the scalar loss and statistics (all rows), on logp/entropy
-(all rows), on sampled dlogits rows, and on properties that hold at any size
-(masked rows exactly zero).
+are compared on the scalar loss and statistics, on logp/entropy of every
+row and on every element of every gradient row (masked rows exactly zero),
+at grad_scale N and 1.  Rows whose ratio lies within CLIP_BAND of a clip
+boundary must match the gradient of one of the surrogate's two branches.
 """
 import numpy as np
 import pytest
@@ -66,13 +67,11 @@ def _run_both(w, ld=None, grad_scales=(1.0, "N"), in_place=False, with_old=True,
         st = torch_api.read_stats(out["stats"])
         assert_stats_match(st, ref, n_band)
         assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
-        keep = ~band  # rows whose clip decision may flip are compared separately
-        rows = np.nonzero(keep)[0]
-        scale = np.where(mask[rows] != 0, gsv / N if N else 0.0, 0.0)
-        d_ref = oracle.dlogits_rows(host, w.dtype, V, ids, rows, lse[rows], ent[rows],
-                                    ref["g"][rows], scale, w.c_ent, w.dtype)
-        d_gpu = storage_np(out["dlogits"][:, :V])[rows]
-        report[gs] = assert_dlogits_close(d_gpu, d_ref, w.dtype, where=f"{w.name} gs={gs}")
+        rows = np.arange(R)  # every row; clip-band rows may match either branch
+        scale = np.where(mask != 0, gsv / N if N else 0.0, 0.0)
+        report[gs] = check_dlogits_rows(out["dlogits"][:, :V], host, w.dtype, V, ids, rows, lse,
+                                        ent, ref_rows(ref, rows), band, scale, w.c_ent,
+                                        where=f"{w.name} gs={gs}")
         assert np.all(storage_np(out["dlogits"][:, :V])[mask == 0] == 0)
         if ldv != V and not in_place:  # padding columns are never written
             assert bool((out["dlogits"][:, V:] == 7.0).all())
@@ -282,7 +281,11 @@ FULL = ["qwen3_0p6b_grpo", "long_seq_grpo", "ppo_gae", "large_grpo"]
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload(name):
-    """The benchmark's launch configuration at the workload's full size."""
+    """The benchmark's launch configuration at the workload's full size, at
+    grad_scale N and 1: the loss and statistics, logp and entropy of every
+    row, every element of every valid row's gradient (the oracle computes
+    them on the host a chunk of rows at a time; the comparison runs on the
+    device), and every masked row exactly zero."""
     w = W[name]
     small = synth.small_inputs(w)
     logits = synth.logits(w, device="cuda")
@@ -302,25 +305,31 @@ def test_full_size_workload(name):
         d_adv = d_adv.reshape(-1)
     else:
         d_adv = torch_api.group_advantages(to_dev(small["rewards"]), w.group)
-    out = torch_api.policy_loss(logits, to_dev(ids), to_dev(mask), d_adv, w.B, w.T,
-                                logp_old=to_dev(lo), ref_logp=to_dev(rf) if rf_arg is not None else None,
-                                eps=w.eps, beta=w.beta, c_ent=w.c_ent, grad_scale=float(N))
-    torch.cuda.synchronize()
-    st = torch_api.read_stats(out["stats"])
-    assert_stats_match(st, ref, int(band.sum()))
-    assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
-    rows = np.array([r for r in valid_and_masked_sample(mask, 24, seed=w.seed) if not band[r]])
-    host = storage_np(logits.index_select(0, to_dev(rows)))
-    scale = np.where(mask[rows] != 0, 1.0, 0.0)
-    d_ref = oracle.dlogits_rows(host, w.dtype, V, ids[rows], np.arange(rows.size), lse[rows],
-                                ent[rows], ref["g"][rows], scale, w.c_ent, w.dtype)
-    d_gpu = storage_np(out["dlogits"].index_select(0, to_dev(rows)))
-    assert_dlogits_close(d_gpu, d_ref, w.dtype, where=name)
-    # every masked row is exactly zero (checked on the device, in chunks)
+    d_ids, d_mask = to_dev(ids), to_dev(mask)
+    dlogits = torch.empty_like(logits)
+    valid = np.nonzero(mask)[0]
     dm = to_dev(mask == 0)
-    for r0 in range(0, R, 4096):
-        blk = out["dlogits"][r0:r0 + 4096][dm[r0:r0 + 4096]]
-        assert int(torch.count_nonzero(blk.view(torch.int16))) == 0
+    for gs in (float(N), 1.0):
+        out = torch_api.policy_loss(logits, d_ids, d_mask, d_adv, w.B, w.T,
+                                    logp_old=to_dev(lo),
+                                    ref_logp=to_dev(rf) if rf_arg is not None else None,
+                                    eps=w.eps, beta=w.beta, c_ent=w.c_ent, grad_scale=gs,
+                                    dlogits=dlogits)
+        torch.cuda.synchronize()
+        st = torch_api.read_stats(out["stats"])
+        assert_stats_match(st, ref, int(band.sum()))
+        assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
+        for c0 in range(0, valid.size, 1024):
+            sel = valid[c0:c0 + 1024]
+            dsel = to_dev(sel)
+            host = storage_np(logits.index_select(0, dsel))
+            check_dlogits_rows(dlogits.index_select(0, dsel), host, w.dtype, V, ids[sel],
+                               np.arange(sel.size), lse[sel], ent[sel], ref_rows(ref, sel),
+                               band[sel], np.full(sel.size, gs / N), w.c_ent,
+                               where=f"{name} gs={gs:g} rows {sel[0]}..{sel[-1]}")
+        for r0 in range(0, R, 4096):  # every masked row is exactly zero
+            blk = dlogits[r0:r0 + 4096][dm[r0:r0 + 4096]]
+            assert int(torch.count_nonzero(blk.view(torch.int16))) == 0
 
 
 # ----------------------------------------------------------------- loss options (descriptor API)
@@ -357,11 +366,9 @@ def test_aggregation_and_clip_higher(agg, eps_high):
     torch.cuda.synchronize()
     st = torch_api.read_stats(out["stats"])
     assert_stats_match(st, ref, int(band.sum()))
-    rows = np.nonzero(~band)[0]
-    scale = gs * ref["weights"][rows]
-    d_ref = oracle.dlogits_rows(host, w.dtype, w.V, ids, rows, lse[rows], ent[rows],
-                                ref["g"][rows], scale, w.c_ent, w.dtype)
-    assert_dlogits_close(storage_np(out["dlogits"])[rows], d_ref, w.dtype, where=agg)
+    rows = np.arange(w.R)
+    check_dlogits_rows(out["dlogits"], host, w.dtype, w.V, ids, rows, lse, ent, ref_rows(ref, rows),
+                       band, gs * ref["weights"], w.c_ent, where=agg)
 
 
 @pytest.mark.parametrize("ddof", [1, 0])
@@ -588,11 +595,10 @@ def test_randomized_shapes_and_options(seed):
     st = torch_api.read_stats(out["stats"])
     assert_stats_match(st, ref, int(band.sum()))
     assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
-    rows = np.nonzero(~band)[0]
-    d_ref = oracle.dlogits_rows(host, w.dtype, V, ids, rows, lse[rows], ent[rows], ref["g"][rows],
-                                gs * ref["weights"][rows], w.c_ent, w.dtype)
-    assert_dlogits_close(storage_np(out["dlogits"][:, :V])[rows], d_ref, w.dtype,
-                         where=f"seed {seed} {w.dtype} V={V} ld={ld} {o}")
+    rows = np.arange(R)
+    check_dlogits_rows(out["dlogits"][:, :V], host, w.dtype, V, ids, rows, lse, ent,
+                       ref_rows(ref, rows), band, gs * ref["weights"], w.c_ent,
+                       where=f"seed {seed} {w.dtype} V={V} ld={ld} {o}")
     if ld != V and not o["in_place"]:
         assert bool((out["dlogits"][:, V:] == 7.0).all())
 
@@ -708,10 +714,8 @@ def test_minus_infinity_and_extreme_logits(dtype, V):
     st = torch_api.read_stats(out["stats"])
     assert_stats_match(st, ref, int(band.sum()))
     assert_rows_close(out["logp"].cpu().numpy(), out["entropy"].cpu().numpy(), ref, mask)
-    rows = np.array([r for r in range(R) if not band[r]])
-    scale = np.where(mask[rows] != 0, 1.0, 0.0)  # grad_scale N times the 1/N of the token mean
-    d_ref = oracle.dlogits_rows(host[rows], dtype, V, ids[rows], np.arange(rows.size), lse[rows],
-                                ent[rows], ref["g"][rows], scale, w.c_ent, dtype)
-    d_gpu = storage_np(out["dlogits"].index_select(0, to_dev(rows)))
-    assert_dlogits_close(d_gpu, d_ref, dtype, where=f"{dtype} V={V}")
+    rows = np.arange(R)
+    scale = np.where(mask != 0, 1.0, 0.0)  # grad_scale N times the 1/N of the token mean
+    check_dlogits_rows(out["dlogits"], host, dtype, V, ids, rows, lse, ent, ref_rows(ref, rows),
+                       band, scale, w.c_ent, where=f"{dtype} V={V}")
     assert not torch.isnan(out["dlogits"].float()).any()

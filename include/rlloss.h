@@ -192,10 +192,14 @@ size_t rl_policy_loss_workspace_size(long long n_rows);
  *                 Base address 16-byte aligned; ld * sizeof(dtype) a multiple
  *                 of 16 (pad rows if V is odd); ld >= V.
  *   dtype       : RL_F32, RL_BF16 or RL_F16 (for logits and dlogits alike).
- *   B, T, V, ld : B >= 0, T >= 0, 1 <= V <= 2^30.  Rows of at most 64 KB
- *                 stay on chip for both passes; longer rows are streamed
- *                 through shared memory twice, the second time from L2.
- *                 Larger V returns RL_ERR_SHAPE.
+ *   B, T, V, ld : B >= 0, T >= 0, 1 <= V <= 2^30.  A row that fits two
+ *                 chunks of the kernel's shared-memory ring stays on chip for
+ *                 both passes: rows of at most 32 KB (short-row build, 16 KB
+ *                 chunks, rows up to 100 KB) or 64 KB (long-row build, 32 KB
+ *                 chunks, rows over 100 KB).  Other rows are streamed through
+ *                 shared memory twice, the second time from L2 (a 64 KB row,
+ *                 e.g. V = 32000 fp16, takes the short-row build and is
+ *                 streamed).  Larger V returns RL_ERR_SHAPE.
  *   ids         : int64[R], the sampled token of each row.  An id outside
  *                 [0, V) on a valid row sets RL_DEVERR_ID_RANGE and makes
  *                 that row's logp, entropy, loss and gradient NaN.
@@ -340,14 +344,17 @@ rl_status rl_policy_loss_fwd_bwd_ex(const rl_policy_loss_desc* desc, void* strea
  *
  * Same arguments, meaning and results as rl_policy_loss_fwd_bwd, minus
  * `workspace` and `workspace_bytes`.  The scratch is a file-scope device
- * array of 131,328 bytes inside the library (the workspace of a persistent
- * grid of up to 2048 CTAs, which covers every row count of the current
- * kernel); every GPU that loads the library holds it until the process
- * exits.  A call needing more scratch than that returns RL_ERR_WORKSPACE.
- * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ * array of 131,328 bytes inside the library: the status header and one
+ * partial per CTA of a persistent grid of up to 2048 CTAs.  The library
+ * never plans a larger grid, so the array covers every call; a launch plan
+ * that did not fit would return RL_ERR_WORKSPACE.  Every GPU that loads the
+ * library holds the array until the process exits.  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library call.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *     with the calling thread's current device and context), so a
+ *     cudaDeviceReset or another context on the device is followed
+ *     correctly.  The first call on a device also loads the library's device
+ *     code there; make that first call before any stream capture.
  *   - Each call clears the array's 256-byte status header with
  *     cudaMemsetAsync on `stream` before launching.  The array keeps the
  *     last call's contents otherwise.

@@ -1386,29 +1386,23 @@ bool short_rows(rl_dtype dtype, long long V) {
 // Scratch for rl_policy_loss_fwd_bwd_noalloc: the workspace a caller would
 // otherwise allocate (status header + one partial per CTA, kWorkspaceBytes =
 // 131,328 bytes), held in a file-scope device array instead.  Every GPU that
-// loads the library holds it until the process exits.
+// loads the library holds it until the process exits.  plan() never gives a
+// grid of more than kMaxGrid CTAs, so the array covers every call.
 static __device__ __align__(256) unsigned char g_loss_scratch[kWorkspaceBytes];
+static_assert(sizeof(g_loss_scratch) >= sizeof(WsHeader) + sizeof(WsPartial) * kMaxGrid,
+              "the static scratch holds the workspace of the largest grid plan() gives");
 
 namespace {
-std::mutex g_scratch_mu;
-std::map<int, void*> g_scratch_addr;  // device ordinal -> device address of g_loss_scratch
-
 // In host code g_loss_scratch names a host-side stand-in, not device memory:
-// the device address must come from cudaGetSymbolAddress, once per device,
-// with that device current.
+// the device address comes from cudaGetSymbolAddress with the target device
+// current.  It is looked up on every call rather than cached, so that a
+// cudaDeviceReset, or another context made current on the same device, never
+// leaves a stale address behind (the lookup is a host-side table read once
+// the module is loaded; the first call on a device loads it).
 rl_status loss_scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RL_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  auto found = g_scratch_addr.find(dev);
-  if (found != g_scratch_addr.end()) {
-    *out = found->second;
-    return RL_OK;
-  }
   void* ptr = nullptr;
   if (cudaGetSymbolAddress(&ptr, g_loss_scratch) != cudaSuccess || ptr == nullptr)
     return RL_ERR_CUDA;
-  g_scratch_addr[dev] = ptr;
   *out = ptr;
   return RL_OK;
 }
@@ -1494,7 +1488,12 @@ extern "C" rl_status rl_policy_loss_fwd_bwd_noalloc(
     rl_loss_stats* stats_dev, void* stream) {
   if (B < 0 || T < 0) return RL_ERR_SHAPE;
   if (B > 0 && T > (1LL << 40) / B) return RL_ERR_SHAPE;
-  if (rl_policy_loss_workspace_size(B * T) > sizeof(g_loss_scratch)) return RL_ERR_WORKSPACE;
+  // The scratch this call's grid needs: the header and one partial per CTA.
+  int cluster = 0, n_clusters = 0, smem = 0;
+  const rl_status shape = rl_policy_loss_launch_shape(dtype, V, B * T, &cluster, &n_clusters, &smem);
+  if (shape != RL_OK) return shape;
+  if (sizeof(WsHeader) + sizeof(WsPartial) * static_cast<size_t>(cluster) * n_clusters > sizeof(g_loss_scratch))
+    return RL_ERR_WORKSPACE;
   void* scratch = nullptr;
   const rl_status st = loss_scratch_address(&scratch);
   if (st != RL_OK) return st;

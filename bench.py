@@ -54,6 +54,9 @@ LMHEAD_SHAPE = dict(R=32 * 1024, D=1024, V=151936, logit_sd=3.0, seed=202)
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
 LMHEAD_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "lmhead.cu")
 LMHEAD_TRAFFIC = os.path.join(ROOT, "profiles", "lmhead_logprobs_qwen3_head_traffic.txt")
+# the workloads timed after the headline (their kernel times and roofline
+# fractions go into the line's "workloads" object)
+OTHER_WORKLOADS = ("ppo_gae", "large_grpo", "long_seq_grpo", "tiny_grpo")
 DESCRIBE = {
     "tiny_grpo": "tiny GRPO: 2 prompts x group 4 = 8 seqs, T=16, V=1024 fp32",
     "qwen3_0p6b_grpo": "Qwen3-0.6B GRPO: 4 prompts x group 8 = 32 seqs, T=1024, V=151936 bf16, "
@@ -422,13 +425,78 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, inp["logits"], budget_s=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baselines(w, args.workload, inp["logits"],
+                                            budget_s=args.cpu_seconds)
+    if world == 1 and not args.no_workloads and not reshaped(args):
+        del step, inp
+        torch.cuda.empty_cache()
+        out["workloads"] = {name: time_workload(name, dev, stream, args,
+                                                int(vis.split(",")[local]) if vis else local)
+                            for name in OTHER_WORKLOADS if name != args.workload}
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def time_workload(name, dev, stream, args, gpu_index, min_region_s=0.6, max_steps=3000):
+    """The same step on another workload, timed after the headline's timed
+    region with the headline's buffers freed: warm-up, then enough steps for
+    a timed region of about ``min_region_s`` (at least --steps), the loss
+    launch bracketed by CUDA events, clocks sampled over the region."""
+    import torch
+
+    from ppo_policy_loss_gb300 import synth, torch_api
+
+    w = synth.WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    n_valid = int(inp["small"]["mask"].sum())
+    step = Step(w, inp, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == args.warmup - 1:
+            e0.record(stream)
+        step.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    st = torch_api.read_stats(step.stats)
+    assert st["device_error"] == 0 and st["n_tokens"] == n_valid, (name, st)
+    est_ms = max(e0.elapsed_time(e1), 1e-3)
+    steps = int(min(max_steps, max(args.steps, min_region_s * 1e3 / est_ms)))
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    sampler = ClockSampler(gpu_index)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(steps):
+        step.launch(stream, kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms_step = t0.elapsed_time(t1) / steps
+    k_ms = [a.elapsed_time(b) for a, b in kev]
+    kern_ms = statistics.mean(k_ms)
+    nbytes = alg_bytes(w, n_valid)
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (kern_ms / 1e3) / 1e9
+    in_l2 = w.R * w.V * w.elem_bytes * 2 < 64e6
+    out = {"workload": f"{name}: {DESCRIBE.get(name, '')}", "B": w.B, "T": w.T, "V": w.V,
+           "dtype": w.dtype, "rows": w.R, "valid_tokens": n_valid, "steps": steps,
+           "ms_per_step": ms_step, "tokens_per_s": w.R / (ms_step / 1e3),
+           "kernel_ms": kern_ms, "kernel_ms_min": min(k_ms), "alg_bytes_per_launch": nbytes,
+           "achieved_GB_per_s": achieved, "peak": peak, "peak_source": peak_kind,
+           "frac": None if in_l2 else achieved / peak,
+           "bound": "latency (inputs stay in L2)" if in_l2 else "hbm",
+           "traffic": recorded_traffic(name), "clocks": clocks,
+           "gpu_launches": 2 * steps}
+    del step, inp
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_aux(w, inp, dev, stream, reps=50):
@@ -549,6 +617,7 @@ def run_e2e(args, w, inp, dev, stream, step0):
     one(0)
     one(1)
     torch.cuda.synchronize(dev)
+    link = host_link(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(s_cmp)
     s_in.wait_event(t0)
@@ -568,9 +637,32 @@ def run_e2e(args, w, inp, dev, stream, step0):
             "results": "loss statistics, per-token logp and entropy; dlogits stays on the "
                        "device for the backward pass",
             "pipeline": "double-buffered: upload of step i+1 beside compute of step i",
-            "host_link": "measured ~211 GB/s host-to-device on this GPU (copy engines and "
-                         "zero-copy loads alike)",
+            "effective_h2d_GB_per_s": h2d / (ms / 1e3) / 1e9,
+            "host_link": link,
             "loss_last_step": st["loss"]}
+
+
+def host_link(dev, nbytes=1 << 30, reps=3):
+    """Host<->device copy rate of this machine, timed in this run: a 1 GiB pinned
+    buffer copied each way with CUDA events (best of `reps`)."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, dst, src in (("h2d_GB_per_s", d, h), ("d2h_GB_per_s", h, d)):
+        best = float("inf")
+        for _ in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        out[name] = nbytes / (best / 1e3) / 1e9
+    out["how"] = f"{nbytes >> 20} MiB pinned copy each way, best of {reps} after one warm-up"
+    del h, d
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -642,11 +734,12 @@ def _sample_text(w, s, threads, extra=""):
             f"{extra}; fp64 C oracle on {threads} host threads")
 
 
-def cpu_baseline(w, dev_logits=None, budget_s=15.0, n_rows=512):
-    """The oracle as it stands, timed on the host cores over a bounded sample."""
+def cpu_baseline(w, dev_logits=None, budget_s=15.0, n_rows=512, threads=None):
+    """The oracle as it stands, timed on the host cores over a bounded sample
+    (all of the process's host threads unless ``threads`` is given)."""
     import oracle
 
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     s = cpu_sample(w, sample_rows(w, n_rows), dev_logits)
     t0 = time.time()
     done = 0
@@ -658,6 +751,25 @@ def cpu_baseline(w, dev_logits=None, budget_s=15.0, n_rows=512):
     dt = time.time() - t0
     return {"value": done / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": _sample_text(w, s, threads, f", repeated for {dt:.1f} s")}
+
+
+def cpu_baselines(w, name, dev_logits=None, budget_s=15.0):
+    """The oracle on the host cores in two settings, all host threads and one
+    thread, for the timed workload (its all-thread figure is the line's
+    cpu_baseline) and, on smaller samples, for every other workload."""
+    from ppo_policy_loss_gb300 import synth
+
+    out = cpu_baseline(w, dev_logits, budget_s=0.4 * budget_s)
+    out["one_thread"] = cpu_baseline(w, dev_logits, budget_s=0.15 * budget_s, n_rows=64, threads=1)
+    per = {}
+    others = [n for n in OTHER_WORKLOADS + (WORKLOAD,) if n != name]
+    for other in others:
+        wk = synth.WORKLOADS[other]
+        b = 0.45 * budget_s / (2 * len(others))
+        per[other] = {"all_threads": cpu_baseline(wk, None, budget_s=b, n_rows=64),
+                      "one_thread": cpu_baseline(wk, None, budget_s=b, n_rows=16, threads=1)}
+    out["other_workloads"] = per
+    return out
 
 
 def run_reference(args):
@@ -899,6 +1011,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other workloads after the headline")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip timing the O(B*T) kernels beside the loss")
     ap.add_argument("--global-token-mean", action="store_true",

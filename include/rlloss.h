@@ -305,6 +305,18 @@ typedef struct {
   float* partials_out;           /* launch 1: float[4 * B * T], device */
   const float* shard_partials;   /* launch 2: float[4 * n_shards * B * T], device */
   int n_shards;                  /* launch 2: >= 1 */
+  /* Launch 2 only (shard_partials != NULL), nullable: each row's gradient
+   * coefficients float[4] = (cL, a0, a1, gy) at row_coef_out[4 * row], with
+   * which the row's gradient is
+   *   dz_v = 2^x (a0 + a1 x) - [v == y] gy,   x = z_v log2(e) - cL,
+   * where cL = (max z) log2(e) + log2(sum 2^(..)), a0 = s (g + c_ent H),
+   * a1 = s c_ent ln 2 and gy = s g, s being the row's gradient scale
+   * (grad_scale w_t); all four are 0 on masked rows.  This is how the
+   * tensor-core LM-head backward (rl_lmhead_dlogits) forms the gradient
+   * without the logits: the row statistics come from rl_lmhead_row_partials
+   * (one shard), and this launch may then have V = 0 columns of its own
+   * (logits, ld and dlogits unused; vocab_total > 0 gives the id range). */
+  float* row_coef_out;
 } rl_policy_loss_desc;
 
 /*
@@ -456,6 +468,92 @@ rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* wei
                              float* logp_out, float* entropy_out, float* lse_out,
                              unsigned int* status_dev, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/*
+ * rl_lmhead_logprobs with each row's partial softmax statistics as output,
+ * in the form the loss's merge launch takes (rl_policy_loss_desc
+ * .shard_partials with n_shards = 1): float[4] at partials_out[4 * r] =
+ *   (m, s, t, z_y) with m = max_v z_rv, s = sum_v 2^x, t = sum_v 2^x x,
+ *   x = (z_rv - m) log2(e), and z_y the sampled id's logit (-inf when ids[r]
+ *   is outside [0, V)),
+ * so lse = m + ln s and H = ln 2 (log2 s - t / s).  Same kernel, arguments,
+ * workspace, status bits and errors as rl_lmhead_logprobs; partials_out is
+ * device float[4 * R], 16-byte aligned (RL_ERR_NULL / RL_ERR_ALIGN).  This is
+ * the first step of the policy loss through the LM head without the logits:
+ * then the merge launch with row_coef_out, then rl_lmhead_dlogits,
+ * rl_lmhead_dhidden and rl_lmhead_dweight.
+ */
+rl_status rl_lmhead_row_partials(const void* hidden, long long ld_h, const void* weight,
+                                 long long ld_w, rl_dtype dtype, long long R, long long D,
+                                 long long V, const long long* ids, float* partials_out,
+                                 unsigned int* status_dev, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * The loss gradient with respect to the LM-head logits, formed from the
+ * hidden states on the tensor cores without the logits ever being written:
+ * the logits tile z = hidden . W^T (fp32 accumulation of the 16-bit
+ * products, as for rl_lmhead_logprobs) is recomputed in tensor memory and
+ * the epilogue writes, for each row r < R and column v < V,
+ *   dlogits[r, v] = 2^x (a0 + a1 x) - [v == ids[r]] gy,   x = z_rv log2(e) - cL
+ * rounded to `dtype`, with (cL, a0, a1, gy) = row_coef[4 * r .. 4 * r + 3] the
+ * row's coefficients from the loss's merge launch (rl_policy_loss_desc
+ * .row_coef_out).  That is the fused loss's gradient
+ *   s [ g (p_v - [v = y]) + c_ent p_v (log p_v + H) ]
+ * (the pages' PPO update kernel: ainews.cool RL.cu article, section
+ * "技术深度解析", bullet "PPO 更新内核"; the actor's own matrix multiplication:
+ * the same section's policy and value networks bullet).  A row whose a0 and
+ * a1 are both 0 (masked rows) gets only the -gy term (0 for masked rows).
+ *   hidden, weight, ids : as rl_lmhead_logprobs;
+ *   row_coef : float[4 * R] device, 16-byte aligned, read only;
+ *   dlogits  : [R, ld_dz] of `dtype`, device, 16-byte aligned, ld_dz >= V a
+ *              multiple of 8 elements; columns V .. ld_dz-1 are not written;
+ *   status_dev : as rl_lmhead_logprobs (RL_DEVERR_TIMEOUT).
+ * One launch of a persistent tensor-core kernel (tcgen05, TMA, tensor
+ * memory); allocates nothing; stream-ordered.  Errors: RL_ERR_DTYPE,
+ * RL_ERR_SHAPE (R < 0, R >= 2^31, V < 1, V >= 2^31, D < 8 or not a multiple
+ * of 8, a stride below its row or not a multiple of 8 elements), RL_ERR_NULL,
+ * RL_ERR_ALIGN, RL_ERR_CUDA.  R == 0 launches nothing.
+ */
+rl_status rl_lmhead_dlogits(const void* hidden, long long ld_h, const void* weight, long long ld_w,
+                            rl_dtype dtype, long long R, long long D, long long V,
+                            const long long* ids, const float* row_coef, void* dlogits,
+                            long long ld_dz, unsigned int* status_dev, void* stream);
+
+/*
+ * Gradient with respect to the hidden states through the LM head:
+ *   dhidden[r, d] = sum_v dlogits[r, v] weight[v, d]
+ * (the backward of the actor's LM-head matrix multiplication, ainews.cool
+ * RL.cu article, section "技术深度解析", policy and value networks bullet),
+ * on the tensor cores with fp32 accumulation of the exact 16-bit products,
+ * rounded once to `dtype`.
+ *   dlogits : [R, ld_dz] of `dtype`, device, read only (ld_dz >= V);
+ *   weight  : [V, ld_w] of `dtype`, device, read only (ld_w >= D);
+ *   dhidden : [R, ld_dh] of `dtype`, device, written (ld_dh >= D);
+ *   strides multiples of 8 elements, bases 16-byte aligned; status_dev as
+ *   rl_lmhead_logprobs.  Errors as rl_lmhead_dlogits.  R == 0 launches nothing.
+ */
+rl_status rl_lmhead_dhidden(const void* dlogits, long long ld_dz, const void* weight, long long ld_w,
+                            rl_dtype dtype, long long R, long long D, long long V, void* dhidden,
+                            long long ld_dh, unsigned int* status_dev, void* stream);
+
+/*
+ * Gradient with respect to the LM-head weight:
+ *   dweight[v, d] (+)= sum_r dlogits[r, v] hidden[r, d]
+ * (the same backward, for the weight), on the tensor cores with fp32
+ * accumulation of the exact 16-bit products; fp32 output.  accumulate != 0
+ * adds the product to what dweight holds (a batch taken in chunks of rows),
+ * 0 overwrites it.
+ *   dlogits : [R, ld_dz] of `dtype`, device, read only;
+ *   hidden  : [R, ld_h] of `dtype`, device, read only;
+ *   dweight : float [V, ld_dw], device, 16-byte aligned, ld_dw >= D a
+ *             multiple of 4;
+ *   status_dev as rl_lmhead_logprobs.  Errors as rl_lmhead_dlogits.  R == 0
+ *   leaves dweight as it is (accumulate) or zero (overwrite).
+ */
+rl_status rl_lmhead_dweight(const void* dlogits, long long ld_dz, const void* hidden, long long ld_h,
+                            rl_dtype dtype, long long R, long long D, long long V, float* dweight,
+                            long long ld_dw, int accumulate, unsigned int* status_dev, void* stream);
 
 /*
  * Workspace bytes rl_lmhead_logprobs needs for its best work split of R rows

@@ -501,3 +501,38 @@ def lmhead_row_stats(hidden, weight, ids, dtype="bf16", threads=None):
     logits = Hm @ Wm.T
     ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
     return row_stats(logits, F64, Wm.shape[0], ids, np.ones(logits.shape[0], np.uint8), threads)
+
+
+def lmhead_logits(hidden, weight, dtype="bf16"):
+    """Logits = hidden @ weight^T in float64 on the exactly decoded 16-bit
+    inputs (a library matmul), never rounded.  hidden [R, D], weight [V, D]."""
+    Hm = decode(np.ascontiguousarray(hidden), dtype)
+    Wm = decode(np.ascontiguousarray(weight), dtype)
+    return Hm @ Wm.T
+
+
+def lmhead_policy_loss(hidden, weight, dtype, ids, mask, adv_row, logp_old=None, ref_logp=None,
+                       eps=0.2, beta=0.0, c_ent=0.0, grad_scale=1.0, eps_high=None,
+                       agg="token_mean", T=None, agg_norm=None, threads=None):
+    """The policy loss from hidden states and its gradients, all in float64.
+
+    The actor's logits are its LM-head projection (ainews.cool RL.cu article,
+    "技术深度解析", policy and value networks bullet), so by the chain rule
+      z  = hidden @ W^T                         (lmhead_logits)
+      dz = dL/dz  of policy_loss on z           (row_stats, loss_from_stats,
+                                                 dlogits_rows with no rounding)
+      dhidden = dz @ W,   dW = dz^T @ hidden    (library matmuls)
+    with every step the plain definition and nothing rounded.  Returns the
+    policy_loss outputs plus z, dz (float64 [R, V]), dhidden and dweight.
+    """
+    z = lmhead_logits(hidden, weight, dtype)
+    R, V = z.shape
+    m = np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
+    ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+    out = policy_loss(z, F64, V, ids, m, adv_row, logp_old, ref_logp, eps, beta, c_ent,
+                      grad_scale, None, F64, threads, eps_high, agg, T, agg_norm)
+    dz = out["dlogits"]
+    Hm = decode(np.ascontiguousarray(hidden), dtype)
+    Wm = decode(np.ascontiguousarray(weight), dtype)
+    out.update(z=z, dz=dz, dhidden=dz @ Wm, dweight=dz.T @ Hm)
+    return out

@@ -68,7 +68,7 @@ class rl_policy_loss_desc(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("global_counts", ctypes.c_void_p),
                 ("vocab_offset", ctypes.c_longlong), ("vocab_total", ctypes.c_longlong),
                 ("partials_out", ctypes.c_void_p), ("shard_partials", ctypes.c_void_p),
-                ("n_shards", ctypes.c_int)]
+                ("n_shards", ctypes.c_int), ("row_coef_out", ctypes.c_void_p)]
 
 
 class rl_value_stats(ctypes.Structure):
@@ -116,6 +116,13 @@ def load(path: str | None = None):
     lib.rl_count_tokens.restype = I
     lib.rl_masked_whiten.restype = I
     lib.rl_lmhead_logprobs.restype = I
+    lib.rl_lmhead_row_partials.argtypes = [P, LL, P, LL, I, LL, LL, LL, P, P, P, P, SZ, P]
+    lib.rl_lmhead_dlogits.argtypes = [P, LL, P, LL, I, LL, LL, LL, P, P, P, LL, P, P]
+    lib.rl_lmhead_dhidden.argtypes = [P, LL, P, LL, I, LL, LL, LL, P, LL, P, P]
+    lib.rl_lmhead_dweight.argtypes = [P, LL, P, LL, I, LL, LL, LL, P, LL, I, P, P]
+    for fn in ("rl_lmhead_row_partials", "rl_lmhead_dlogits", "rl_lmhead_dhidden",
+               "rl_lmhead_dweight"):
+        getattr(lib, fn).restype = I
     lib.rl_policy_loss_launch_shape.argtypes = [I, LL, LL, ctypes.POINTER(I), ctypes.POINTER(I),
                                                 ctypes.POINTER(I)]
     lib.rl_read_device_status.argtypes = [P, P]
@@ -244,6 +251,37 @@ def rl_lmhead_logprobs(hidden, ld_h, weight, ld_w, dtype, R, D, V, ids, logp_out
                                      _ptr(ids), _ptr(logp_out), _ptr(entropy_out), _ptr(lse_out),
                                      _ptr(status_dev), _ptr(workspace), workspace_bytes,
                                      _stream(stream)), "rl_lmhead_logprobs")
+
+
+def rl_lmhead_row_partials(hidden, ld_h, weight, ld_w, dtype, R, D, V, ids, partials_out,
+                           status_dev=None, workspace=None, workspace_bytes=0, stream=None):
+    if workspace is not None and hasattr(workspace, "numel") and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().rl_lmhead_row_partials(_ptr(hidden), ld_h, _ptr(weight), ld_w, _dtype(dtype), R, D,
+                                         V, _ptr(ids), _ptr(partials_out), _ptr(status_dev),
+                                         _ptr(workspace), workspace_bytes, _stream(stream)),
+           "rl_lmhead_row_partials")
+
+
+def rl_lmhead_dlogits(hidden, ld_h, weight, ld_w, dtype, R, D, V, ids, row_coef, dlogits, ld_dz,
+                      status_dev=None, stream=None):
+    _check(load().rl_lmhead_dlogits(_ptr(hidden), ld_h, _ptr(weight), ld_w, _dtype(dtype), R, D, V,
+                                    _ptr(ids), _ptr(row_coef), _ptr(dlogits), ld_dz,
+                                    _ptr(status_dev), _stream(stream)), "rl_lmhead_dlogits")
+
+
+def rl_lmhead_dhidden(dlogits, ld_dz, weight, ld_w, dtype, R, D, V, dhidden, ld_dh,
+                      status_dev=None, stream=None):
+    _check(load().rl_lmhead_dhidden(_ptr(dlogits), ld_dz, _ptr(weight), ld_w, _dtype(dtype), R, D, V,
+                                    _ptr(dhidden), ld_dh, _ptr(status_dev), _stream(stream)),
+           "rl_lmhead_dhidden")
+
+
+def rl_lmhead_dweight(dlogits, ld_dz, hidden, ld_h, dtype, R, D, V, dweight, ld_dw, accumulate,
+                      status_dev=None, stream=None):
+    _check(load().rl_lmhead_dweight(_ptr(dlogits), ld_dz, _ptr(hidden), ld_h, _dtype(dtype), R, D, V,
+                                    _ptr(dweight), ld_dw, int(accumulate), _ptr(status_dev),
+                                    _stream(stream)), "rl_lmhead_dweight")
 
 
 def rl_lmhead_workspace_size(R, V) -> int:

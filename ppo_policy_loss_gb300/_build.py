@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "librlloss.so")
-SOURCES = ["policy_loss.cu", "advantages.cu", "critic.cu", "status.cu", "lmhead.cu"]
+SOURCES = ["policy_loss.cu", "advantages.cu", "critic.cu", "status.cu", "lmhead.cu", "lmhead_grad.cu"]
 # (object, source, extra flags): policy_loss.cu builds a second time with the
 # short-row configuration of the loss kernel.
 UNITS = [(src.replace(".cu", ".o"), src, []) for src in SOURCES] + [

@@ -40,7 +40,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "rl_device.cuh"
+#include "tc_device.cuh"
 
 namespace rl {
 namespace {
@@ -76,64 +76,9 @@ struct LmArgs {
   float* logp_out;
   float* entropy_out;
   float* lse_out;
+  float4* row_partials;  // nullable: each row's (max, sum 2^x, sum 2^x x, sampled logit)
   unsigned int* status;  // nullable: RL_DEVERR_* bits
 };
-
-// ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem] . B[smem]^T, bf16 in, fp32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // First vocabulary tile of slice vs when n_nt tiles are cut into n_sl slices.
 __device__ __forceinline__ int slice_begin(int vs, int n_nt, int n_sl) {
@@ -154,49 +99,12 @@ __device__ __forceinline__ void unit_coords(int u, int n_mt, int n_sl, int g, in
   mt = base + within % gc;
 }
 
-// v[j] through a tree of selects on the bits of j (constant register
-// indices only, so v stays in registers).
-__device__ __forceinline__ float select32(const float (&v)[32], int j) {
-  float h[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) h[i] = (j & 16) ? v[i + 16] : v[i];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) h[i] = (j & 8) ? h[i + 8] : h[i];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = (j & 4) ? h[i + 4] : h[i];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) h[i] = (j & 2) ? h[i + 2] : h[i];
-  return (j & 1) ? h[1] : h[0];
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 B, 8-row (1024 B) swizzle atoms.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);     // start address
-  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: one 8-row atom
-  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: fp32 D, A and B both bf16 (format 1) or both fp16
-// (format 0), both K-major, M x N.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
-}
+// Instruction descriptor: fp32 D, A and B both bf16 or both fp16, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16) { return make_idesc_f16(bf16, kBM, kBN, false, false); }
 
 template <bool kDrain>
 __device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  if (kDrain) {
-    const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-      if (global_ns() - t0 > kWaitLimitNs) return false;
-    return true;
-  }
-  return wait_bounded<false>(bar, parity, abort);
+  return tc_wait<kDrain>(bar, parity, abort);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -287,7 +195,7 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
             const uint32_t a_base = smem_addr(sm.a[s]), b_base = smem_addr(sm.b[s]);
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
-              umma_bf16(d_tmem, smem_desc_sw128(a_base + k * kUmmaK * 2), smem_desc_sw128(b_base + k * kUmmaK * 2),
+              umma_f16(d_tmem, smem_desc_sw128(a_base + k * kUmmaK * 2), smem_desc_sw128(b_base + k * kUmmaK * 2),
                         a.idesc, (kb | k) != 0);
             issued = true;
             umma_commit(smem_addr(&sm.empty[s]));  // the stage is free once these MMAs have read it
@@ -408,6 +316,7 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
         if (a.logp_out) a.logp_out[row] = y_ok ? zy - lse : __int_as_float(0x7fc00000);
         if (a.entropy_out) a.entropy_out[row] = H;
         if (a.lse_out) a.lse_out[row] = lse;
+        if (a.row_partials) a.row_partials[row] = make_float4(m, S, Tt, zy);
         if (!y_ok && a.status) atomicOr(a.status, RL_DEVERR_ID_RANGE);
       }
     }
@@ -424,40 +333,15 @@ lmhead_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_
 }
 
 // ------------------------------------------------------------------ host side
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 std::mutex g_lm_mu;
-EncodeTiled g_encode = nullptr;
 int g_lm_attr_dev = -1;
 
-rl_status encode_fn(EncodeTiled* out) {
-  std::lock_guard<std::mutex> lock(g_lm_mu);
-  if (!g_encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return RL_ERR_CUDA;
-    g_encode = reinterpret_cast<EncodeTiled>(fn);
-  }
-  *out = g_encode;
-  return RL_OK;
-}
+rl_status encode_fn(EncodeTiled* out) { return tc_encode_fn(out); }
 
-// 2-D bf16 tensor map [rows, cols] (row stride ld elements), box box_rows x 64, 128B swizzle.
+// 2-D tensor map [rows, cols] (row stride ld elements), box box_rows x 64, 128B swizzle.
 bool make_map(EncodeTiled enc, CUtensorMap* map, CUtensorMapDataType dt, const void* base, long long rows,
-              long long cols, long long ld,
-              uint32_t box_rows) {
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              long long cols, long long ld, uint32_t box_rows) {
+  return tc_make_map(enc, map, dt, base, rows, cols, ld, kBK, box_rows);
 }
 
 // Work split: S vocabulary slices per 128-row tile, chosen to minimise the
@@ -511,13 +395,7 @@ LmPlan lm_plan(long long R, long long V, long long D, int sms, size_t ws_cap) {
   return p;
 }
 
-rl_status device_sms(int* sms) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || *sms < 1)
-    return RL_ERR_CUDA;
-  return RL_OK;
-}
+rl_status device_sms(int* sms) { return tc_device_sms(sms); }
 
 bool lm_shape_ok(long long R, long long V) { return R >= 0 && R < (1LL << 31) && V >= 1 && V <= (1LL << 31); }
 
@@ -545,12 +423,11 @@ extern "C" rl_status rl_lmhead_plan(long long R, long long D, long long V, size_
   return RL_OK;
 }
 
-extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
-                                        rl_dtype dtype, long long R, long long D, long long V,
-                                        const long long* ids,
-                                        float* logp_out, float* entropy_out, float* lse_out,
-                                        unsigned int* status_dev, void* workspace, size_t workspace_bytes,
-                                        void* stream) {
+namespace {
+rl_status lmhead_launch(const void* hidden, long long ld_h, const void* weight, long long ld_w, rl_dtype dtype,
+                        long long R, long long D, long long V, const long long* ids, float* logp_out,
+                        float* entropy_out, float* lse_out, float4* row_partials, unsigned int* status_dev,
+                        void* workspace, size_t workspace_bytes, void* stream) {
   using namespace rl;
   if (dtype != RL_BF16 && dtype != RL_F16) return RL_ERR_DTYPE;
   if (!lm_shape_ok(R, V) || D < 8 || D % 8 != 0 || ld_h < D || ld_w < D) return RL_ERR_SHAPE;
@@ -596,7 +473,30 @@ extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, cons
   args.logp_out = logp_out;
   args.entropy_out = entropy_out;
   args.lse_out = lse_out;
+  args.row_partials = row_partials;
   args.status = status_dev;
   lmhead_logprobs_kernel<<<plan.grid, kThreadsL, smem, static_cast<cudaStream_t>(stream)>>>(mh, mw, args);
   return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" rl_status rl_lmhead_logprobs(const void* hidden, long long ld_h, const void* weight, long long ld_w,
+                                        rl_dtype dtype, long long R, long long D, long long V,
+                                        const long long* ids,
+                                        float* logp_out, float* entropy_out, float* lse_out,
+                                        unsigned int* status_dev, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  return lmhead_launch(hidden, ld_h, weight, ld_w, dtype, R, D, V, ids, logp_out, entropy_out, lse_out, nullptr,
+                       status_dev, workspace, workspace_bytes, stream);
+}
+
+extern "C" rl_status rl_lmhead_row_partials(const void* hidden, long long ld_h, const void* weight,
+                                            long long ld_w, rl_dtype dtype, long long R, long long D,
+                                            long long V, const long long* ids, float* partials_out,
+                                            unsigned int* status_dev, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  if (R > 0 && !partials_out) return RL_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(partials_out) & 15) return RL_ERR_ALIGN;
+  return lmhead_launch(hidden, ld_h, weight, ld_w, dtype, R, D, V, ids, nullptr, nullptr, nullptr,
+                       reinterpret_cast<float4*>(partials_out), status_dev, workspace, workspace_bytes, stream);
 }

@@ -167,6 +167,7 @@ struct LossArgs {
   float4* partials_out;            // shard partials, pass-1 launch
   const float4* shard_partials;    // [n_shards][R] gathered partials, merge launch
   int n_shards;
+  float4* row_coef_out;            // merge launch: (cL, a0, a1, gy) per row, or null
 };
 
 // ------------------------------------------------------------------ element formats
@@ -594,7 +595,10 @@ __device__ __forceinline__ float warp_group_advantage(const LossArgs& a, long lo
 // otherwise each CTA's slice of a row stays in the ring for both passes.
 // kMode: 0 the whole loss; 1 (vocabulary shard) pass 1 only, writing each
 // row's partial statistics; 2 (vocabulary shard) merge the gathered shard
-// partials instead of pass 1, then the loss and this shard's gradient.
+// partials instead of pass 1, then the loss and this shard's gradient; 3 the
+// merge of mode 2 with no columns at all (each row's gradient coefficients
+// are its only per-row output besides logp and entropy): nothing is shared
+// between the warps of a row then, so every consumer warp takes its own rows.
 template <int DT, bool kStream, int kMode, bool kEnt>
 __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(const LossArgs a) {
   using E = Elem<DT>;
@@ -696,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
     const volatile long long* pace = &sm.pace;
     RowWalk<false> walk(cid, ncl);
     for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R; row = walk.next(a.mask, ncl, a.R, lane)) {
-      if (*pace < row - kZeroLead * static_cast<long long>(ncl)) {  // bounded wait, then go on
+      if (kMode != 3 && *pace < row - kZeroLead * static_cast<long long>(ncl)) {  // bounded wait, then go on
         const uint64_t t0 = global_ns();
         while (*pace < row - kZeroLead * static_cast<long long>(ncl) && global_ns() - t0 < kWaitLimitNs)
           __nanosleep(500);
@@ -714,13 +718,17 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       if (rank == 0 && lane == 0) {
         if (a.logp_out) a.logp_out[row] = 0.f;
         if (a.entropy_out) a.entropy_out[row] = 0.f;
+        if (kMode >= 2 && a.row_coef_out) a.row_coef_out[row] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     if (lane == 0) bulk_wait_all();  // the block is read until the last copy is done
   } else {
     // ---------------------------------------------------------------- consumers
-    RowWalk<true> walk(cid, ncl);  // the valid rows of this CTA
-    long long nrow = walk.next(a.mask, ncl, a.R, lane);
+    // the valid rows of this CTA (mode 3: of this warp)
+    const long long rfirst = kMode == 3 ? static_cast<long long>(cid) * kConsumerWarps + warp : cid;
+    const long long rstride = kMode == 3 ? static_cast<long long>(ncl) * kConsumerWarps : ncl;
+    RowWalk<true> walk(rfirst, rstride);
+    long long nrow = walk.next(a.mask, rstride, a.R, lane);
     RowScalars cur = load_row(a, nrow);  // in flight while the mask is counted
 
     // N = number of valid tokens; every CTA counts the whole mask.
@@ -770,10 +778,11 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
     unsigned int err = 0;
     uint32_t it = 0, vrow = 0;
     bool aborted = false;
+    double wacc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // mode 3: this warp's sums (lane 0)
 
     for (long long row = nrow; row < a.R; row = nrow) {  // masked rows: the zero warp
-      if (tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = row;
-      nrow = walk.next(a.mask, ncl, a.R, lane);
+      if (kMode != 3 && tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = row;
+      nrow = walk.next(a.mask, rstride, a.R, lane);
       const RowScalars rs = cur;
       cur = load_row(a, nrow);  // next row's scalars, in flight during this row
       unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes + lo * E::kBytes : nullptr;
@@ -813,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
 
       const uint32_t base = it;
       float M = -INFINITY, S = 0.f, Tt = 0.f, zyr = -INFINITY;
-      if constexpr (kMode != 2) {
+      if constexpr (kMode < 2) {
         // ---- pass 1: online statistics of this thread's share of the slice
         ThreadStats st;
         stats_init(st);
@@ -942,12 +951,13 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         J = logp;
         g = logp;
       }
-      if (rank == 0 && tid == 0) {
-        sm.acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(J) : w_row * J;
-        sm.acc[1] += pg;
-        sm.acc[2] += kl;
-        sm.acc[3] += H;
-        sm.acc[4] += clipped ? 1.0 : 0.0;
+      if (rank == 0 && (kMode == 3 ? lane == 0 : tid == 0)) {
+        double* acc = kMode == 3 ? wacc : sm.acc;
+        acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(J) : w_row * J;
+        acc[1] += pg;
+        acc[2] += kl;
+        acc[3] += H;
+        acc[4] += clipped ? 1.0 : 0.0;
         if (!y_ok) err |= RL_DEVERR_ID_RANGE;
         if (a.logp_out) a.logp_out[row] = logp;
         if (a.entropy_out) a.entropy_out[row] = H;
@@ -959,6 +969,8 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       const float a0 = sc_row * fmaf(a.c_ent, H, g);
       const float a1 = sc_row * a.c_ent * kLn2;
       const float gy = sc_row * g;
+      if (kMode >= 2 && a.row_coef_out && rank == 0 && (kMode == 3 ? lane == 0 : tid == 0))
+        a.row_coef_out[row] = make_float4(cL, a0, a1, gy);
       for (int c = 0; c < nchunks; ++c) {
         uint32_t slot;
         if (kStream) {
@@ -1034,6 +1046,20 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       ++vrow;
     }
     if (tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = a.R + 1;  // release the zero warp
+    if constexpr (kMode == 3) {  // the warps' sums, combined in warp order
+      if (lane == 0) {
+        for (int k = 0; k < 5; ++k) sm.wred[warp][k] = wacc[k];
+        if (err) {
+          atomicOr(&a.ws->status, err);
+          __threadfence();
+        }
+      }
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      if (tid == 0)
+        for (int w = 0; w < kConsumerWarps; ++w)
+          for (int k = 0; k < 5; ++k) sm.acc[k] += sm.wred[w][k];
+      err = 0;
+    }
 
     // ---- per-CTA partial, then the last CTA reduces all partials in CTA order
     if (tid == 0) {
@@ -1145,6 +1171,8 @@ void* kernel_for_mode(rl_dtype dt, bool stream) {
 }
 
 void* kernel_for(rl_dtype dt, bool stream, int mode, bool ent) {
+  // no columns: the element format and row layout do not matter
+  if (mode == 3) return reinterpret_cast<void*>(&RL_LOSS_KERNEL<RL_BF16, false, 3, false>);
   if (mode == 1) return kernel_for_mode<1, false>(dt, stream);
   if (mode == 2) return ent ? kernel_for_mode<2, true>(dt, stream) : kernel_for_mode<2, false>(dt, stream);
   return ent ? kernel_for_mode<0, true>(dt, stream) : kernel_for_mode<0, false>(dt, stream);
@@ -1193,7 +1221,7 @@ rl_status max_clusters(rl_dtype dt, bool stream, int cluster, int mode, int* out
 rl_status plan(rl_dtype dt, long long V, long long R, Plan* p, int mode = 0) {
   const int es = elem_bytes(dt);
   if (es == 0) return RL_ERR_DTYPE;
-  if (V < 1 || R < 0) return RL_ERR_SHAPE;
+  if (V < (mode >= 2 ? 0 : 1) || R < 0) return RL_ERR_SHAPE;
   if (!choose_layout(es, V, p)) return RL_ERR_SHAPE;
   int occ = 0;
   const rl_status st = max_clusters(dt, p->stream, p->cluster, mode, &occ);
@@ -1216,6 +1244,7 @@ using namespace rl;
 namespace {
 template <int DT, bool S>
 cudaError_t launch_one(cudaLaunchConfig_t* cfg, int mode, bool ent, const LossArgs& args) {
+  if (mode == 3) return cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<RL_BF16, false, 3, false>, args);
   if (mode == 1) return cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 1, false>, args);
   if (mode == 2)
     return ent ? cudaLaunchKernelEx(cfg, RL_LOSS_KERNEL<DT, S, 2, true>, args)
@@ -1254,12 +1283,17 @@ RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream) {
       d->agg != RL_AGG_SEQ_MEAN_TOKEN_SUM && d->agg != RL_AGG_TOKEN_SUM_NORM)
     return RL_ERR_DTYPE;
   const long long B = d->B, T = d->T, V = d->V, ld = d->ld;
-  if (B < 0 || T < 0 || V < 1 || ld < V) return RL_ERR_SHAPE;
+  // A merge launch that only writes row coefficients may have no columns of its own.
+  const bool coef_only = d->shard_partials && d->row_coef_out && V == 0;
+  if (coef_only && d->vocab_total < 1) return RL_ERR_SHAPE;
+  if (B < 0 || T < 0 || V < (coef_only ? 0 : 1) || ld < V) return RL_ERR_SHAPE;
   if (B > 0 && T > (1LL << 40) / B) return RL_ERR_SHAPE;
   const long long R = B * T;
   if (!d->stats_dev) return RL_ERR_NULL;
   if (!d->workspace || d->workspace_bytes < kWorkspaceBytes) return RL_ERR_WORKSPACE;
-  if (R > 0 && (!d->logits || !d->ids || !d->mask || !d->adv)) return RL_ERR_NULL;
+  if (R > 0 && ((!d->logits && !coef_only) || !d->ids || !d->mask || !d->adv)) return RL_ERR_NULL;
+  if (d->row_coef_out && !d->shard_partials) return RL_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(d->row_coef_out) & 15) != 0) return RL_ERR_ALIGN;
   if (d->beta != 0.f && !d->ref_logp) return RL_ERR_NULL;
   if (!finite(d->eps) || d->eps < 0.f || !finite(d->eps_high) || !finite(d->beta) ||
       !finite(d->c_ent) || !finite(d->grad_scale))
@@ -1271,12 +1305,12 @@ RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream) {
   }
   if (d->agg == RL_AGG_TOKEN_SUM_NORM && !(d->agg_norm > 0.0 && std::isfinite(d->agg_norm)))
     return RL_ERR_ARG;
-  // vocabulary shards
-  const int mode = d->partials_out ? 1 : d->shard_partials ? 2 : 0;
+  // vocabulary shards; a merge launch with no columns of its own runs warp-parallel rows
+  const int mode = d->partials_out ? 1 : d->shard_partials ? (coef_only ? 3 : 2) : 0;
   const long long v_total = d->vocab_total > 0 ? d->vocab_total : V;
   if (d->partials_out && d->shard_partials) return RL_ERR_ARG;
   if (d->vocab_offset < 0 || d->vocab_total < 0 || d->vocab_offset + V > v_total) return RL_ERR_SHAPE;
-  if (mode == 2 && d->n_shards < 1) return RL_ERR_ARG;
+  if (mode >= 2 && d->n_shards < 1) return RL_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(d->partials_out) & 15) != 0 ||
       (reinterpret_cast<uintptr_t>(d->shard_partials) & 15) != 0)
     return RL_ERR_ALIGN;
@@ -1331,7 +1365,9 @@ RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream) {
   args.v_total = v_total;
   args.partials_out = reinterpret_cast<float4*>(d->partials_out);
   args.shard_partials = reinterpret_cast<const float4*>(d->shard_partials);
-  args.n_shards = mode == 2 ? d->n_shards : 0;
+  args.n_shards = mode >= 2 ? d->n_shards : 0;
+  args.row_coef_out = reinterpret_cast<float4*>(d->row_coef_out);
+  if (coef_only) args.dlogits = nullptr;
   if (mode == 1) {  // statistics only
     args.dlogits = nullptr;
     args.logp_out = nullptr;

@@ -1,0 +1,210 @@
+// tc_device.cuh — 5th-generation tensor-core building blocks (sm_103a) shared
+// by the LM-head kernels: inline-PTX wrappers for 2-D TMA tile loads, tensor
+// memory allocation and loads, tcgen05.mma / commit, the shared-memory and
+// instruction descriptors of 128-byte-swizzled bf16/fp16 tiles, and the host
+// side that encodes TMA tensor maps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "rl_device.cuh"
+
+namespace rl {
+namespace {
+
+// ------------------------------------------------------------------ device
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] . B[smem]^T, 16-bit inputs (format in idesc), fp32 accumulate.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2-D TMA store of a box from this CTA's shared memory, added to the calling
+// thread's bulk group.  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+// Until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// v[j] through a tree of selects on the bits of j (constant register
+// indices only, so v stays in registers).
+__device__ __forceinline__ float select32(const float (&v)[32], int j) {
+  float h[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) h[i] = (j & 16) ? v[i + 16] : v[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = (j & 8) ? h[i + 8] : h[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = (j & 4) ? h[i + 4] : h[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) h[i] = (j & 2) ? h[i + 2] : h[i];
+  return (j & 1) ? h[1] : h[0];
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 B (64 elements along K), 8-row (1024 B)
+// swizzle atoms stacked along M/N (stride byte offset); the K extent of one
+// MMA (32 B) lies inside a row, so the leading byte offset is unused.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);     // start address
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: one 8-row atom
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Descriptor of an MN-major tile (M or N contiguous in memory) written by TMA
+// with the 128-byte swizzle: each 64-element (128 B) block along M/N is a
+// stack of 8-row (1024 B) swizzle atoms, one atom per 8 consecutive K.  The
+// leading byte offset steps between 64-element blocks along M/N, the stride
+// byte offset between the 8-K atoms of a block.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64 along M/N
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                         // stride byte offset: next 8 along K
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 D; A and B both
+// bf16 (format 1) or both fp16 (format 0); bit 15 / 16 mark A / B as
+// MN-major (transposed) instead of K-major; N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <bool kDrain>
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (kDrain) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+  }
+  return wait_bounded<false>(bar, parity, abort);
+}
+
+// Row tile and column tile of work unit u.  Units come in groups of g row
+// tiles; inside a group the column index is the slow one, so the CTAs
+// working at one time share a column tile and touch at most g row tiles.
+// g = 1 puts the column tiles of one row tile next to each other instead.
+__device__ __forceinline__ void unit_tile(int u, int n_mt, int n_nt, int g, int& mt, int& nt) {
+  const int per_group = g * n_nt;
+  const int grp = u / per_group;
+  const int base = grp * g;
+  const int gc = min(g, n_mt - base);
+  const int within = u - grp * per_group;
+  nt = within / gc;
+  mt = base + within % gc;
+}
+
+// ------------------------------------------------------------------ host
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline rl_status tc_encode_fn(EncodeTiled* out) {
+  static std::mutex mu;
+  static EncodeTiled fn_cached = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fn_cached) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return RL_ERR_CUDA;
+    fn_cached = reinterpret_cast<EncodeTiled>(fn);
+  }
+  *out = fn_cached;
+  return RL_OK;
+}
+
+// 2-D tensor map of 16-bit elements over [rows, cols] (row stride ld
+// elements), box box_cols x box_rows, 128-byte swizzle (box_cols * 2 must be
+// 128), elements outside the tensor read as zero.
+inline bool tc_make_map(EncodeTiled enc, CUtensorMap* map, CUtensorMapDataType dt, const void* base, long long rows,
+                        long long cols, long long ld, uint32_t box_cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline rl_status tc_device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || *sms < 1)
+    return RL_ERR_CUDA;
+  return RL_OK;
+}
+
+}  // namespace
+}  // namespace rl

@@ -122,6 +122,58 @@ def policy_loss(logits: torch.Tensor, ids: torch.Tensor, mask: torch.Tensor, adv
                 workspace=workspace)
 
 
+def policy_loss_from_partials(partials: torch.Tensor, dtype: str, vocab: int, ids: torch.Tensor,
+                              mask: torch.Tensor, adv: torch.Tensor, B: int, T: int, logp_old=None,
+                              ref_logp=None, eps: float = 0.2, beta: float = 0.0, c_ent: float = 0.0,
+                              grad_scale: float = 1.0, logp_out="new", entropy_out="new",
+                              workspace=None, stats=None, stream=None,
+                              eps_high: float | None = None, agg: str = "token_mean",
+                              agg_norm: float = 1.0, group_size: int | None = None, ddof: int = 1,
+                              std_eps: float = 1e-4,
+                              global_counts: torch.Tensor | None = None) -> dict:
+    """The loss, its statistics, logp, entropy and each row's gradient
+    coefficients from per-row softmax statistics of a ``vocab``-column
+    vocabulary, without any logits: the merge launch of
+    rl_policy_loss_fwd_bwd_ex with no columns of its own (V = 0) and
+    ``row_coef_out``.  ``partials`` is float32 [B*T, 4] (one shard, e.g. from
+    rl_lmhead_row_partials) or [n_shards, B*T, 4]; ``dtype`` names the
+    16-bit format the gradient will be formed in.  Returns the outputs and
+    ``row_coef`` float32 [B*T, 4] (cL, a0, a1, gy) for rl_lmhead_dlogits."""
+    dev = partials.device
+    R = B * T
+    if partials.dim() == 2:
+        partials = partials[None]
+    if isinstance(logp_out, str):
+        logp_out = torch.empty(R, dtype=torch.float32, device=dev)
+    if isinstance(entropy_out, str):
+        entropy_out = torch.empty(R, dtype=torch.float32, device=dev)
+    coef = torch.empty((R, 4), dtype=torch.float32, device=dev)
+    workspace = new_workspace(R, dev) if workspace is None else workspace
+    stats = new_stats(dev) if stats is None else stats
+    if group_size is not None:
+        layout = RL_ADV_GROUP_REWARDS
+    else:
+        layout = RL_ADV_PER_TOKEN if adv.numel() == R and R != B else RL_ADV_PER_SEQ
+    d = rl_policy_loss_desc_init()
+    p = lambda t: t.data_ptr() if t is not None else None
+    d.logits, d.dtype, d.B, d.T, d.V, d.ld = None, DTYPES[dtype], B, T, 0, 0
+    d.ids, d.logp_old, d.ref_logp, d.mask, d.adv = p(ids), p(logp_old), p(ref_logp), p(mask), p(adv)
+    d.adv_layout = layout
+    if group_size is not None:
+        d.group_size, d.ddof, d.std_eps = group_size, ddof, std_eps
+    d.eps, d.eps_high = eps, (-1.0 if eps_high is None else eps_high)
+    d.beta, d.c_ent, d.grad_scale = beta, c_ent, grad_scale
+    d.agg, d.agg_norm = AGGREGATIONS[agg], agg_norm
+    d.dlogits, d.logp_out, d.entropy_out = None, p(logp_out), p(entropy_out)
+    d.stats_dev, d.workspace, d.workspace_bytes = p(stats), p(workspace), workspace.numel()
+    d.global_counts = p(global_counts)
+    d.vocab_offset, d.vocab_total = 0, vocab
+    d.shard_partials, d.n_shards = p(partials), partials.shape[0]
+    d.row_coef_out = p(coef)
+    rl_policy_loss_fwd_bwd_ex(d, stream)
+    return dict(logp=logp_out, entropy=entropy_out, stats=stats, row_coef=coef, workspace=workspace)
+
+
 def value_loss(values: torch.Tensor, returns: torch.Tensor, mask: torch.Tensor, values_old=None,
                clip_eps: float = -1.0, grad_scale: float = 1.0, dvalues="new", stream=None):
     """PPO clipped value loss (rl_value_loss_fwd_bwd); returns (dvalues, stats dict)."""

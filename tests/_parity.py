@@ -227,3 +227,21 @@ def ceil_div(a, b):
 
 
 __all__ = [n for n in dir() if not n.startswith("_")] + ["math"]
+
+
+def accumulation_bound(A: np.ndarray, B: np.ndarray, block: int = 16, u: float = 2.0 ** -24):
+    """Element-wise bound on |C - A @ B| for C an fp32 accumulation of the exact
+    products of A [M, K] and B [K, N] (fp64 arrays of 16-bit values, whose
+    products are exact in fp32), in K order, one block of `block` products
+    per step.  Each step rounds the running sum once: the error is at most u
+    times the sum of the magnitudes of the running sums after each step
+    (recursive summation), plus u times the sum of the products' magnitudes
+    for the rounding inside a step; both are doubled, allowing a unit that
+    truncates instead of rounding to nearest."""
+    K = A.shape[1]
+    S = np.zeros((A.shape[0], B.shape[1]))
+    run = np.zeros_like(S)
+    for k0 in range(0, K, block):
+        S += A[:, k0:k0 + block] @ B[k0:k0 + block]
+        run += np.abs(S)
+    return 2.0 * u * (run + np.abs(A) @ np.abs(B))

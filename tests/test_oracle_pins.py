@@ -643,3 +643,44 @@ def test_lmhead_one_hot_hidden_selects_weight_columns():
         assert abs(lse[r] - ref_lse) < 1e-12
         assert abs(logp[r] - (col[ids[r]] - ref_lse)) < 1e-12
         assert abs(H[r] + np.sum(p * np.log(p))) < 1e-12
+
+
+def test_lmhead_policy_loss_chain_rule_finite_differences():
+    """The oracle's gradients with respect to the hidden states and the LM-head
+    weight are the derivatives of its own loss: central differences of the
+    fp64 loss of hidden @ W^T in single entries of hidden and of W, with
+    clipped tokens, the KL and entropy terms and a sequence-mean aggregation.
+    A transposed product, a dropped term or a wrong sign fails this."""
+    rng = np.random.default_rng(93)
+    R, D, V, T = 6, 5, 11, 3
+    h = rng.normal(0, 1.0, (R, D))
+    W = rng.normal(0, 0.8, (V, D))
+    ids = rng.integers(0, V, R)
+    mask = np.array([1, 1, 0, 1, 1, 1], np.uint8)
+    adv = rng.normal(0, 1, R)
+    _, logp, _ = oracle.row_stats(h @ W.T, "f64", V, ids, mask, threads=1)
+    lo = logp + np.array([0.3, -0.25, 0.0, 0.02, -0.4, 0.1])   # some ratios beyond the clip
+    rf = logp + rng.normal(0, 0.2, R)
+    kw = dict(eps=0.2, beta=0.1, c_ent=0.05, agg="seq_mean_token_mean", T=T, threads=1)
+    base = oracle.lmhead_policy_loss(h, W, "f64", ids, mask, adv, lo, rf, **kw)
+    assert base["clipped"].any()
+    r = base["r"][mask != 0]
+    assert np.min(np.abs(np.concatenate([r - 0.8, r - 1.2]))) > 1e-3  # away from the kinks
+
+    def loss(hh, WW):
+        return oracle.lmhead_policy_loss(hh, WW, "f64", ids, mask, adv, lo, rf, **kw)["loss"]
+
+    step = 1e-6
+    for (i, j) in ((0, 0), (1, 3), (2, 2), (4, 4), (5, 1)):
+        hp, hm = h.copy(), h.copy()
+        hp[i, j] += step
+        hm[i, j] -= step
+        fd = (loss(hp, W) - loss(hm, W)) / (2 * step)
+        assert abs(fd - base["dhidden"][i, j]) < 1e-7, ("dhidden", i, j, fd, base["dhidden"][i, j])
+    for (v, j) in ((0, 0), (int(ids[0]), 2), (7, 4), (10, 1), (int(ids[4]), 3)):
+        Wp, Wm = W.copy(), W.copy()
+        Wp[v, j] += step
+        Wm[v, j] -= step
+        fd = (loss(h, Wp) - loss(h, Wm)) / (2 * step)
+        assert abs(fd - base["dweight"][v, j]) < 1e-7, ("dweight", v, j, fd, base["dweight"][v, j])
+    assert np.all(base["dhidden"][2] == 0)  # a masked row has no gradient

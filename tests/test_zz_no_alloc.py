@@ -57,8 +57,10 @@ def test_noalloc_matches_allocating_entry_point_twice():
     lib = rl.load()
     stream = torch.cuda.current_stream().cuda_stream
     runs = {}
+    keep = []  # the calls below take raw device pointers: keep every input tensor alive
     for name, (w, code) in CASES.items():
         logits, ids, mask, adv, lo, rf = _inputs(w)
+        keep.append((ids, mask, adv, lo, rf))
         common = (logits.data_ptr(), code, w.B, w.T, w.V, w.V, ids.data_ptr(), lo.data_ptr(),
                   rf.data_ptr(), mask.data_ptr(), adv.data_ptr(), rl.RL_ADV_PER_SEQ,
                   ctypes.c_float(w.eps), ctypes.c_float(w.beta), ctypes.c_float(w.c_ent),

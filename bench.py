@@ -969,6 +969,123 @@ def run_lmhead(args):
         print(json.dumps(out), flush=True)
 
 
+LMHEAD_TRAIN_METRIC = ("policy loss + gradients from hidden states through the LM head, rows/s "
+                       "(Qwen3 head, V=151936 bf16); % of tensor roofline")
+
+
+def run_lmhead_train(args):
+    """The training op from hidden states (lmhead_train.lmhead_policy_loss): the
+    forward row statistics, the loss launch, then per chunk the recomputed
+    gradient dz, dhidden and dweight, all on this library's kernels, on the
+    Qwen3-0.6B head over the GRPO workload's 32 x 1024 rows (its mask, ids and
+    rewards).  Four R x D x V products per step; each kernel is also timed
+    alone for its own roofline."""
+    import torch
+
+    import ppo_policy_loss_gb300 as rl
+    from ppo_policy_loss_gb300 import lmhead_train, synth, torch_api
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rl.build()
+    rl.load()
+    h, W, _ = lmhead_inputs_dev(dev, args.lmhead_rows, args.lmhead_dim)
+    R, D = h.shape
+    V = W.shape[0]
+    wl = synth.WORKLOADS[WORKLOAD]
+    T = wl.T
+    B = R // T
+    small = synth.small_inputs(wl)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    ids, mask = t(small["ids"][:R] % V), t(small["mask"][:R])
+    rewards = t(small["rewards"][:B])
+    opts = dict(eps=wl.eps, beta=0.0, c_ent=0.01, grad_scale=1.0)
+    if B % wl.group == 0:  # whole groups: the loss launch normalises the rewards itself
+        opts["group_size"] = wl.group
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return lmhead_train.lmhead_policy_loss(h, W, ids, mask, rewards, B, T, **opts)
+
+    for _ in range(args.warmup):
+        out = step()
+    torch.cuda.synchronize(dev)
+    assert int(out["status"].item()) == 0 and torch_api.read_stats(out["loss_stats"])["device_error"] == 0
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(int(vis.split(",")[local]) if vis else local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for _ in range(args.steps):
+        out = step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms_step = t0.elapsed_time(t1) / args.steps
+    del out
+    torch.cuda.empty_cache()
+
+    # each kernel alone, back to back (CUDA events around 5 launches after 3)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    parts = torch.empty((R, 4), device=dev)
+    nb = rl.rl_lmhead_workspace_size(R, V)
+    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=dev)
+    rl.rl_lmhead_row_partials(h, D, W, D, "bf16", R, D, V, ids, parts, status, ws, nb)
+    coef = torch_api.policy_loss_from_partials(parts, "bf16", V, ids, mask, rewards, B, T,
+                                               **opts)["row_coef"]
+    dz = torch.empty((R, V), dtype=torch.bfloat16, device=dev)
+    dH = torch.empty_like(h)
+    dW = torch.empty((V, D), dtype=torch.float32, device=dev)
+    kernels = {
+        "rl_lmhead_row_partials": lambda: rl.rl_lmhead_row_partials(h, D, W, D, "bf16", R, D, V, ids,
+                                                                    parts, status, ws, nb),
+        "rl_lmhead_dlogits": lambda: rl.rl_lmhead_dlogits(h, D, W, D, "bf16", R, D, V, ids, coef, dz, V,
+                                                          status),
+        "rl_lmhead_dhidden": lambda: rl.rl_lmhead_dhidden(dz, V, W, D, "bf16", R, D, V, dH, D, status),
+        "rl_lmhead_dweight": lambda: rl.rl_lmhead_dweight(dz, V, h, D, "bf16", R, D, V, dW, D, 0, status),
+    }
+    flops = 2.0 * R * D * V
+    peak, peak_kind = bf16_peak()
+    sust = bf16_sustained_peak()
+    per = {}
+    for name, fn in kernels.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / 5
+        tf = flops / (ms / 1e3) / 1e12
+        per[name] = {"ms": ms, "TFLOP_per_s": tf, "frac_of_burst": tf / peak,
+                     "frac_of_sustained": (tf / sust) if sust else None}
+    assert int(status.item()) == 0
+    achieved = 4 * flops / (ms_step / 1e3) / 1e12
+    top = max(per, key=lambda k: per[k]["ms"])
+    out = {
+        "metric": LMHEAD_TRAIN_METRIC, "value": R / (ms_step / 1e3), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": dict(lmhead_config(R, D, V), loss="GRPO group rewards in the loss launch, c_ent=0.01",
+                       valid_tokens=int(small["mask"][:R].sum()), parallelism="single GPU"),
+        "roofline": {"bound": "tensor", "achieved": achieved,
+                     "peak": sust if sust else peak, "unit": "TFLOP/s",
+                     "frac": achieved / (sust if sust else peak),
+                     "peak_source": "measured (sustained: four GEMMs back to back)" if sust else peak_kind,
+                     "peak_burst": peak, "frac_of_burst": achieved / peak, "traffic": None,
+                     "alg_flops_per_step": 4 * flops, "dominant_kernel": top},
+        "kernels": per, "e2e": None, "clocks": clocks,
+        # per step: statistics, loss, and dlogits / dhidden / dweight per chunk of sequences
+        "gpu_launches": args.steps * (2 + 3 * -(-B // lmhead_train._seqs_per_chunk(B, T, V, 2, 16 << 30))),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_lmhead_reference(args):
     """Reference arm of the LM-head leg: the oracle on host cores, bounded sample."""
     world, rank, _ = dist_env()
@@ -1027,6 +1144,9 @@ def main():
                     help="profiling only: every position valid (no masked rows)")
     ap.add_argument("--lmhead", action="store_true",
                     help="time rl_lmhead_logprobs on the Qwen3-0.6B LM head instead")
+    ap.add_argument("--lmhead-train", action="store_true",
+                    help="time the policy loss and its gradients from hidden states through the "
+                         "Qwen3-0.6B LM head (rl_lmhead_* kernels) instead")
     ap.add_argument("--lmhead-rows", type=int, default=0,
                     help="profiling only: rows of the LM-head leg (default 32768)")
     ap.add_argument("--lmhead-dim", type=int, default=0,
@@ -1035,7 +1155,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.lmhead:
+    if args.lmhead_train:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the LM-head training leg has no CPU "
+                              "reference arm; run the default leg"}))
+        else:
+            run_lmhead_train(args)
+    elif args.lmhead:
         (run_lmhead_reference if args.impl == "reference" else run_lmhead)(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -26,14 +26,16 @@
 //     per box, 2 (A) or 4 (B) boxes side by side.
 //   * warp 1 (one lane): MMA issuer (tcgen05.mma.kind::f16, M=128 N=256 K=16;
 //     the instruction descriptor marks M/N-major operands as transposed).
-//   * warps 2-5: epilogue, one accumulator row per thread, 32 columns per
-//     tensor-memory load.  dlogits stages each warp's 32 rows x 64 columns in
-//     shared memory (128-byte swizzle, two buffers) and writes them with one
-//     TMA store; dhidden and dweight store 16-bit or fp32 rows directly.
-//   * Persistent over (row tile, column tile) units.  dlogits units run in
-//     groups of row tiles that sweep W together (shared through L2); the
-//     dhidden / dweight units put the column tiles of one row tile next to
-//     each other, so the CTAs working at one time read the same dz tiles.
+//   * warps 2-5: epilogue, one accumulator row per thread.  dlogits stages
+//     each warp's 32 rows x 64 columns in shared memory (128-byte swizzle, two
+//     blocks per warp) and writes them with one TMA store; dhidden and dweight
+//     store 16-bit or fp32 rows directly.
+//   * Persistent over units of one tile each (the kernel also takes units of
+//     several column tiles, n_sl < n_nt; for dlogits that measured slower).
+//     dlogits units run in groups of row tiles that sweep W together (shared
+//     through L2); the dhidden / dweight units put the column tiles of one
+//     row tile next to each other, so the CTAs working at one time read the
+//     same dz tiles.
 //   * Every mbarrier wait is bounded; on timeout the kernel raises an error
 //     flag, waits for its own copies and tensor-core work, frees its tensor
 //     memory and exits.
@@ -54,7 +56,34 @@ constexpr int kGStages = 4;
 constexpr uint32_t kGStageA = kGM * kGK * 2;  // 16 KB
 constexpr uint32_t kGStageB = kGN * kGK * 2;  // 32 KB
 constexpr uint32_t kMnBlock = kGK * 128;      // one 64-element M/N block of an M/N-major tile: 64 K-rows x 128 B
-constexpr int kGThreads = 192;                // producer, MMA, 4 epilogue warps
+// Epilogue shape (compile-time knobs; the defaults are the shipped configuration):
+// RLG_EPI_WARPS epilogue warps (4: one warpgroup; 8: two, each on half of a
+// tile's columns), RLG_STAGE_BUFS staging blocks per warp for dlogits, and
+// RLG_STORE how dlogits leaves the staging block: 0 a TMA store, 1 the same
+// with an evict-first L2 hint, 2 coalesced 16-byte stores by the warp.
+#ifndef RLG_EPI_WARPS
+#define RLG_EPI_WARPS 4
+#endif
+#ifndef RLG_STAGE_BUFS
+#define RLG_STAGE_BUFS 2
+#endif
+#ifndef RLG_STORE
+#define RLG_STORE 0
+#endif
+// RLG_CLUSTER CTAs per cluster (1 or 2).  With 2, the CTAs of a pair take
+// row tiles 2p and 2p + 1 of the same column tile: each TMA-loads half of the
+// B tile and multicasts it to both, so each CTA reads 32 KB per K block from
+// L2 instead of 48 KB, and each MMA commit frees the stage in both CTAs.
+#ifndef RLG_CLUSTER
+#define RLG_CLUSTER 1
+#endif
+constexpr int kCl = RLG_CLUSTER;
+static_assert(kCl == 1 || kCl == 2, "one CTA or a pair per cluster");
+constexpr int kEpiWarps = RLG_EPI_WARPS;
+constexpr int kEpiGroups = kEpiWarps / 4;          // warpgroups, each on kGN / kEpiGroups columns
+constexpr int kStageBufs = RLG_STAGE_BUFS;
+constexpr int kGThreads = 64 + 32 * kEpiWarps;     // producer, MMA, epilogue warps
+static_assert(kEpiWarps == 4 || kEpiWarps == 8, "one or two epilogue warpgroups");
 constexpr uint32_t kGTmemCols = 2 * kGN;      // two fp32 accumulators
 constexpr long long kHiddenL2Bytes = 40LL << 20;  // row tiles a dlogits unit group may keep in L2
 
@@ -66,8 +95,8 @@ struct GSmem {
   alignas(1024) unsigned char a[kGStages][kGStageA];
   alignas(1024) unsigned char b[kGStages][kGStageB];
   // dlogits: each epilogue warp stages 32 rows x 64 columns of dz here (128-byte
-  // swizzled rows, two buffers) for a TMA store
-  alignas(1024) unsigned char stage[4][2][kStageBytes];
+  // swizzled rows) for a TMA store
+  alignas(1024) unsigned char stage[kEpiWarps][kStageBufs][kStageBytes];
   unsigned long long full[kGStages], empty[kGStages];
   unsigned long long acc_full[2], acc_empty[2];
   unsigned long long drain;
@@ -81,6 +110,7 @@ struct GArgs {
   long long M, N;
   uint32_t idesc;
   int n_mt, n_nt, n_kb, group;
+  int n_sl;              // column slices: a unit is (row tile, slice of n_nt / n_sl column tiles)
   void* out;             // row-major [M, ld_out]: 16-bit (dlogits, dhidden) or fp32 (dweight)
   long long ld_out;
   int out_f16;           // 16-bit outputs: fp16 instead of bf16
@@ -156,16 +186,23 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   GSmem& sm = *reinterpret_cast<GSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abort_flag = &sm.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_mt = a.n_mt, n_nt = a.n_nt, n_kb = a.n_kb, n_units = n_mt * n_nt;
+  // units are (row tile, or pair of row tiles with clusters of two CTAs;
+  // slice of column tiles), the slice's tiles taken in order
+  const int n_nt = a.n_nt, n_kb = a.n_kb, n_sl = a.n_sl;
+  const int n_mt = (a.n_mt + kCl - 1) / kCl, n_units = n_mt * n_sl;
+  const uint32_t crank = kCl > 1 ? cluster_rank() : 0;
+  const int cid = kCl > 1 ? static_cast<int>(cluster_id()) : static_cast<int>(blockIdx.x);
+  const int ncl = kCl > 1 ? static_cast<int>(cluster_count()) : static_cast<int>(gridDim.x);
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << kCl) - 1);
 
   if (tid == 0) {
     for (int s = 0; s < kGStages; ++s) {
       mbar_init(smem_addr(&sm.full[s]), 1);
-      mbar_init(smem_addr(&sm.empty[s]), 1);
+      mbar_init(smem_addr(&sm.empty[s]), kCl);  // freed by the MMA commits of every CTA that writes it
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&sm.acc_full[s]), 1);
-      mbar_init(smem_addr(&sm.acc_empty[s]), kGM);
+      mbar_init(smem_addr(&sm.acc_empty[s]), 32 * kEpiWarps);
     }
     mbar_init(smem_addr(&sm.drain), 1);
     sm.abort = 0;
@@ -181,6 +218,7 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
+  if (kCl > 1) cluster_sync_all();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -189,9 +227,11 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     if (lane == 0) {
       uint32_t it = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        int mt, nt;
-        unit_tile(u, n_mt, n_nt, a.group, mt, nt);
+      for (int u = cid; u < n_units && !stop; u += ncl) {
+        int mt, vs;
+        unit_tile(u, n_mt, n_sl, a.group, mt, vs);
+        mt = mt * kCl + static_cast<int>(crank);
+        for (int nt = slice_first(vs, n_nt, n_sl); nt < slice_first(vs + 1, n_nt, n_sl) && !stop; ++nt)
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const uint32_t s = it % kGStages, round = it / kGStages;
           if (round > 0 && !tc_wait<false>(smem_addr(&sm.empty[s]), (round - 1) & 1, abort_flag)) {
@@ -207,12 +247,22 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
           } else {
             tma_load_2d(smem_addr(sm.a[s]), &tmap_a, kb * kGK, mt * kGM, fb);
           }
+          // this CTA's share of the B tile (all of it without a cluster)
           if (kBMN) {
 #pragma unroll
-            for (int j = 0; j < kGN / 64; ++j)
-              tma_load_2d(smem_addr(sm.b[s]) + j * kMnBlock, &tmap_b, nt * kGN + j * 64, kb * kGK, fb);
+            for (int j = 0; j < kGN / 64 / kCl; ++j) {
+              const int jj = static_cast<int>(crank) * (kGN / 64 / kCl) + j;
+              if (kCl > 1)
+                tma_load_2d_mc(smem_addr(sm.b[s]) + jj * kMnBlock, &tmap_b, nt * kGN + jj * 64, kb * kGK, fb, kMask);
+              else
+                tma_load_2d(smem_addr(sm.b[s]) + jj * kMnBlock, &tmap_b, nt * kGN + jj * 64, kb * kGK, fb);
+            }
           } else {
-            tma_load_2d(smem_addr(sm.b[s]), &tmap_b, kb * kGK, nt * kGN, fb);
+            const int r0 = static_cast<int>(crank) * (kGN / kCl);
+            if (kCl > 1)
+              tma_load_2d_mc(smem_addr(sm.b[s]) + r0 * 128, &tmap_b, kb * kGK, nt * kGN + r0, fb, kMask);
+            else
+              tma_load_2d(smem_addr(sm.b[s]), &tmap_b, kb * kGK, nt * kGN, fb);
           }
         }
       }
@@ -225,8 +275,19 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
       bool stop = false, issued = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++acc_it) {
+      int mt_u = 0, vs = 0, nt = 0, nt_end = 0, u = cid - ncl;
+      while (!stop) {
+        if (nt == nt_end) {  // next unit: its slice's column tiles
+          u += ncl;
+          if (u >= n_units) break;
+          unit_tile(u, n_mt, n_sl, a.group, mt_u, vs);
+          nt = slice_first(vs, n_nt, n_sl);
+          nt_end = slice_first(vs + 1, n_nt, n_sl);
+          if (nt == nt_end) continue;
+        }
+        ++nt;
         const uint32_t buf = acc_it & 1, use = acc_it >> 1;
+        ++acc_it;
         if (use > 0 && !tc_wait<false>(smem_addr(&sm.acc_empty[buf]), (use - 1) & 1, abort_flag)) {
           stop = true;
           break;
@@ -252,7 +313,11 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
             umma_f16(d_tmem, ad, bd, a.idesc, (kb | k) != 0);
           }
           issued = true;
-          umma_commit(smem_addr(&sm.empty[s]));  // the stage is free once these MMAs have read it
+          // the stage is free once these MMAs have read it (in every CTA that loads into it)
+          if (kCl > 1)
+            umma_commit_mc(smem_addr(&sm.empty[s]), kMask);
+          else
+            umma_commit(smem_addr(&sm.empty[s]));
         }
         if (stop) break;
         umma_commit(smem_addr(&sm.acc_full[buf]));  // accumulator ready for the epilogue
@@ -265,13 +330,20 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) / 4;  // which part of the tile's columns this warp takes
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const bool f16 = a.out_f16 != 0;
     uint32_t acc_it = 0, blk = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++acc_it) {
-      int mt, nt;
-      unit_tile(u, n_mt, n_nt, a.group, mt, nt);
+#if RLG_STORE == 1
+    const uint64_t store_pol = policy_evict_first();
+#endif
+    bool stop = false;
+    for (int u = cid; u < n_units && !stop; u += ncl) {
+      int mt, vs;
+      unit_tile(u, n_mt, n_sl, a.group, mt, vs);
+      mt = mt * kCl + static_cast<int>(crank);
+      for (int nt = slice_first(vs, n_nt, n_sl); nt < slice_first(vs + 1, n_nt, n_sl); ++nt, ++acc_it) {
       const long long row = static_cast<long long>(mt) * kGM + r_in_tile;
       const bool row_ok = row < a.M;
       float cL = 0.f, a0 = 0.f, a1 = 0.f, gy = 0.f;
@@ -284,13 +356,17 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         gy = c.w;
         y = a.ids[row];
       }
-      // a row with no probability term (a masked row, or g = c_ent = 0) keeps
-      // only the -gy of its sampled id: 2^x is never formed for it
-      const bool p_term = a0 != 0.f || a1 != 0.f;
       const uint32_t buf = acc_it & 1, use = acc_it >> 1;
       // warp-uniform outcome: the tensor-memory loads below are warp-collective
-      if (!__all_sync(0xffffffffu, tc_wait<false>(smem_addr(&sm.acc_full[buf]), use & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, tc_wait<false>(smem_addr(&sm.acc_full[buf]), use & 1, abort_flag))) {
+        stop = true;
+        break;
+      }
       tc_fence_after();
+      // a row with no probability term (a masked row, or g = c_ent = 0) keeps
+      // only the -gy of its sampled id: 2^x is never formed for it (used only
+      // now, so the coefficient loads above overlap the accumulator wait)
+      const bool p_term = a0 != 0.f || a1 != 0.f;
       const long long n0 = static_cast<long long>(nt) * kGN;
       if (kEpi == kEpiDlogits) {
         // 64 columns at a time: two tensor-memory loads into this warp's staging
@@ -298,14 +374,26 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         // the TMA 128-byte swizzle), then one TMA store of the 32 x 64 box; the
         // store clips rows past R and columns past V.
 #pragma unroll 1
-        for (int c2 = 0; c2 < kGN / 64; ++c2, ++blk) {
-          const uint32_t sbuf = smem_addr(sm.stage[q][blk & 1]) + lane * 128;
-          if (lane == 0) bulk_wait_read_1();  // the store that last read this buffer is done with it
+        for (int c2 = half * (kGN / 64 / kEpiGroups); c2 < (half + 1) * (kGN / 64 / kEpiGroups); ++c2, ++blk) {
+          const uint32_t stage = smem_addr(sm.stage[warp - 2][blk % kStageBufs]);
+          const uint32_t sbuf = stage + lane * 128;
+#if RLG_STORE != 2
+          // the store that last read this staging block is done with it
+          if (lane == 0) {
+            if (kStageBufs == 1)
+              bulk_wait_all_read();
+            else
+              bulk_wait_read_1();
+          }
+#endif
           __syncwarp();
+          float v64[64];
+          tmem_ld64(tmem + lane_addr + buf * kGN + c2 * 64, v64);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float v[32];
-            tmem_ld32(tmem + lane_addr + buf * kGN + c2 * 64 + h * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = v64[h * 32 + i];
             dlogits32(v, cL, a0, a1, p_term);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -321,17 +409,44 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
               st_shared_u16(sbuf + (((e >> 3) ^ (lane & 7)) << 4) + (e & 7) * 2, static_cast<uint16_t>(bits));
             }
           }
+#if RLG_STORE == 2
+          // each lane sends 16-byte pieces: four full 128-byte rows per instruction
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = i * 4 + (lane >> 3), c = lane & 7;
+            const uint4 w = ld_shared_v4(stage + r * 128 + ((c ^ (r & 7)) << 4));
+            const long long grow = static_cast<long long>(mt) * kGM + q * 32 + r;
+            const long long gcol = n0 + c2 * 64 + c * 8;
+            if (grow < a.M && gcol < a.N) {
+              unsigned char* o = static_cast<unsigned char*>(a.out) + (grow * a.ld_out + gcol) * 2;
+              if (gcol + 8 <= a.N) {
+                *reinterpret_cast<uint4*>(o) = w;
+              } else {
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int e = 0; e < a.N - gcol; ++e)
+                  *reinterpret_cast<uint16_t*>(o + 2 * e) = static_cast<uint16_t>(ww[e >> 1] >> (16 * (e & 1)));
+              }
+            }
+          }
+          __syncwarp();
+#else
           fence_proxy_async_shared();  // this lane's staging writes, before the async proxy reads them
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmap_out, static_cast<int>(n0 + c2 * 64), mt * kGM + q * 32,
-                         smem_addr(sm.stage[q][blk & 1]));
+#if RLG_STORE == 1
+            tma_store_2d_hint(&tmap_out, static_cast<int>(n0 + c2 * 64), mt * kGM + q * 32, stage, store_pol);
+#else
+            tma_store_2d(&tmap_out, static_cast<int>(n0 + c2 * 64), mt * kGM + q * 32, stage);
+#endif
             bulk_commit();
           }
+#endif
         }
       }
 #pragma unroll 1
-      for (int c = 0; kEpi != kEpiDlogits && c < kGN / 32; ++c) {
+      for (int c = half * (kGN / 32 / kEpiGroups); kEpi != kEpiDlogits && c < (half + 1) * (kGN / 32 / kEpiGroups);
+           ++c) {
         float v[32];
         __syncwarp();
         tmem_ld32(tmem + lane_addr + buf * kGN + c * 32, v);
@@ -372,6 +487,7 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       }
       tc_fence_before();
       mbar_arrive(smem_addr(&sm.acc_empty[buf]));  // the MMA warp may overwrite this accumulator
+      }
     }
     if (kEpi == kEpiDlogits && lane == 0) bulk_wait_all();  // every store done before the CTA exits
   }
@@ -384,6 +500,7 @@ lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, kGTmemCols);
   }
+  if (kCl > 1) cluster_sync_all();  // no CTA leaves while its peer may still multicast into it
 }
 
 // ------------------------------------------------------------------ host side
@@ -395,20 +512,38 @@ rl_status launch_grad(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
   const int smem = static_cast<int>(sizeof(GSmem)) + 1024;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || tc_device_sms(&sms) != RL_OK) return RL_ERR_CUDA;
+  static int max_clusters = 0;
+  auto fn = lmhead_grad_kernel<kAMN, kBMN, kEpi>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (attr_dev != dev) {
-      if (cudaFuncSetAttribute(lmhead_grad_kernel<kAMN, kBMN, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem) != cudaSuccess)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return RL_ERR_CUDA;
+      int n = sms;
+      if (kCl > 1) {
+        cfg.gridDim = dim3(kCl);
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) return RL_ERR_CUDA;
+      }
+      max_clusters = n;
       attr_dev = dev;
     }
   }
-  const long long units = static_cast<long long>(args.n_mt) * args.n_nt;
+  const long long units = static_cast<long long>((args.n_mt + kCl - 1) / kCl) * args.n_sl;
   if (units == 0) return RL_OK;
-  const int grid = static_cast<int>(units < sms ? units : sms);
-  lmhead_grad_kernel<kAMN, kBMN, kEpi><<<grid, kGThreads, smem, stream>>>(ma, mb, mo, args);
-  return cudaGetLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+  const long long n_clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(n_clusters * kCl));
+  return cudaLaunchKernelEx(&cfg, fn, ma, mb, mo, args) == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -438,6 +573,7 @@ GArgs base_args(long long M, long long N, long long K, bool bf16, bool a_mn, boo
   g.n_nt = static_cast<int>((N + kGN - 1) / kGN);
   g.n_kb = static_cast<int>((K + kGK - 1) / kGK);
   g.group = 1;
+  g.n_sl = g.n_nt;  // one column tile per unit
   return g;
 }
 
@@ -460,12 +596,12 @@ extern "C" rl_status rl_lmhead_dlogits(const void* hidden, long long ld_h, const
   if (tc_encode_fn(&enc) != RL_OK) return RL_ERR_CUDA;
   CUtensorMap ma, mb, mo;
   if (!tc_make_map(enc, &ma, tmap_type(dtype), hidden, R, D, ld_h, kGK, kGM) ||
-      !tc_make_map(enc, &mb, tmap_type(dtype), weight, V, D, ld_w, kGK, kGN) ||
+      !tc_make_map(enc, &mb, tmap_type(dtype), weight, V, D, ld_w, kGK, kGN / kCl) ||
       !tc_make_map(enc, &mo, tmap_type(dtype), dlogits, R, V, ld_dz, 64, kStageRows))
     return RL_ERR_CUDA;
   GArgs g = base_args(R, V, D, dtype == RL_BF16, false, false);
   const long long tile_bytes = static_cast<long long>(kGM) * g.n_kb * kGK * 2;
-  const long long grp = kHiddenL2Bytes / tile_bytes;
+  const long long grp = kHiddenL2Bytes / tile_bytes / kCl;  // groups of row-tile pairs
   g.group = static_cast<int>(grp < 1 ? 1 : (grp > g.n_mt ? g.n_mt : grp));
   g.out = dlogits;
   g.ld_out = ld_dz;

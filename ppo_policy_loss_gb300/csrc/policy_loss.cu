@@ -448,11 +448,27 @@ __device__ __forceinline__ float element_of(uint4 w, int i) {
   return r;
 }
 
+// Two-word fp32 arithmetic for the fp32 build's per-row constants:
+// s + e == a + b exactly (Knuth's two-sum; __fadd_rn is never contracted).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// ln 2 as a head of 15 significant bits, so that e * head is exact for
+// |e| < 512, plus the rest (Cody and Waite's split of the constant).
+constexpr float kLn2Hi = 45426.0f / 65536.0f;
+constexpr float kLn2Lo = static_cast<float>(0.69314718055994530942 - 45426.0 / 65536.0);
+
 // Pass-2 gradient of one vector: d_v = 2^x (a0 + a1 x), x = z log2(e) - cL.
 // Without the entropy term (a1 = 0) no clamp is needed: a -inf logit gives
 // 2^x = 0 and 0 * a0 = 0.
+// fp32 logits (E::kBytes == 4) carry cL in two words, x = (z log2(e) - cL)
+// - cL_lo, and take exp2f: their gradient keeps a few fp32 ulps where a
+// 16-bit output's rounding would hide the difference.
 template <class E, bool kEntropy>
-__device__ __forceinline__ void grad_vec(uint4 w, float cL, float a0, float a1, float (&d)[E::kVec]) {
+__device__ __forceinline__ void grad_vec(uint4 w, float cL, float cLlo, float a0, float a1,
+                                         float (&d)[E::kVec]) {
   if (kEntropy) E::clamp(w);
   float z[E::kVec];
   E::unpack(w, z);
@@ -461,8 +477,14 @@ __device__ __forceinline__ void grad_vec(uint4 w, float cL, float a0, float a1, 
   const float2 A0 = make_float2(a0, a0);
 #pragma unroll
   for (int i = 0; i < E::kVec; i += 2) {
-    const float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, ncL);
-    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    float2 x = __ffma2_rn(make_float2(z[i], z[i + 1]), L2, ncL);
+    float2 p;
+    if constexpr (E::kBytes == 4) {
+      x = __fadd2_rn(x, make_float2(-cLlo, -cLlo));
+      p = make_float2(exp2f(x.x), exp2f(x.y));
+    } else {
+      p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    }
     const float2 r = kEntropy ? __fmul2_rn(p, __ffma2_rn(make_float2(a1, a1), x, A0)) : __fmul2_rn(p, A0);
     d[i] = r.x;
     d[i + 1] = r.y;
@@ -927,23 +949,67 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
 
       const bool y_ok = (y >= 0) && (y < a.v_total);
       const float zv = y_ok ? zyr : __int_as_float(0x7fc00000);
-      const float log2S = log2f(S);
-      const float lse = fmaf(log2S, kLn2, M);
+      // lse = M + ln S, logp = z_y - lse and cL = M log2(e) + log2 S (pass 2's
+      // exponent offset).  fp32 logits keep logp and cL in two words: with
+      // S = m 2^e (m in [0.5, 1)), log2 S = e + log2 m and ln S = e ln 2 + ln m,
+      // summed without rounding away the bits a single fp32 lse (|lse| ~ 10)
+      // would lose; 16-bit logits need no more than one word.
+      float log2S, logp, lp_lo = 0.f, cL, cL_lo = 0.f;
+      if constexpr (DT == RL_F32) {
+        int e2;
+        const float m2 = frexpf(S, &e2);
+        const float l2m = log2f(m2), ef = static_cast<float>(e2);
+        log2S = ef + l2m;
+        float s1, r1, s2, r2, s3, r3;
+        two_sum(zv, -M, s1, r1);
+        two_sum(s1, -ef * kLn2Hi, s2, r2);
+        two_sum(s2, -kLn2 * l2m, s3, r3);
+        logp = s3;
+        lp_lo = (r1 + r2) + (r3 - ef * kLn2Lo);
+        const float p1 = M * kLog2e, q1 = fmaf(M, kLog2e, -p1);  // M log2(e) = p1 + q1 exactly
+        float c1, f1, c2, f2;
+        two_sum(p1, ef, c1, f1);
+        two_sum(c1, l2m, c2, f2);
+        cL = c2;
+        cL_lo = (f1 + f2) + q1;
+      } else {
+        log2S = log2f(S);
+        logp = zv - fmaf(log2S, kLn2, M);
+        cL = fmaf(M, kLog2e, log2S);
+      }
       const float H = kLn2 * (log2S - Tt / S);
-      const float logp = zv - lse;
 
       // ---- per-token objective and its derivative with respect to logp
       const float A = a.adv_mode == RL_ADV_GROUP_REWARDS ? cache_A : rs.A;
-      const float r = a.logp_old ? expf(logp - rs.lpo) : 1.f;
+      float r = 1.f;
+      if (a.logp_old) {
+        if constexpr (DT == RL_F32) {  // exp of the two-word difference
+          float u, ue;
+          two_sum(logp, -rs.lpo, u, ue);
+          const float r0 = expf(u);
+          r = fmaf(r0, ue + lp_lo, r0);
+        } else {
+          r = expf(logp - rs.lpo);
+        }
+      }
       const float rA = r * A;
       const float pg = fminf(rA, fminf(fmaxf(r, a.clip_lo), a.clip_hi) * A);
       const bool clipped = (A > 0.f && r > a.clip_hi) || (A < 0.f && r < a.clip_lo);
       const float dpg = clipped ? 0.f : rA;
       float kl = 0.f, dkl = 0.f;
       if (a.ref_logp) {
-        const float d = rs.rf - logp;
-        dkl = expm1f(d);
-        kl = dkl - d;
+        if constexpr (DT == RL_F32) {
+          float d, de;
+          two_sum(rs.rf, -logp, d, de);
+          de -= lp_lo;
+          const float em = expm1f(d);
+          dkl = fmaf(em + 1.f, de, em);
+          kl = (em - d) + fmaf(em, de, 0.f);
+        } else {
+          const float d = rs.rf - logp;
+          dkl = expm1f(d);
+          kl = dkl - d;
+        }
       }
       float J = pg - a.beta * kl + a.c_ent * H;
       float g = dpg + a.beta * dkl;
@@ -965,7 +1031,6 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
 
       // ---- pass 2: dz_v = sc [g (p_v - [v == y]) + c_ent p_v (ln p_v + H)]
       //      with x_v = z_v log2(e) - (M log2(e) + log2 S):  p_v = 2^x_v, ln p_v = x_v ln 2
-      const float cL = fmaf(M, kLog2e, log2S);
       const float a0 = sc_row * fmaf(a.c_ent, H, g);
       const float a1 = sc_row * a.c_ent * kLn2;
       const float gy = sc_row * g;
@@ -990,9 +1055,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
               float d[kVec];
               const uint4 w = ld_shared_v4(buf + (tid + q * kConsumerThreads) * 16);
               if (with_entropy)
-                grad_vec<E, true>(w, cL, a0, a1, d);
+                grad_vec<E, true>(w, cL, cL_lo, a0, a1, d);
               else
-                grad_vec<E, false>(w, cL, a0, a1, d);
+                grad_vec<E, false>(w, cL, cL_lo, a0, a1, d);
               st_global_cs_v4(dst + q * kConsumerThreads * 16, E::pack(d));
             }
           } else {
@@ -1003,9 +1068,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
                 float d[kVec];
                 const uint4 w = ld_shared_v4(buf + (tid + q * kConsumerThreads) * 16);
                 if (with_entropy)
-                  grad_vec<E, true>(w, cL, a0, a1, d);
+                  grad_vec<E, true>(w, cL, cL_lo, a0, a1, d);
                 else
-                  grad_vec<E, false>(w, cL, a0, a1, d);
+                  grad_vec<E, false>(w, cL, cL_lo, a0, a1, d);
                 unsigned char* o = dst + q * kConsumerThreads * 16;
                 if (nelem - e0 >= kVec) {
                   st_global_cs_v4(o, E::pack(d));
@@ -1023,9 +1088,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
             float d[kVec];
             const uint4 w = ld_shared_v4(buf + jy * 16);
             if (with_entropy)
-              grad_vec<E, true>(w, cL, a0, a1, d);
+              grad_vec<E, true>(w, cL, cL_lo, a0, a1, d);
             else
-              grad_vec<E, false>(w, cL, a0, a1, d);
+              grad_vec<E, false>(w, cL, cL_lo, a0, a1, d);
 #pragma unroll
             for (int i = 0; i < kVec; ++i)
               if (i == iy) d[i] -= gy;

@@ -53,7 +53,6 @@ LMHEAD_METRIC = "fused LM-head + log-softmax rows/s (Qwen3 head, V=151936 bf16);
 LMHEAD_SHAPE = dict(R=32 * 1024, D=1024, V=151936, logit_sd=3.0, seed=202)
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
 LMHEAD_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "lmhead.cu")
-LMHEAD_TRAFFIC = os.path.join(ROOT, "profiles", "lmhead_logprobs_qwen3_head_traffic.txt")
 # the workloads timed after the headline (their kernel times and roofline
 # fractions go into the line's "workloads" object)
 OTHER_WORKLOADS = ("ppo_gae", "large_grpo", "long_seq_grpo", "tiny_grpo")
@@ -949,8 +948,9 @@ def run_lmhead(args):
                                                            "row_tiles_per_group": group}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": (recorded_traffic(path=LMHEAD_TRAFFIC, src=LMHEAD_SRC)
-                                 if not (args.lmhead_rows or args.lmhead_dim) else None),
+                     # no full-size record: the weight's sweeps through L2 depend on the
+                     # row count, so a slice's traffic does not scale by rows (see profiles/)
+                     "traffic": None,
                      "alg_flops_per_launch": flops, "kernel": "rl_lmhead_logprobs",
                      "kernel_ms": kern_ms},
         "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,

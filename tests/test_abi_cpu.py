@@ -174,6 +174,15 @@ def test_desc_defaults(lib):
     (dict(vocab_offset=8, vocab_total=1024), rl.RL_ERR_SHAPE),      # shard runs past the vocabulary
     (dict(vocab_offset=-8, vocab_total=4096), rl.RL_ERR_SHAPE),
     (dict(partials_out=FAKE + 0x700008), rl.RL_ERR_ALIGN),
+    # row coefficients for the LM-head backward: merge launches only, 16-byte aligned;
+    # a merge launch without columns (V = 0) needs them and the vocabulary size
+    (dict(row_coef_out=FAKE + 0x900000), rl.RL_ERR_ARG),
+    (dict(shard_partials=FAKE + 0x800000, n_shards=1, row_coef_out=FAKE + 0x900008), rl.RL_ERR_ALIGN),
+    (dict(shard_partials=FAKE + 0x800000, n_shards=1, V=0, ld=0), rl.RL_ERR_SHAPE),
+    (dict(shard_partials=FAKE + 0x800000, n_shards=1, V=0, ld=0, row_coef_out=FAKE + 0x900000),
+     rl.RL_ERR_SHAPE),                                               # no vocab_total
+    (dict(shard_partials=FAKE + 0x800000, n_shards=1, V=0, ld=0, vocab_total=1024, logits=None,
+          row_coef_out=FAKE + 0x900000, ids=None), rl.RL_ERR_NULL),
 ])
 def test_desc_argument_errors(lib, over, status):
     assert lib.rl_policy_loss_fwd_bwd_ex(ctypes.byref(_desc(**over)), None) == status
@@ -268,3 +277,76 @@ def test_selftest_wait_timeout_host_errors(lib):
     assert lib.rl_selftest_wait_timeout(1000000, None, None, None) == rl.RL_ERR_NULL
     assert lib.rl_selftest_wait_timeout(10, FAKE, None, None) == rl.RL_ERR_ARG
     assert lib.rl_selftest_wait_timeout(11 * 10**9, FAKE, None, None) == rl.RL_ERR_ARG
+
+
+# ----------------------------------------------------------------- the LM-head backward entry points
+G_DZ, G_W, G_H, G_OUT, G_COEF, G_IDS = (FAKE + k * 0x10000000 for k in range(1, 7))
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dtype=rl.RL_F32), rl.RL_ERR_DTYPE),
+    (dict(R=-1), rl.RL_ERR_SHAPE),
+    (dict(R=1 << 31), rl.RL_ERR_SHAPE),
+    (dict(V=0), rl.RL_ERR_SHAPE),
+    (dict(D=1020, ld_h=1020, ld_w=1020), rl.RL_ERR_SHAPE),      # D not a multiple of 8
+    (dict(ld_dz=151932), rl.RL_ERR_SHAPE),                      # below V
+    (dict(ld_dz=151937, V=151937), rl.RL_ERR_SHAPE),            # not a multiple of 8 elements
+    (dict(coef=None), rl.RL_ERR_NULL),
+    (dict(ids=None), rl.RL_ERR_NULL),
+    (dict(out=None), rl.RL_ERR_NULL),
+    (dict(coef=G_COEF + 8), rl.RL_ERR_ALIGN),
+    (dict(out=G_OUT + 2), rl.RL_ERR_ALIGN),
+    (dict(R=0, coef=None, out=None), rl.RL_OK),                  # nothing to launch
+])
+def test_lmhead_dlogits_host_errors(lib, over, expect):
+    a = dict(h=G_H, ld_h=1024, w=G_W, ld_w=1024, dtype=rl.RL_BF16, R=256, D=1024, V=151936,
+             ids=G_IDS, coef=G_COEF, out=G_OUT, ld_dz=151936)
+    a.update(over)
+    assert lib.rl_lmhead_dlogits(a["h"], a["ld_h"], a["w"], a["ld_w"], a["dtype"], a["R"], a["D"],
+                                 a["V"], a["ids"], a["coef"], a["out"], a["ld_dz"], None,
+                                 None) == expect
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dtype=7), rl.RL_ERR_DTYPE),
+    (dict(D=4), rl.RL_ERR_SHAPE),
+    (dict(ld_dh=512), rl.RL_ERR_SHAPE),
+    (dict(dz=None), rl.RL_ERR_NULL),
+    (dict(out=None), rl.RL_ERR_NULL),
+    (dict(w=G_W + 4), rl.RL_ERR_ALIGN),
+    (dict(R=0, dz=None), rl.RL_OK),
+])
+def test_lmhead_dhidden_host_errors(lib, over, expect):
+    a = dict(dz=G_DZ, ld_dz=151936, w=G_W, ld_w=1024, dtype=rl.RL_BF16, R=256, D=1024, V=151936,
+             out=G_OUT, ld_dh=1024)
+    a.update(over)
+    assert lib.rl_lmhead_dhidden(a["dz"], a["ld_dz"], a["w"], a["ld_w"], a["dtype"], a["R"], a["D"],
+                                 a["V"], a["out"], a["ld_dh"], None, None) == expect
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dtype=rl.RL_F32), rl.RL_ERR_DTYPE),
+    (dict(ld_dw=1022), rl.RL_ERR_SHAPE),                          # below D
+    (dict(ld_dw=1030), rl.RL_ERR_SHAPE),                          # not a multiple of 4 floats
+    (dict(out=None), rl.RL_ERR_NULL),
+    (dict(out=G_OUT + 4), rl.RL_ERR_ALIGN),
+    (dict(dz=None), rl.RL_ERR_NULL),
+    (dict(h=G_H + 2), rl.RL_ERR_ALIGN),
+    (dict(R=0, dz=None, h=None, acc=1), rl.RL_OK),               # adds nothing
+])
+def test_lmhead_dweight_host_errors(lib, over, expect):
+    a = dict(dz=G_DZ, ld_dz=151936, h=G_H, ld_h=1024, dtype=rl.RL_BF16, R=256, D=1024, V=151936,
+             out=G_OUT, ld_dw=1024, acc=0)
+    a.update(over)
+    assert lib.rl_lmhead_dweight(a["dz"], a["ld_dz"], a["h"], a["ld_h"], a["dtype"], a["R"], a["D"],
+                                 a["V"], a["out"], a["ld_dw"], a["acc"], None, None) == expect
+
+
+def test_lmhead_row_partials_host_errors(lib):
+    f = lib.rl_lmhead_row_partials
+    args = [FAKE, 1024, FAKE + 0x1000000, 1024, rl.RL_BF16, 256, 1024, 151936, FAKE + 0x2000000]
+    assert f(*args, None, None, None, 0, None) == rl.RL_ERR_NULL               # no output
+    assert f(*args, FAKE + 0x3000008, None, None, 0, None) == rl.RL_ERR_ALIGN  # 16-byte records
+    bad = list(args)
+    bad[4] = rl.RL_F32
+    assert f(*bad, FAKE + 0x3000000, None, None, 0, None) == rl.RL_ERR_DTYPE

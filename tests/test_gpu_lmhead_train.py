@@ -251,3 +251,73 @@ def test_chunking_changes_only_the_weight_gradients_summation_order():
     assert torch.equal(a["dhidden"], b["dhidden"])
     dw_a, dw_b = a["dweight"].double(), b["dweight"].double()
     assert float((dw_a - dw_b).abs().max()) <= 1e-5 * float(dw_b.abs().max())
+
+
+def test_lmhead_policy_loss_qwen3_head_full_size_sampled_rows():
+    """The training op at the Qwen3-0.6B head's full size (32 x 1024 rows, D 1024,
+    V 151936 bf16) with the GRPO workload's mask, ids and rewards, in its default
+    chunking.  The oracle recomputes 16 sampled valid rows one by one (their
+    fp64 logits, statistics, gradient coefficients with the batch's token
+    count and group advantages, dz and dhidden = dz W) and 4 masked rows; the
+    loss and the counts hold over the whole batch."""
+    dev = torch.device("cuda:0")
+    w = synth.WORKLOADS["qwen3_0p6b_grpo"]
+    B, T, V, R, D = w.B, w.T, w.V, w.R, 1024
+    small = synth.small_inputs(w)
+    ids, mask = small["ids"], small["mask"]
+    hidden, weight, _ = synth.lmhead_inputs(R, D, V, 203, 3.0)
+    Hs, Ws = storage_np(hidden), storage_np(weight)
+    Wd = oracle.decode(Ws, "bf16")
+    rng = np.random.default_rng(204)
+    valid = np.nonzero(mask)[0]
+    rows = np.unique(np.concatenate([rng.choice(valid, 14, replace=False), valid[[0, -1]]]))
+    masked = rng.choice(np.nonzero(mask == 0)[0], 4, replace=False)
+    # per sampled row: fp64 logits and statistics; logp_old / ref = that logp + the noise.
+    # Other rows get seeded values far from their logp (inputs only: those rows are not compared).
+    z = oracle.decode(Hs[rows], "bf16") @ Wd.T
+    lse, logp, ent = oracle.row_stats(z, "f64", V, ids[rows], np.ones(rows.size, np.uint8))
+    lo = np.where(mask != 0, -12.0 + small["noise_old"], 0.0)
+    rf = np.where(mask != 0, -12.0 + small["noise_ref"], 0.0)
+    lo[rows] = logp + small["noise_old"][rows]
+    rf[rows] = logp + small["noise_ref"][rows]
+    lo, rf = lo.astype(np.float32), rf.astype(np.float32)
+    A = oracle.group_advantages(small["rewards"], w.group)
+    N = int(mask.sum())
+    out = lmhead_train.lmhead_policy_loss(hidden.to(dev), weight.to(dev), to_dev(ids), to_dev(mask),
+                                          to_dev(small["rewards"]), B, T, logp_old=to_dev(lo),
+                                          ref_logp=to_dev(rf), eps=w.eps, beta=w.beta,
+                                          c_ent=0.01, group_size=w.group, grad_scale=float(N))
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == 0
+    st = torch_api.read_stats(out["loss_stats"])
+    assert st["device_error"] == 0 and st["n_tokens"] == N and np.isfinite(st["loss"])
+    lp_gpu, h_gpu = out["logp"].cpu().numpy(), out["entropy"].cpu().numpy()
+    assert np.abs(lp_gpu[rows] - logp).max() <= LOGP_ATOL
+    assert np.abs(h_gpu[rows] - ent).max() <= LOGP_ATOL
+    assert np.all(lp_gpu[mask == 0] == 0) and np.all(h_gpu[mask == 0] == 0)
+    # the sampled rows' gradient coefficients, as the oracle's token objective gives them
+    # (token_mean at grad_scale N: each valid row's scale is 1).  A row whose ratio lies
+    # within the logp tolerance of a clip boundary may take either one-sided derivative.
+    obj = oracle.token_objective(logp, ent, np.ones(rows.size, np.uint8), A[rows // T], lo[rows],
+                                 rf[rows], w.eps, w.beta, 0.01)
+    log_r = logp - lo[rows]
+    band = np.zeros(rows.size, bool)
+    for edge in (np.log1p(w.eps), np.log1p(-w.eps)):
+        band |= np.abs(log_r - edge) <= LOGP_ATOL
+    dh = oracle.decode(storage_np(out["dhidden"][torch.from_numpy(rows)]), "bf16")
+    ok_any = np.zeros(rows.size, bool)
+    variants = [obj["g"]] + ([obj["g_unclipped"], obj["g_clipped"]] if band.any() else [])
+    for k, g in enumerate(variants):
+        dz = oracle.dlogits_rows(z, "f64", V, ids[rows], np.arange(rows.size), lse, ent, g,
+                                 np.ones(rows.size), 0.01, "f64")
+        dh_ref = dz @ Wd
+        dz_err = oracle.ulp(dz, "bf16") + DLOGIT_ATOL
+        tol = oracle.ulp(dh_ref, "bf16") + dz_err @ np.abs(Wd) + accumulation_bound(dz, Wd)
+        ok = (np.abs(dh - dh_ref) <= tol).all(axis=1)
+        if k == 0:
+            assert ok[~band].all(), _assert_within(dh[~band], dh_ref[~band], tol[~band],
+                                                   "full-size dhidden")
+        ok_any |= ok
+    assert ok_any.all(), np.nonzero(~ok_any)[0]
+    assert int(torch.count_nonzero(out["dhidden"][torch.from_numpy(masked)].view(torch.int16))) == 0
+    assert bool(torch.isfinite(out["dweight"]).all())

@@ -325,12 +325,15 @@ def workload_for(args):
         w = w.scaled(T=args.seq_len)
     if getattr(args, "all_valid", False):
         w = w.scaled(lengths=("full",))
+    if getattr(args, "c_ent", None) is not None:
+        w = w.scaled(c_ent=args.c_ent)
     return w
 
 
 def reshaped(args) -> bool:
     return bool(args.seqs or getattr(args, "vocab", 0) or getattr(args, "dtype", None)
-                or getattr(args, "seq_len", 0) or getattr(args, "all_valid", False))
+                or getattr(args, "seq_len", 0) or getattr(args, "all_valid", False)
+                or getattr(args, "c_ent", None) is not None)
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -1142,6 +1145,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=0, help="profiling only: another T")
     ap.add_argument("--all-valid", action="store_true",
                     help="profiling only: every position valid (no masked rows)")
+    ap.add_argument("--c-ent", type=float, default=None,
+                    help="profiling only: another entropy coefficient (0 drops the entropy term)")
     ap.add_argument("--lmhead", action="store_true",
                     help="time rl_lmhead_logprobs on the Qwen3-0.6B LM head instead")
     ap.add_argument("--lmhead-train", action="store_true",

@@ -14,43 +14,45 @@
 //     in the rest of this comment are the long-row build's.
 //   * One producer warp streams the valid rows with 1-D bulk copies
 //     (cp.async.bulk) into a ring of 6 x 32 KB shared-memory chunks guarded
-//     by full/empty mbarriers.  It runs ahead of the consumers by up to the
+//     by full/empty mbarriers, running ahead of the consumers by up to the
 //     whole ring.  32 KB chunks give each consumer thread four 16-byte
-//     vectors per chunk, independent work that hides latency; 16 KB chunks
-//     (two vectors) measured 6-13% slower, 48 KB ones spill registers.
+//     vectors per chunk, independent work that hides latency.
 //   * Two row modes:
-//       - resident: a row that fits the ring twice over (at most 2 chunks,
-//         e.g. 32000 fp16 logits) is loaded once and kept in shared memory
-//         for both passes;
+//       - resident: a row that fits the ring twice over (at most 2 chunks)
+//         is loaded once and kept in shared memory for both passes;
 //       - streaming: a longer row (151936 bf16 logits = 10 chunks) is streamed
 //         twice: the first load keeps its L2 lines (evict-last), the second
 //         pass re-reads them from L2 (evict-first).  Logits still cross the
-//         HBM bus once, and the ring is always free to prefetch.
-//     A cluster layout (each CTA of a 2..8-CTA cluster holding one slice of a
-//     resident row, statistics exchanged through distributed shared memory)
-//     is kept for comparison builds; it costs a cluster-wide exchange per row
-//     and loses to streaming on GB300.
-//   * A zero warp writes the all-zero gradient of masked rows (their logits
-//     are never read) as bulk copies of a zeroed shared-memory block, kept
-//     within eight rows of the consumers, so masked rows' stores overlap the
-//     valid rows' arithmetic without taking the consumers' store path.
+//         HBM bus once, and the ring is always free to prefetch.  When no
+//         row is masked the second pass runs in reverse chunk order.
+//   * Consumer warps: pass 1 keeps a per-thread online (max, sum 2^x,
+//     sum 2^x * x) in packed fp32x2 with independent accumulator chains;
+//     each warp then reduces its lanes and publishes one partial.  Pass 2
+//     writes the gradient with 16-byte streaming stores.  The entropy term
+//     is a template argument, so each launch runs only the pass-2 code it
+//     needs.
+//   * A row warp merges the consumer warps' partials of each row and turns
+//     them into the row's loss terms and pass-2 coefficients: a long chain
+//     of dependent scalar arithmetic, run once per row instead of once per
+//     consumer warp.  Two rows are in flight between the consumers and the
+//     row warp (two mbarrier pairs); in the short-row build the consumers
+//     run the first chunk of the next row's pass 1 before a row's pass 2,
+//     which covers the row warp's time for that row.
+//   * Masked rows need no logits, only an all-zero gradient row, written as
+//     bulk copies of a zeroed shared-memory block (the copy engine, not the
+//     consumers' store path): by a zero warp kept within eight rows of the
+//     consumers (long rows), or by the producer as it walks the rows (short
+//     rows: one warp fewer leaves 96 registers per thread at two CTAs per
+//     SM).
 //   * Each row loop reads the mask bytes of 32 of its rows with one ballot
 //     and jumps to the next row it handles.
-//   * Consumer warps.  Pass 1: per-thread online (max, sum 2^x,
-//     sum 2^x * x) in packed fp32x2 with independent accumulator chains.
-//     Each warp shuffle-merges its lanes and publishes one partial; the
-//     partials meet through one mbarrier (no CTA-wide barrier per row), and
-//     every warp merges them with shuffles.  Pass 2: the gradient, written
-//     with 16-byte streaming stores.  The entropy term is a template
-//     argument, so each launch runs only the pass-2 code it needs.
-//   * Masked rows: all-zero gradient stores only, their logits are not read.
 //   * N (valid tokens) is counted by every CTA at start (R bytes from L2);
-//     the loss is reduced in fp64: per-CTA partials in a fixed row order,
-//     then the last CTA (atomic ticket, no spinning) sums them in CTA order.
-//     Same inputs, same device -> bitwise identical results.
+//     the loss is reduced in fp64: per-warp and per-CTA partials in a fixed
+//     row order, then the last CTA (atomic ticket, no spinning) sums them in
+//     CTA order.  Same inputs, same device -> bitwise identical results.
 //   * Every wait on an mbarrier is bounded (1 s); on timeout the kernel
-//     raises RL_DEVERR_TIMEOUT, stops, drains its own bulk copies and exits
-//     through the final cluster barrier.  No trap, no unbounded spin.
+//     raises RL_DEVERR_TIMEOUT, stops, drains its own bulk copies and
+//     exits.  No trap, no unbounded spin.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -69,8 +71,8 @@ namespace {
 // rows: 16 consumer warps, one CTA per SM, 32 KB chunks.  With RL_SHORT_ROWS
 // it builds the one for rows of at most kShortRowBytes: 8 consumer warps,
 // two CTAs per SM and 16 KB chunks, so that each SM has two rows in flight
-// and one row's per-row latencies (the exchange, the row's scalar math)
-// overlap the other's streaming.  The C entry points, compiled in the
+// and one row's per-row latencies (the partials' exchange, the row's scalar
+// math) overlap the other's streaming.  The C entry points, compiled in the
 // default build only, pick one per call from the row length.
 #define RL_INTERNAL __attribute__((visibility("hidden")))  // shared by the two builds only
 #ifdef RL_SHORT_ROWS
@@ -97,45 +99,74 @@ namespace {
 #ifndef RL_MIN_CTAS_PER_SM
 #define RL_MIN_CTAS_PER_SM 1
 #endif
-// 0: rows that do not fit the ring twice are streamed (re-read from L2);
-// 1: such rows are split across a cluster and held on chip (comparison).
-#ifndef RL_CLUSTER_RESIDENT
-#define RL_CLUSTER_RESIDENT 0
-#endif
 // L2 policy of the first load of a streamed row: 1 evict-last, 0 normal.
 #ifndef RL_STREAM_KEEP_L2
 #define RL_STREAM_KEEP_L2 1
+#endif
+// Chunks of the next row's first pass that the consumers run before the
+// second pass of a row: the time the row warp has for that row's arithmetic.
+#ifndef RL_LEAD_CHUNKS
+#ifdef RL_SHORT_ROWS
+#define RL_LEAD_CHUNKS 1
+#else
+#define RL_LEAD_CHUNKS 0
+#endif
+#endif
+
+// Masked rows' zero gradient: 1 a warp of its own, kept within kZeroLead
+// rows of the consumers; 0 the producer writes them as it walks the rows
+// (one warp fewer: the short-row build keeps 96 registers per thread).
+#ifndef RL_ZERO_WARP
+#ifdef RL_SHORT_ROWS
+#define RL_ZERO_WARP 0
+#else
+#define RL_ZERO_WARP 1
+#endif
 #endif
 
 constexpr int kChunkBytes = RL_CHUNK_BYTES;
 constexpr int kSlots = RL_RING_SLOTS;
 constexpr int kConsumerWarps = RL_CONSUMER_WARPS;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 64;  // + the producer warp and the zero warp
-constexpr int kMaxCluster = 8;
+constexpr int kRowWarp = kConsumerWarps;  // warps: consumers, the row warp, the producer, the zero warp
+constexpr int kProducerWarp = kConsumerWarps + 1;
+constexpr int kZeroWarp = RL_ZERO_WARP ? kConsumerWarps + 2 : -1;
+constexpr int kThreads = kConsumerThreads + (RL_ZERO_WARP ? 96 : 64);
+constexpr int kRedWarps = kConsumerWarps + 1;  // consumers and the row warp: token counts and sums
+constexpr int kRedThreads = kRedWarps * 32;
+constexpr int kLeadChunks = RL_LEAD_CHUNKS;
 constexpr int kVecsPerChunk = kChunkBytes / 16;
 constexpr int kVecsPerThread = kVecsPerChunk / kConsumerThreads;
 static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly over consumers");
-static_assert(kConsumerWarps * kMaxCluster <= 128, "partials of one row fit 4 per lane");
+static_assert(kConsumerWarps <= 32, "the row warp takes one consumer partial per lane");
+static_assert(kLeadChunks >= 0, "chunks of look-ahead");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
-constexpr uint32_t kConsumerBarrier = 1;  // named barrier id (0 is __syncthreads)
+constexpr uint32_t kRedBarrier = 1;  // named barrier id (0 is __syncthreads): consumers + row warp
 constexpr int kZeroBytes = kChunkBytes / 2;  // zero block the masked rows are copied from
-constexpr long long kZeroLead = 8;        // rows the zero warp may run ahead of the consumers
+constexpr long long kZeroLead = 8;           // rows a zero warp may run ahead of the consumers
+
+// A row's pass-2 coefficients: d_v = 2^x (a0 + a1 x) with x = z log2(e) - cL
+// (- cL_lo as well for fp32 logits); the sampled id's element also gets -gy.
+struct RowCoef {
+  float cL, cL_lo, a0, a1, gy;
+};
 
 struct LossSmem {
   alignas(128) unsigned char ring[kSlots][kChunkBytes];
   alignas(128) unsigned char zeros[kZeroBytes];  // source of the masked rows' bulk stores
   unsigned long long full[kSlots];
   unsigned long long empty[kSlots];
-  unsigned long long xbar[2];
-  float4 xpart[2][kMaxCluster * kConsumerWarps];  // (m, s, t, z_y or -inf) per warp
-  long long wcount[kConsumerWarps];
-  long long wseq[kConsumerWarps];
-  double wred[kConsumerWarps][5];
-  double acc[5];  // this CTA's J, pg, kl, H, clipped sums (kept by thread 0 of rank 0)
+  unsigned long long xbar[2];  // a row's consumer partials are in (one arrival per consumer warp)
+  unsigned long long cbar[2];  // the row warp is done with a row's partials, coef holds its coefficients
+  float4 xpart[2][kConsumerWarps];  // (m, s, t, -) per consumer warp
+  float zy[2];                      // the sampled logit, from the thread that holds it (or -inf)
+  RowCoef coef[2];
+  long long wcount[kThreads / 32];
+  long long wseq[kRedWarps];
+  double wred[kRedWarps][5];  // per-warp J, pg, kl, H, clipped sums
   int abort;
   int is_last;
-  long long pace;  // row the consumers are on (the zero warp keeps within a few rows of it)
+  long long pace;  // row the consumers are on (a zero warp keeps within kZeroLead rows of it)
 };
 
 struct LossArgs {
@@ -153,7 +184,6 @@ struct LossArgs {
   WsPartial* partials;
   long long R, T, V;
   long long row_bytes;  // ld * element bytes
-  long long slice;      // vocabulary elements per cluster rank (V when not clustered)
   int adv_mode;         // rl_adv_layout
   int group_size, ddof; // RL_ADV_GROUP_REWARDS
   double std_eps;       // RL_ADV_GROUP_REWARDS
@@ -573,6 +603,33 @@ struct RowWalk {
   }
 };
 
+// Every row first, first + stride, ... (below R) in order, with its mask
+// bit: one ballot per window of 32 rows.  next() returns the next row (R
+// after the last) and whether it is valid; whole warp.
+struct RowScan {
+  long long base;
+  uint32_t bits;
+  int i;
+  __device__ RowScan(long long first, long long stride) : base(first - 32 * stride), bits(0u), i(32) {}
+  __device__ __forceinline__ long long next(const unsigned char* mask, long long stride, long long R,
+                                            int lane, bool& valid) {
+    if (i == 32) {
+      base += 32 * stride;
+      if (base >= R) {
+        valid = false;
+        return R;
+      }
+      const long long r = base + lane * stride;
+      bits = __ballot_sync(0xffffffffu, r < R && mask[r] != 0);
+      i = 0;
+    }
+    const long long row = base + i * stride;
+    valid = (bits >> i) & 1u;
+    ++i;
+    return row < R ? row : R;
+  }
+};
+
 // Nonzero bytes of mask[begin, begin + n), counted by one warp (every lane
 // gets the count).
 __device__ __forceinline__ int warp_count_mask(const unsigned char* m, long long n, int lane) {
@@ -613,14 +670,268 @@ __device__ __forceinline__ float warp_group_advantage(const LossArgs& a, long lo
 }
 
 // ------------------------------------------------------------------ the kernel
+// Where a row's sampled id sits, for the consumer thread that holds it:
+// chunk cy and, in jv, vector jv / kVec of the chunk and element jv % kVec
+// of the vector.  cy = -1 on every other thread, and everywhere when the id
+// is not one of this launch's columns.
+struct IdPos {
+  int cy, jv;
+};
+
+template <int kElemsPerChunk, int kVec>
+__device__ __forceinline__ IdPos id_pos(const LossArgs& a, long long y, int tid) {
+  IdPos p;
+  p.cy = -1;
+  p.jv = 0;
+  const long long yl = y - a.v_offset;  // column of y in this shard
+  if (yl >= 0 && yl < a.V) {
+    const int off = static_cast<int>(yl);
+    const int jv = off % kElemsPerChunk;  // element within the chunk
+    if ((jv / kVec) % kConsumerThreads == tid) {
+      p.cy = off / kElemsPerChunk;
+      p.jv = jv;
+    }
+  }
+  return p;
+}
+
+// Per-sequence quantities of a warp's current sequence.
+struct SeqCache {
+  long long b;
+  int L;    // valid tokens of the sequence (seq-mean-token-mean)
+  float A;  // group advantage from the rewards
+};
+
+// Merge of per-shard statistics (vocabulary shards, merge launch): shard
+// order over the lanes, then a fixed shuffle tree; every lane returns lane
+// 0's bits.  Whole warp.
+__device__ __forceinline__ void merge_shards(const LossArgs& a, long long row, int lane, float& M,
+                                             float& S, float& Tt, float& zyr) {
+  M = -INFINITY;
+  S = Tt = 0.f;
+  zyr = -INFINITY;
+  for (int k = lane; k < a.n_shards; k += 32) {
+    const float4 P = __ldg(&a.shard_partials[static_cast<long long>(k) * a.R + row]);
+    merge_stats(M, S, Tt, P.x, P.y, P.z);
+    zyr = max_nan(zyr, P.w);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
+    merge_stats(M, S, Tt, m2, s2, t2);
+    zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
+  }
+  M = __shfl_sync(0xffffffffu, M, 0);
+  S = __shfl_sync(0xffffffffu, S, 0);
+  Tt = __shfl_sync(0xffffffffu, Tt, 0);
+  zyr = __shfl_sync(0xffffffffu, zyr, 0);
+}
+
+// Sum of (m, s, t) partials over the warp: the maximum first, then each
+// lane's sums rescaled to it and added.  Lane 0 holds the result (every lane
+// gets it with `bcast`).  A partial with s = 0 adds exactly 0; a NaN s or t
+// poisons the sum.
+__device__ __forceinline__ void warp_stats(float& m, float& s, float& t, bool bcast) {
+  float M;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(M) : "f"(m));
+  const float d = (M - m) * kLog2e;  // >= 0, finite: every m is at least the floor
+  const float f = ex2_approx(-d);
+  t = f * fmaf(-d, s, t);
+  s = f * s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+  }
+  m = M;
+  if (bcast) {
+    s = __shfl_sync(0xffffffffu, s, 0);
+    t = __shfl_sync(0xffffffffu, t, 0);
+  }
+}
+
+// A row's loss terms and the coefficients of its gradient.
+struct RowVals {
+  RowCoef cf;
+  float J, pg, kl, H, logp;
+  double w_row;
+  bool clipped, y_ok;
+};
+
+// From a row's softmax statistics (M, S, Tt, z_y) to its loss terms and the
+// coefficients of its gradient.  Whole warp: every lane computes the same
+// values from the same inputs.  16-bit logits take the fast hardware log2,
+// exp and division for lse, the ratio and the entropy (errors near 1e-6
+// relative, far below what a 16-bit gradient or the loss's tolerance can
+// show); fp32 logits keep the accurate two-word path.
+template <int DT>
+__device__ __forceinline__ RowVals row_values(const LossArgs& a, const RowScalars& rs, SeqCache& cache,
+                                              long long Bp, float sc, float M, float S, float Tt,
+                                              float zyr, int lane) {
+  RowVals v;
+  // per-sequence quantities, recomputed when the sequence changes
+  const long long bseq = rs.b;
+  if (bseq != cache.b) {
+    cache.b = bseq;
+    if (a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN) cache.L = warp_count_mask(a.mask + bseq * a.T, a.T, lane);
+    if (a.adv_mode == RL_ADV_GROUP_REWARDS) cache.A = warp_group_advantage(a, bseq, lane);
+  }
+  // loss weight of this token and the gradient scale of its row
+  v.w_row = 1.0;  // token mean: the 1/N is applied once, at the end
+  float sc_row = sc;
+  if (a.agg != RL_AGG_TOKEN_MEAN) {
+    v.w_row = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN ? 1.0 / (static_cast<double>(Bp) * cache.L)
+            : a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM  ? 1.0 / static_cast<double>(Bp)
+                                                   : a.agg_w;
+    sc_row = static_cast<float>(static_cast<double>(a.grad_scale) * v.w_row);
+  }
+  const long long y = rs.y;
+  v.y_ok = (y >= 0) && (y < a.v_total);
+  const float zv = v.y_ok ? zyr : __int_as_float(0x7fc00000);
+  // lse = M + ln S, logp = z_y - lse and cL = M log2(e) + log2 S (pass 2's
+  // exponent offset).  fp32 logits keep logp and cL in two words: with
+  // S = m 2^e (m in [0.5, 1)), log2 S = e + log2 m and ln S = e ln 2 + ln m,
+  // summed without rounding away the bits a single fp32 lse (|lse| ~ 10)
+  // would lose; 16-bit logits need no more than one word.
+  float log2S, logp, lp_lo = 0.f, cL, cL_lo = 0.f, TtS;
+  if constexpr (DT == RL_F32) {
+    int e2;
+    const float m2 = frexpf(S, &e2);
+    const float l2m = log2f(m2), ef = static_cast<float>(e2);
+    log2S = ef + l2m;
+    float s1, r1, s2, r2, s3, r3;
+    two_sum(zv, -M, s1, r1);
+    two_sum(s1, -ef * kLn2Hi, s2, r2);
+    two_sum(s2, -kLn2 * l2m, s3, r3);
+    logp = s3;
+    lp_lo = (r1 + r2) + (r3 - ef * kLn2Lo);
+    const float p1 = M * kLog2e, q1 = fmaf(M, kLog2e, -p1);  // M log2(e) = p1 + q1 exactly
+    float c1, f1, c2, f2;
+    two_sum(p1, ef, c1, f1);
+    two_sum(c1, l2m, c2, f2);
+    cL = c2;
+    cL_lo = (f1 + f2) + q1;
+    TtS = Tt / S;
+  } else {
+    log2S = __log2f(S);  // S >= 1: the row's maximum contributes 2^0
+    TtS = __fdividef(Tt, S);
+    logp = zv - fmaf(log2S, kLn2, M);
+    cL = fmaf(M, kLog2e, log2S);
+  }
+  v.H = kLn2 * (log2S - TtS);
+  v.logp = logp;
+
+  // per-token objective and its derivative with respect to logp
+  const float A = a.adv_mode == RL_ADV_GROUP_REWARDS ? cache.A : rs.A;
+  float r = 1.f;
+  if (a.logp_old) {
+    if constexpr (DT == RL_F32) {  // exp of the two-word difference
+      float u, ue;
+      two_sum(logp, -rs.lpo, u, ue);
+      const float r0 = expf(u);
+      r = fmaf(r0, ue + lp_lo, r0);
+    } else {
+      r = __expf(logp - rs.lpo);
+    }
+  }
+  const float rA = r * A;
+  v.pg = fminf(rA, fminf(fmaxf(r, a.clip_lo), a.clip_hi) * A);
+  v.clipped = (A > 0.f && r > a.clip_hi) || (A < 0.f && r < a.clip_lo);
+  const float dpg = v.clipped ? 0.f : rA;
+  float dkl = 0.f;
+  v.kl = 0.f;
+  if (a.ref_logp) {
+    if constexpr (DT == RL_F32) {
+      float d, de;
+      two_sum(rs.rf, -logp, d, de);
+      de -= lp_lo;
+      const float em = expm1f(d);
+      dkl = fmaf(em + 1.f, de, em);
+      v.kl = (em - d) + fmaf(em, de, 0.f);
+    } else {
+      const float d = rs.rf - logp;
+      dkl = expm1f(d);
+      v.kl = dkl - d;
+    }
+  }
+  v.J = v.pg - a.beta * v.kl + a.c_ent * v.H;
+  float g = dpg + a.beta * dkl;
+  if (logp != logp) {  // NaN logp (bad id or NaN logits): poison the row
+    v.J = logp;
+    g = logp;
+  }
+  // pass 2: dz_v = sc [g (p_v - [v == y]) + c_ent p_v (ln p_v + H)]
+  // with x_v = z_v log2(e) - cL:  p_v = 2^x_v, ln p_v = x_v ln 2
+  v.cf.cL = cL;
+  v.cf.cL_lo = cL_lo;
+  v.cf.a0 = sc_row * fmaf(a.c_ent, v.H, g);
+  v.cf.a1 = sc_row * a.c_ent * kLn2;
+  v.cf.gy = sc_row * g;
+  return v;
+}
+
+// Lane 0 adds the row's terms to `acc` and writes its per-row outputs
+// (logp, entropy, row coefficients).
+__device__ __forceinline__ void row_book(const LossArgs& a, long long row, const RowVals& v, int lane,
+                                         double* acc, unsigned int& err) {
+  if (lane != 0) return;
+  acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(v.J) : v.w_row * v.J;
+  acc[1] += v.pg;
+  acc[2] += v.kl;
+  acc[3] += v.H;
+  acc[4] += v.clipped ? 1.0 : 0.0;
+  if (!v.y_ok) err |= RL_DEVERR_ID_RANGE;
+  if (a.logp_out) a.logp_out[row] = v.logp;
+  if (a.entropy_out) a.entropy_out[row] = v.H;
+  if (a.row_coef_out) a.row_coef_out[row] = make_float4(v.cf.cL, v.cf.a0, v.cf.a1, v.cf.gy);
+}
+
+// A masked row needs no logits, only an all-zero gradient row: bulk copies
+// of a zeroed shared-memory block (the copy engine, not the consumers' store
+// path) plus plain stores for a row end that is not a multiple of 16 bytes,
+// and zero per-row outputs.  Whole warp.
+template <class E, int kMode>
+__device__ __forceinline__ void zero_row(const LossArgs& a, uint32_t zeros, long long row, int nelem,
+                                         uint64_t pol, int lane) {
+  if (a.dlogits) {
+    const long long nb16 = static_cast<long long>(nelem) * E::kBytes & ~15LL;  // bulk part of the row
+    unsigned char* d = a.dlogits + row * a.row_bytes;
+    if (lane == 0) {
+      for (long long off = 0; off < nb16; off += kZeroBytes)
+        bulk_store(d + off, zeros, static_cast<uint32_t>(min(static_cast<long long>(kZeroBytes), nb16 - off)),
+                   pol);
+      bulk_commit();
+    }
+    for (long long e = nb16 / E::kBytes + lane; e < nelem; e += 32) E::store1(d + e * E::kBytes, 0.f);
+  }
+  if (lane == 0) {
+    if (a.logp_out) a.logp_out[row] = 0.f;
+    if (a.entropy_out) a.entropy_out[row] = 0.f;
+    if (kMode >= 2 && a.row_coef_out) a.row_coef_out[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 // kStream: rows are streamed twice through the ring (second pass from L2);
-// otherwise each CTA's slice of a row stays in the ring for both passes.
+// otherwise each row stays in the ring for both passes.
 // kMode: 0 the whole loss; 1 (vocabulary shard) pass 1 only, writing each
 // row's partial statistics; 2 (vocabulary shard) merge the gathered shard
 // partials instead of pass 1, then the loss and this shard's gradient; 3 the
 // merge of mode 2 with no columns at all (each row's gradient coefficients
 // are its only per-row output besides logp and entropy): nothing is shared
 // between the warps of a row then, so every consumer warp takes its own rows.
+//
+// Roles (modes 0-2).  The consumer warps stream the ring: pass 1 of a row,
+// then each warp publishes one (m, s, t) partial.  The row warp merges the
+// partials and turns them into the row's loss terms and pass-2
+// coefficients; meanwhile the consumers already run the first kLead chunks
+// of the next row's pass 1, then pass 2 of the row, then the rest of the
+// next row's pass 1.  So a row's merge and scalar arithmetic (a long
+// dependent chain) overlap streaming instead of stalling every consumer
+// warp, and run once per row instead of once per warp.  The producer issues
+// the chunks in exactly that order; xbar[b] (consumers -> row warp) and
+// cbar[b] (row warp -> consumers) alternate between two rows in flight.
 template <int DT, bool kStream, int kMode, bool kEnt>
 __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(const LossArgs a) {
   using E = Elem<DT>;
@@ -633,415 +944,314 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_rank(), csize = cluster_size();
-  const uint32_t cid = cluster_id(), ncl = cluster_count();
-  const int n_parts = static_cast<int>(csize) * kConsumerWarps;  // partials per row
+  const long long cid = blockIdx.x, ncl = gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_addr(&sm.full[s]), 1);
       mbar_init(smem_addr(&sm.empty[s]), kConsumerWarps);
     }
-    mbar_init(smem_addr(&sm.xbar[0]), n_parts);
-    mbar_init(smem_addr(&sm.xbar[1]), n_parts);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&sm.xbar[b]), kConsumerWarps);
+      mbar_init(smem_addr(&sm.cbar[b]), 1);
+      sm.zy[b] = -INFINITY;
+    }
     sm.abort = 0;
     sm.is_last = 0;
     sm.pace = -1;
-    for (int k = 0; k < 5; ++k) sm.acc[k] = 0.0;
     fence_mbar_init();
   }
   __syncthreads();
-  cluster_sync_all();  // every peer's barriers exist before any remote arrive
   // Launched with programmatic stream serialisation: the set-up above overlaps
   // the previous kernel (e.g. the advantages); nothing in global memory is
   // read before that kernel has finished.
   grid_dependency_wait();
 
-  const long long lo = static_cast<long long>(rank) * a.slice;
-  const long long hi = min(a.V, lo + a.slice);
-  const int nelem = hi > lo ? static_cast<int>(hi - lo) : 0;
-  const long long slice_bytes = (static_cast<long long>(nelem) * E::kBytes + 15) & ~15LL;
-  const int nchunks = static_cast<int>((slice_bytes + kChunkBytes - 1) / kChunkBytes);
+  const int nelem = static_cast<int>(a.V);
+  const long long row_bytes16 = (static_cast<long long>(nelem) * E::kBytes + 15) & ~15LL;
+  const int nchunks = static_cast<int>((row_bytes16 + kChunkBytes - 1) / kChunkBytes);
+  constexpr bool kTwoPass = kStream && kMode == 0;  // pass-2 chunks come through the ring again
 
-  if (warp == kConsumerWarps) {
+  // N = number of valid tokens; every CTA counts the whole mask.
+  long long cnt = 0;
+  {
+    long long i0 = 0;
+    if ((reinterpret_cast<uintptr_t>(a.mask) & 15) == 0) {
+      const long long nv = a.R >> 4;
+      const uint4* mv = reinterpret_cast<const uint4*>(a.mask);
+      for (long long i = tid; i < nv; i += kThreads) {
+        const uint4 w = __ldg(mv + i);
+        cnt += (__popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
+                __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u))) >> 3;
+      }
+      i0 = nv << 4;
+    }
+    for (long long i = i0 + tid; i < a.R; i += kThreads) cnt += a.mask[i] != 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) sm.wcount[warp] = cnt;
+    __syncthreads();
+    cnt = 0;
+    for (int w = 0; w < kThreads / 32; ++w) cnt += sm.wcount[w];
+  }
+  const long long N_local = cnt;
+  // A streamed row's second pass runs in reverse chunk order when no row is
+  // masked (its last chunks, loaded most recently, are read again first);
+  // with masked rows, whose zero writes also pass through L2, in load order.
+  const bool rev = kTwoPass && N_local == a.R;
+
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
-    // The warp walks the valid rows; lane 0 issues their copies.
+    // The warp walks this CTA's rows; lane 0 issues the valid rows' copies in
+    // the order the consumers take them.  Without a zero warp it also writes
+    // the masked rows as it passes them: the ring keeps it within a few
+    // chunks of the consumers, so those writes spread over the launch.
+    if (!RL_ZERO_WARP) {
+      for (int i = lane; i < kZeroBytes / 16; i += 32)
+        reinterpret_cast<uint4*>(sm.zeros)[i] = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_shared();
+      __syncwarp();
+    }
     const uint64_t pol_last = RL_STREAM_KEEP_L2 ? policy_evict_last() : policy_evict_normal();
     const uint64_t pol_first = policy_evict_first();
     uint32_t it = 0;
-    bool stop = nchunks == 0;
-    RowWalk<true> walk(cid, ncl);
-    for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R && !stop; row = walk.next(a.mask, ncl, a.R, lane)) {
-      if (lane == 0) {
-        const unsigned char* src = a.logits + row * a.row_bytes + lo * E::kBytes;
-        constexpr int kPasses = (kStream && kMode == 0) ? 2 : 1;
-        for (int pass = 0; pass < kPasses && !stop; ++pass) {
-          const uint64_t pol = (kPasses == 2 && pass == 0) ? pol_last : pol_first;
-          for (int c = 0; c < nchunks; ++c, ++it) {
-            const uint32_t slot = it % kSlots, round = it / kSlots;
-            if (round > 0 &&
-                !wait_bounded<false>(smem_addr(&sm.empty[slot]), (round - 1) & 1, abort_flag)) {
-              stop = true;
-              break;
-            }
-            if (*abort_flag) {
-              stop = true;
-              break;
-            }
-            const uint32_t bytes = static_cast<uint32_t>(
-                min(static_cast<long long>(kChunkBytes), slice_bytes - static_cast<long long>(c) * kChunkBytes));
-            const uint32_t fb = smem_addr(&sm.full[slot]);
-            mbar_arrive_expect_tx(fb, bytes);
-            bulk_load(smem_addr(sm.ring[slot]), src + static_cast<long long>(c) * kChunkBytes, bytes,
-                      fb, pol);
-          }
+    bool stop = false;
+    auto issue = [&](long long row, int c0, int c1, uint64_t pol, bool reverse) {
+      if (lane != 0 || stop) return;
+      const unsigned char* src = a.logits + row * a.row_bytes;
+      for (int i = c0; i < c1; ++i, ++it) {
+        const int c = reverse ? c1 - 1 - (i - c0) : i;
+        const uint32_t slot = it % kSlots, round = it / kSlots;
+        if (round > 0 && !wait_bounded<false>(smem_addr(&sm.empty[slot]), (round - 1) & 1, abort_flag)) {
+          stop = true;
+          return;
         }
+        if (*abort_flag) {
+          stop = true;
+          return;
+        }
+        const uint32_t bytes = static_cast<uint32_t>(
+            min(static_cast<long long>(kChunkBytes), row_bytes16 - static_cast<long long>(c) * kChunkBytes));
+        const uint32_t fb = smem_addr(&sm.full[slot]);
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_load(smem_addr(sm.ring[slot]), src + static_cast<long long>(c) * kChunkBytes, bytes, fb, pol);
+      }
+    };
+    long long prev = -1;  // two-pass order: the valid row whose second pass is still to issue
+    auto valid_row = [&](long long row) {
+      if constexpr (kTwoPass) {
+        if (prev >= 0) {
+          const int lead = min(nchunks, kLeadChunks);
+          issue(row, 0, lead, pol_last, false);
+          issue(prev, 0, nchunks, pol_first, rev);
+          issue(row, lead, nchunks, pol_last, false);
+        } else {
+          issue(row, 0, nchunks, pol_last, false);
+        }
+        prev = row;
+      } else if (kMode != 3) {
+        issue(row, 0, nchunks, pol_first, false);
       }
       stop = __shfl_sync(0xffffffffu, stop, 0);
+    };
+    if constexpr (RL_ZERO_WARP) {
+      RowWalk<true> walk(cid, ncl);
+      if (kMode != 3)
+        for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R && !stop;
+             row = walk.next(a.mask, ncl, a.R, lane))
+          valid_row(row);
+    } else {
+      const uint64_t pol_zero = policy_evict_first();
+      RowScan scan(cid, ncl);
+      while (!stop) {
+        bool valid;
+        const long long row = scan.next(a.mask, ncl, a.R, lane, valid);
+        if (row >= a.R) break;
+        if (valid)
+          valid_row(row);
+        else
+          zero_row<E, kMode>(a, smem_addr(sm.zeros), row, nelem, pol_zero, lane);
+      }
     }
+    if (kTwoPass && prev >= 0) issue(prev, 0, nchunks, pol_first, rev);
     if (lane == 0 && stop && nchunks > 0) {  // let every copy already issued land before this CTA can exit
       for (uint32_t k = it > kSlots ? it - kSlots : 0; k < it; ++k)
         drain_wait(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1);
     }
-  } else if (warp == kConsumerWarps + 1) {
+    if (!RL_ZERO_WARP && lane == 0) bulk_wait_all();  // the zero block is read until the last copy is done
+    return;
+  }
+
+  if (warp == kZeroWarp) {
     // ---------------------------------------------------------------- zero warp
-    // Masked rows need no logits, only an all-zero gradient slice: this warp
-    // writes them while the consumers work on the valid rows, so the masked
-    // rows' stores overlap the valid rows' arithmetic.  It keeps within
+    // Writes the masked rows while the consumers work on the valid rows, so
+    // their stores overlap the valid rows' arithmetic.  It keeps within
     // kZeroLead rows of the consumers, so the writes stay spread over the
     // launch instead of arriving as one burst at its start.
-    // The writes are bulk copies of a zeroed shared-memory block: they go
-    // through the copy engine, not the load/store path that the consumers'
-    // gradient stores keep busy.
     for (int i = lane; i < kZeroBytes / 16; i += 32)
       reinterpret_cast<uint4*>(sm.zeros)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_shared();
     __syncwarp();
     const uint64_t pol = policy_evict_first();
-    const long long nb16 = static_cast<long long>(nelem) * E::kBytes & ~15LL;  // bulk part of a slice
     const volatile long long* pace = &sm.pace;
     RowWalk<false> walk(cid, ncl);
     for (long long row = walk.next(a.mask, ncl, a.R, lane); row < a.R; row = walk.next(a.mask, ncl, a.R, lane)) {
-      if (kMode != 3 && *pace < row - kZeroLead * static_cast<long long>(ncl)) {  // bounded wait, then go on
+      if (kMode != 3 && *pace < row - kZeroLead * ncl) {  // bounded wait, then go on
         const uint64_t t0 = global_ns();
-        while (*pace < row - kZeroLead * static_cast<long long>(ncl) && global_ns() - t0 < kWaitLimitNs)
-          __nanosleep(500);
+        while (*pace < row - kZeroLead * ncl && global_ns() - t0 < kWaitLimitNs) __nanosleep(500);
       }
-      if (a.dlogits) {
-        unsigned char* d = a.dlogits + row * a.row_bytes + lo * E::kBytes;
-        if (lane == 0) {
-          for (long long off = 0; off < nb16; off += kZeroBytes)
-            bulk_store(d + off, smem_addr(sm.zeros),
-                       static_cast<uint32_t>(min(static_cast<long long>(kZeroBytes), nb16 - off)), pol);
-          bulk_commit();
-        }
-        for (long long e = nb16 / E::kBytes + lane; e < nelem; e += 32) E::store1(d + e * E::kBytes, 0.f);
-      }
-      if (rank == 0 && lane == 0) {
-        if (a.logp_out) a.logp_out[row] = 0.f;
-        if (a.entropy_out) a.entropy_out[row] = 0.f;
-        if (kMode >= 2 && a.row_coef_out) a.row_coef_out[row] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      zero_row<E, kMode>(a, smem_addr(sm.zeros), row, nelem, pol, lane);
     }
     if (lane == 0) bulk_wait_all();  // the block is read until the last copy is done
-  } else {
-    // ---------------------------------------------------------------- consumers
-    // the valid rows of this CTA (mode 3: of this warp)
-    const long long rfirst = kMode == 3 ? static_cast<long long>(cid) * kConsumerWarps + warp : cid;
-    const long long rstride = kMode == 3 ? static_cast<long long>(ncl) * kConsumerWarps : ncl;
-    RowWalk<true> walk(rfirst, rstride);
-    long long nrow = walk.next(a.mask, rstride, a.R, lane);
-    RowScalars cur = load_row(a, nrow);  // in flight while the mask is counted
+    return;
+  }
 
-    // N = number of valid tokens; every CTA counts the whole mask.
-    long long cnt = 0;
-    {
-      long long i0 = 0;
-      if ((reinterpret_cast<uintptr_t>(a.mask) & 15) == 0) {
-        const long long nv = a.R >> 4;
-        const uint4* mv = reinterpret_cast<const uint4*>(a.mask);
-        for (long long i = tid; i < nv; i += kConsumerThreads) {
-          const uint4 w = __ldg(mv + i);
-          cnt += (__popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
-                  __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u))) >> 3;
-        }
-        i0 = nv << 4;
+  // ------------------------------------------------------------------ consumers and the row warp
+  // Data parallel over ranks: the means run over every rank's tokens.
+  const long long N = a.global_counts ? a.global_counts[0] : N_local;
+  const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
+  const bool seq_agg = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN || a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM;
+  long long Bp = 0;  // sequences with at least one valid token
+  if (seq_agg && a.global_counts) {
+    Bp = a.global_counts[1];
+  } else if (seq_agg) {
+    const long long nseq = a.R / a.T;
+    long long nb = 0;
+    for (long long b = warp; b < nseq; b += kRedWarps) nb += warp_count_mask(a.mask + b * a.T, a.T, lane) > 0;
+    if (lane == 0) sm.wseq[warp] = nb;
+    named_barrier(kRedBarrier, kRedThreads);
+    for (int w = 0; w < kRedWarps; ++w) Bp += sm.wseq[w];
+  }
+
+  unsigned int err = 0;
+  double wacc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // this warp's sums (lane 0)
+
+  if constexpr (kMode == 3) {
+    // ---------------------------------------------------------------- coefficient-only merge
+    // Each consumer warp takes its own rows; the row warp has none.
+    if (warp < kConsumerWarps) {
+      const long long rstride = ncl * kConsumerWarps;
+      RowWalk<true> walk(cid * kConsumerWarps + warp, rstride);
+      SeqCache cache{-1, 0, 0.f};
+      long long nrow = walk.next(a.mask, rstride, a.R, lane);
+      RowScalars cur = load_row(a, nrow);
+      for (long long row = nrow; row < a.R; row = nrow) {
+        nrow = walk.next(a.mask, rstride, a.R, lane);
+        const RowScalars rs = cur;
+        cur = load_row(a, nrow);
+        float M, S, Tt, zyr;
+        merge_shards(a, row, lane, M, S, Tt, zyr);
+        row_book(a, row, row_values<DT>(a, rs, cache, Bp, sc, M, S, Tt, zyr, lane), lane, wacc, err);
       }
-      for (long long i = i0 + tid; i < a.R; i += kConsumerThreads) cnt += a.mask[i] != 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      if (lane == 0) sm.wcount[warp] = cnt;
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      cnt = 0;
-      for (int w = 0; w < kConsumerWarps; ++w) cnt += sm.wcount[w];
     }
-    const long long N_local = cnt;
-    // Data parallel over ranks: the means run over every rank's tokens.
-    const long long N = a.global_counts ? a.global_counts[0] : N_local;
-    const float sc = N > 0 ? static_cast<float>(static_cast<double>(a.grad_scale) / static_cast<double>(N)) : 0.f;
-    constexpr bool with_entropy = kEnt;  // c_ent != 0: the entropy term is in the gradient
-    const bool seq_agg = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN || a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM;
-    long long Bp = 0;  // sequences with at least one valid token
-    if (seq_agg && a.global_counts) {
-      Bp = a.global_counts[1];
-    } else if (seq_agg) {
-      const long long nseq = a.R / a.T;
-      long long nb = 0;
-      for (long long b = warp; b < nseq; b += kConsumerWarps)
-        nb += warp_count_mask(a.mask + b * a.T, a.T, lane) > 0;
-      if (lane == 0) sm.wseq[warp] = nb;
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      for (int w = 0; w < kConsumerWarps; ++w) Bp += sm.wseq[w];
-    }
-    long long cache_b = -1;  // sequence whose length / advantage this warp holds
-    int cache_L = 0;
-    float cache_A = 0.f;
-
-    unsigned int err = 0;
-    uint32_t it = 0, vrow = 0;
-    bool aborted = false;
-    double wacc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // mode 3: this warp's sums (lane 0)
-
-    for (long long row = nrow; row < a.R; row = nrow) {  // masked rows: the zero warp
-      if (kMode != 3 && tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = row;
-      nrow = walk.next(a.mask, rstride, a.R, lane);
-      const RowScalars rs = cur;
-      cur = load_row(a, nrow);  // next row's scalars, in flight during this row
-      unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes + lo * E::kBytes : nullptr;
-      if (*abort_flag) {
-        aborted = true;
-        break;
-      }
-      // Per-sequence quantities, recomputed by each warp when the sequence changes.
-      const long long bseq = rs.b;
-      if (bseq != cache_b) {
-        cache_b = bseq;
-        if (a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN)
-          cache_L = warp_count_mask(a.mask + bseq * a.T, a.T, lane);
-        if (a.adv_mode == RL_ADV_GROUP_REWARDS) cache_A = warp_group_advantage(a, bseq, lane);
-      }
-      // Loss weight of this token and the gradient scale of its row.
-      double w_row = 1.0;  // token mean: the 1/N is applied once, at the end
-      float sc_row = sc;
-      if (a.agg != RL_AGG_TOKEN_MEAN) {
-        w_row = a.agg == RL_AGG_SEQ_MEAN_TOKEN_MEAN ? 1.0 / (static_cast<double>(Bp) * cache_L)
-              : a.agg == RL_AGG_SEQ_MEAN_TOKEN_SUM  ? 1.0 / static_cast<double>(Bp)
-                                                     : a.agg_w;
-        sc_row = static_cast<float>(static_cast<double>(a.grad_scale) * w_row);
-      }
-      const long long y = rs.y;
-      // Where the sampled id sits in this CTA's slice: chunk cy, vector jy of
-      // the chunk (owned by thread ty as its vector qy), element iy.
-      int cy = -1, jy = 0, iy = 0, ty = -1;
-      const long long yl = y - a.v_offset;  // column of y in this shard
-      if (yl >= lo && yl < hi) {
-        const int off = static_cast<int>(yl - lo);
-        cy = off / kChunkElems;
-        jy = (off % kChunkElems) / kVec;
-        iy = off % kVec;
-        ty = jy % kConsumerThreads;
-      }
-
-      const uint32_t base = it;
-      float M = -INFINITY, S = 0.f, Tt = 0.f, zyr = -INFINITY;
+  } else if (warp == kRowWarp) {
+    // ---------------------------------------------------------------- row warp
+    RowWalk<true> walk(cid, ncl);
+    SeqCache cache{-1, 0, 0.f};
+    long long row = walk.next(a.mask, ncl, a.R, lane);
+    RowScalars rs = load_row(a, row);
+    for (uint32_t k = 0; row < a.R; ++k) {
+      const long long nrow = walk.next(a.mask, ncl, a.R, lane);
+      const RowScalars nrs = load_row(a, nrow);  // next row's scalars, in flight during this row
+      const uint32_t b = k & 1;
+      float M, S, Tt, zyr;
       if constexpr (kMode < 2) {
-        // ---- pass 1: online statistics of this thread's share of the slice
-        ThreadStats st;
-        stats_init(st);
-        float zy = -INFINITY;
-        for (int c = 0; c < nchunks; ++c) {
-          const uint32_t k = it++, slot = k % kSlots;
-          wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
-          const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
-          const int c0 = c * kChunkElems;
-          if (c0 + kChunkElems <= nelem)
-            accumulate_chunk<E>(buf, st);
-          else
-            accumulate_chunk_tail<E>(buf, c0 + tid * kVec, nelem, st);
-          if (c == cy && tid == ty) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + jy * 16), iy);
-          if (kStream || kMode == 1) {  // re-read from L2 in pass 2 (or no pass 2): free it now
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
-          }
-        }
-
-        // ---- one partial per warp; the C * 16 partials meet through xbar[b]
-        float m = st.m, s = 0.f, t = 0.f;
-  #pragma unroll
-        for (int q = 0; q < kVecsPerThread; ++q) {
-          s += st.s[q].x + st.s[q].y;
-          t += st.t[q].x + st.t[q].y;
-        }
-  #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-          const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-          const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
-          merge_stats(m, s, t, m2, s2, t2);
-          zy = max_nan(zy, __shfl_xor_sync(0xffffffffu, zy, o));
-        }
-        const uint32_t b = vrow & 1;
-        if (!RL_CLUSTER_RESIDENT || csize == 1) {  // one CTA per row: CTA-scope publish and wait
-          if (lane == 0) {
-            sm.xpart[b][warp] = make_float4(m, s, t, zy);
-            mbar_arrive(smem_addr(&sm.xbar[b]));
-          }
-          wait_bounded<false>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
-        } else {  // cluster: every rank gets every warp's partial through DSMEM
-          if (lane == 0) {
-            const float4 P = make_float4(m, s, t, zy);
-            const uint32_t xa = smem_addr(&sm.xpart[b][rank * kConsumerWarps + warp]);
-            const uint32_t ba = smem_addr(&sm.xbar[b]);
-            for (uint32_t q = 0; q < csize; ++q) st_cluster_f4(map_to_rank(xa, q), P);
-            for (uint32_t q = 0; q < csize; ++q) mbar_arrive_remote(map_to_rank(ba, q));
-          }
-          wait_bounded<true>(smem_addr(&sm.xbar[b]), (vrow >> 1) & 1, abort_flag);
-        }
-        for (int p = lane; p < n_parts; p += 32) {
-          const float4 P = sm.xpart[b][p];
-          merge_stats(M, S, Tt, P.x, P.y, P.z);
-          zyr = max_nan(zyr, P.w);
-        }
-  #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-          const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
-          merge_stats(M, S, Tt, m2, s2, t2);
-          zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
-        }
-        // every lane of every warp uses lane 0's bits
-        M = __shfl_sync(0xffffffffu, M, 0);
-        S = __shfl_sync(0xffffffffu, S, 0);
-        Tt = __shfl_sync(0xffffffffu, Tt, 0);
-        zyr = __shfl_sync(0xffffffffu, zyr, 0);
+        // the consumer warps' partials of this row
+        if (!wait_bounded<false>(smem_addr(&sm.xbar[b]), (k >> 1) & 1, abort_flag)) break;
+        const float4 P = lane < kConsumerWarps ? sm.xpart[b][lane] : make_float4(kFloor, 0.f, 0.f, 0.f);
+        M = P.x;
+        S = P.y;
+        Tt = P.z;
+        warp_stats(M, S, Tt, true);
+        zyr = sm.zy[b];
+        __syncwarp();
+        if (lane == 0) sm.zy[b] = -INFINITY;  // for the row after next (written after cbar[b] below)
       } else {
-        // ---- the gathered shard partials stand in for pass 1
-        if (!kStream) {  // the row's chunks stay in the ring for pass 2
-          for (int c = 0; c < nchunks; ++c) {
-            const uint32_t k = it++;
-            wait_bounded<false>(smem_addr(&sm.full[k % kSlots]), (k / kSlots) & 1, abort_flag);
-          }
-        }
-        for (int k = lane; k < a.n_shards; k += 32) {  // shard order, then a fixed shuffle tree
-          const float4 P = __ldg(&a.shard_partials[static_cast<long long>(k) * a.R + row]);
-          merge_stats(M, S, Tt, P.x, P.y, P.z);
-          zyr = max_nan(zyr, P.w);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-          const float t2 = __shfl_xor_sync(0xffffffffu, Tt, o);
-          merge_stats(M, S, Tt, m2, s2, t2);
-          zyr = max_nan(zyr, __shfl_xor_sync(0xffffffffu, zyr, o));
-        }
-        M = __shfl_sync(0xffffffffu, M, 0);
-        S = __shfl_sync(0xffffffffu, S, 0);
-        Tt = __shfl_sync(0xffffffffu, Tt, 0);
-        zyr = __shfl_sync(0xffffffffu, zyr, 0);
+        // consumers took row k - 2's coefficients before coef[b] is rewritten
+        if (k >= 2 && !wait_bounded<false>(smem_addr(&sm.xbar[b]), ((k - 2) >> 1) & 1, abort_flag)) break;
+        merge_shards(a, row, lane, M, S, Tt, zyr);
       }
       if constexpr (kMode == 1) {  // this shard's statistics of the row, for the exchange
-        if (rank == 0 && tid == 0) a.partials_out[row] = make_float4(M, S, Tt, zyr);
-        ++vrow;
-        continue;
-      }
-
-      const bool y_ok = (y >= 0) && (y < a.v_total);
-      const float zv = y_ok ? zyr : __int_as_float(0x7fc00000);
-      // lse = M + ln S, logp = z_y - lse and cL = M log2(e) + log2 S (pass 2's
-      // exponent offset).  fp32 logits keep logp and cL in two words: with
-      // S = m 2^e (m in [0.5, 1)), log2 S = e + log2 m and ln S = e ln 2 + ln m,
-      // summed without rounding away the bits a single fp32 lse (|lse| ~ 10)
-      // would lose; 16-bit logits need no more than one word.
-      float log2S, logp, lp_lo = 0.f, cL, cL_lo = 0.f;
-      if constexpr (DT == RL_F32) {
-        int e2;
-        const float m2 = frexpf(S, &e2);
-        const float l2m = log2f(m2), ef = static_cast<float>(e2);
-        log2S = ef + l2m;
-        float s1, r1, s2, r2, s3, r3;
-        two_sum(zv, -M, s1, r1);
-        two_sum(s1, -ef * kLn2Hi, s2, r2);
-        two_sum(s2, -kLn2 * l2m, s3, r3);
-        logp = s3;
-        lp_lo = (r1 + r2) + (r3 - ef * kLn2Lo);
-        const float p1 = M * kLog2e, q1 = fmaf(M, kLog2e, -p1);  // M log2(e) = p1 + q1 exactly
-        float c1, f1, c2, f2;
-        two_sum(p1, ef, c1, f1);
-        two_sum(c1, l2m, c2, f2);
-        cL = c2;
-        cL_lo = (f1 + f2) + q1;
+        if (lane == 0) {
+          a.partials_out[row] = make_float4(M, S, Tt, zyr);
+          mbar_arrive(smem_addr(&sm.cbar[b]));
+        }
       } else {
-        log2S = log2f(S);
-        logp = zv - fmaf(log2S, kLn2, M);
-        cL = fmaf(M, kLog2e, log2S);
+        const RowVals v = row_values<DT>(a, rs, cache, Bp, sc, M, S, Tt, zyr, lane);
+        if (lane == 0) {  // the consumers' coefficients first, the bookkeeping after
+          sm.coef[b] = v.cf;
+          mbar_arrive(smem_addr(&sm.cbar[b]));
+        }
+        row_book(a, row, v, lane, wacc, err);
       }
-      const float H = kLn2 * (log2S - Tt / S);
-
-      // ---- per-token objective and its derivative with respect to logp
-      const float A = a.adv_mode == RL_ADV_GROUP_REWARDS ? cache_A : rs.A;
-      float r = 1.f;
-      if (a.logp_old) {
-        if constexpr (DT == RL_F32) {  // exp of the two-word difference
-          float u, ue;
-          two_sum(logp, -rs.lpo, u, ue);
-          const float r0 = expf(u);
-          r = fmaf(r0, ue + lp_lo, r0);
-        } else {
-          r = expf(logp - rs.lpo);
+      row = nrow;
+      rs = nrs;
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    uint32_t it = 0;  // position in the ring
+    // pass 1 over chunks [c0, c1) of a row: this thread's online statistics
+    auto pass1 = [&](int c0, int c1, ThreadStats& st, float& zy, const IdPos& p) {
+      for (int c = c0; c < c1; ++c) {
+        const uint32_t k = it++, slot = k % kSlots;
+        wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
+        const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
+        const int e0 = c * kChunkElems;
+        if (e0 + kChunkElems <= nelem)
+          accumulate_chunk<E>(buf, st);
+        else
+          accumulate_chunk_tail<E>(buf, e0 + tid * kVec, nelem, st);
+        if (c == p.cy) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + p.jv / kVec * 16), p.jv % kVec);
+        if (kStream || kMode == 1) {  // read again from L2 in pass 2 (or no pass 2): free it now
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
         }
       }
-      const float rA = r * A;
-      const float pg = fminf(rA, fminf(fmaxf(r, a.clip_lo), a.clip_hi) * A);
-      const bool clipped = (A > 0.f && r > a.clip_hi) || (A < 0.f && r < a.clip_lo);
-      const float dpg = clipped ? 0.f : rA;
-      float kl = 0.f, dkl = 0.f;
-      if (a.ref_logp) {
-        if constexpr (DT == RL_F32) {
-          float d, de;
-          two_sum(rs.rf, -logp, d, de);
-          de -= lp_lo;
-          const float em = expm1f(d);
-          dkl = fmaf(em + 1.f, de, em);
-          kl = (em - d) + fmaf(em, de, 0.f);
-        } else {
-          const float d = rs.rf - logp;
-          dkl = expm1f(d);
-          kl = dkl - d;
-        }
+    };
+    // this thread's statistics folded into one (m, s, t)
+    auto fold = [&](const ThreadStats& st, float& m, float& s, float& t) {
+      m = st.m;
+      s = t = 0.f;
+#pragma unroll
+      for (int q = 0; q < kVecsPerThread; ++q) {
+        s += st.s[q].x + st.s[q].y;
+        t += st.t[q].x + st.t[q].y;
       }
-      float J = pg - a.beta * kl + a.c_ent * H;
-      float g = dpg + a.beta * dkl;
-      if (logp != logp) {  // NaN logp (bad id or NaN logits): poison the row
-        J = logp;
-        g = logp;
+    };
+    // the warp's partial of row k for the row warp (after row k - 2's partials
+    // were taken); (m0, s0, t0): this thread's fold of the row's first chunks
+    auto publish = [&](uint32_t k, const ThreadStats& st, float m0, float s0, float t0, float zy,
+                       const IdPos& p) {
+      float m, s, t;
+      fold(st, m, s, t);
+      merge_stats(m, s, t, m0, s0, t0);
+      warp_stats(m, s, t, false);
+      const uint32_t b = k & 1;
+      if (k >= 2) wait_bounded<false>(smem_addr(&sm.cbar[b]), ((k - 2) >> 1) & 1, abort_flag);
+      if (p.cy >= 0) sm.zy[b] = zy;
+      __syncwarp();
+      if (lane == 0) {
+        sm.xpart[b][warp] = make_float4(m, s, t, 0.f);
+        mbar_arrive(smem_addr(&sm.xbar[b]));
       }
-      if (rank == 0 && (kMode == 3 ? lane == 0 : tid == 0)) {
-        double* acc = kMode == 3 ? wacc : sm.acc;
-        acc[0] += a.agg == RL_AGG_TOKEN_MEAN ? static_cast<double>(J) : w_row * J;
-        acc[1] += pg;
-        acc[2] += kl;
-        acc[3] += H;
-        acc[4] += clipped ? 1.0 : 0.0;
-        if (!y_ok) err |= RL_DEVERR_ID_RANGE;
-        if (a.logp_out) a.logp_out[row] = logp;
-        if (a.entropy_out) a.entropy_out[row] = H;
+    };
+    // pass 2 of row `row` (the k-th of this CTA; resident rows start at ring position `base`)
+    auto pass2 = [&](long long row, uint32_t k, uint32_t base, const IdPos& p) {
+      const uint32_t b = k & 1;
+      wait_bounded<false>(smem_addr(&sm.cbar[b]), (k >> 1) & 1, abort_flag);
+      const RowCoef cf = sm.coef[b];
+      if (kMode == 2) {  // coef[b] taken: the row warp may rewrite it for row k + 2
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.xbar[b]));
       }
-
-      // ---- pass 2: dz_v = sc [g (p_v - [v == y]) + c_ent p_v (ln p_v + H)]
-      //      with x_v = z_v log2(e) - (M log2(e) + log2 S):  p_v = 2^x_v, ln p_v = x_v ln 2
-      const float a0 = sc_row * fmaf(a.c_ent, H, g);
-      const float a1 = sc_row * a.c_ent * kLn2;
-      const float gy = sc_row * g;
-      if (kMode >= 2 && a.row_coef_out && rank == 0 && (kMode == 3 ? lane == 0 : tid == 0))
-        a.row_coef_out[row] = make_float4(cL, a0, a1, gy);
-      for (int c = 0; c < nchunks; ++c) {
+      unsigned char* drow = a.dlogits ? a.dlogits + row * a.row_bytes : nullptr;
+      for (int i = 0; i < nchunks; ++i) {
+        const int c = rev ? nchunks - 1 - i : i;
         uint32_t slot;
-        if (kStream) {
-          const uint32_t k = it++;
-          slot = k % kSlots;
-          wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
+        if (kStream || kMode == 2) {
+          const uint32_t kk = it++;
+          slot = kk % kSlots;
+          wait_bounded<false>(smem_addr(&sm.full[slot]), (kk / kSlots) & 1, abort_flag);
         } else {
           slot = (base + c) % kSlots;
         }
@@ -1054,10 +1264,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
             for (int q = 0; q < kVecsPerThread; ++q) {
               float d[kVec];
               const uint4 w = ld_shared_v4(buf + (tid + q * kConsumerThreads) * 16);
-              if (with_entropy)
-                grad_vec<E, true>(w, cL, cL_lo, a0, a1, d);
-              else
-                grad_vec<E, false>(w, cL, cL_lo, a0, a1, d);
+              grad_vec<E, kEnt>(w, cf.cL, cf.cL_lo, cf.a0, cf.a1, d);
               st_global_cs_v4(dst + q * kConsumerThreads * 16, E::pack(d));
             }
           } else {
@@ -1067,10 +1274,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
               if (e0 < nelem) {
                 float d[kVec];
                 const uint4 w = ld_shared_v4(buf + (tid + q * kConsumerThreads) * 16);
-                if (with_entropy)
-                  grad_vec<E, true>(w, cL, cL_lo, a0, a1, d);
-                else
-                  grad_vec<E, false>(w, cL, cL_lo, a0, a1, d);
+                grad_vec<E, kEnt>(w, cf.cL, cf.cL_lo, cf.a0, cf.a1, d);
                 unsigned char* o = dst + q * kConsumerThreads * 16;
                 if (nelem - e0 >= kVec) {
                   st_global_cs_v4(o, E::pack(d));
@@ -1082,19 +1286,16 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
               }
             }
           }
-          if (c == cy && tid == ty) {
+          if (c == p.cy) {
             // the owner of the sampled id rewrites its vector with the -g term
             // (after its own store of that vector, so program order settles it)
             float d[kVec];
-            const uint4 w = ld_shared_v4(buf + jy * 16);
-            if (with_entropy)
-              grad_vec<E, true>(w, cL, cL_lo, a0, a1, d);
-            else
-              grad_vec<E, false>(w, cL, cL_lo, a0, a1, d);
+            const uint4 w = ld_shared_v4(buf + p.jv / kVec * 16);
+            grad_vec<E, kEnt>(w, cf.cL, cf.cL_lo, cf.a0, cf.a1, d);
 #pragma unroll
             for (int i = 0; i < kVec; ++i)
-              if (i == iy) d[i] -= gy;
-            const int e0 = c0 + jy * kVec;
+              if (i == p.jv % kVec) d[i] -= cf.gy;
+            const int e0 = c0 + p.jv / kVec * kVec;
             unsigned char* o = drow + static_cast<long long>(e0) * E::kBytes;
             if (nelem - e0 >= kVec) {
               st_global_cs_v4(o, E::pack(d));
@@ -1108,69 +1309,128 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
       }
-      ++vrow;
-    }
-    if (tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = a.R + 1;  // release the zero warp
-    if constexpr (kMode == 3) {  // the warps' sums, combined in warp order
-      if (lane == 0) {
-        for (int k = 0; k < 5; ++k) sm.wred[warp][k] = wacc[k];
-        if (err) {
-          atomicOr(&a.ws->status, err);
-          __threadfence();
+    };
+
+    // the rows of this CTA; the id of the row after the current one is loaded a row ahead
+    RowWalk<true> walk(cid, ncl);
+    long long cur = walk.next(a.mask, ncl, a.R, lane);
+    long long nxt = walk.next(a.mask, ncl, a.R, lane);
+    IdPos pc = id_pos<kChunkElems, kVec>(a, cur < a.R ? a.ids[cur] : 0, tid);
+    long long y_nxt = nxt < a.R ? a.ids[nxt] : 0;
+    auto advance = [&]() {
+      cur = nxt;
+      pc = id_pos<kChunkElems, kVec>(a, y_nxt, tid);
+      nxt = walk.next(a.mask, ncl, a.R, lane);
+      y_nxt = nxt < a.R ? a.ids[nxt] : 0;
+    };
+    uint32_t k = 0;
+    if constexpr (kMode == 0) {
+      // Each step: the first `lead` chunks of the current row's pass 1, pass 2
+      // of the previous row, then the rest of the current row's pass 1 (the
+      // first step has no previous row, the last no current one).  One copy
+      // of each pass's code in the loop keeps the kernel's instruction
+      // footprint small.
+      long long prev = -1;
+      IdPos pp = pc;
+      uint32_t kp = 0, base_p = 0;
+      while ((cur < a.R || prev >= 0) && !*abort_flag) {
+        const bool has_cur = cur < a.R;
+        if (RL_ZERO_WARP && tid == 0 && has_cur) *reinterpret_cast<volatile long long*>(&sm.pace) = cur;
+        const int lead = !has_cur ? 0 : prev >= 0 ? min(nchunks, kLeadChunks) : nchunks;
+        const uint32_t base = it;  // resident rows: ring position of the current row's first chunk
+        ThreadStats st;
+        stats_init(st);
+        float zy = -INFINITY, m0 = kFloor, s0 = 0.f, t0 = 0.f;
+#pragma unroll 1
+        for (int seg = 0; seg < 2; ++seg) {
+          const int c0 = seg == 0 ? 0 : lead;
+          const int c1 = !has_cur ? 0 : seg == 0 ? lead : nchunks;
+          pass1(c0, c1, st, zy, pc);
+          if (seg == 0) {
+            if (lead > 0) {  // the current row's first chunks, kept as one (m, s, t) over pass 2
+              fold(st, m0, s0, t0);
+              stats_init(st);
+            }
+            if (prev >= 0) pass2(prev, kp, base_p, pp);
+          }
+        }
+        if (has_cur) publish(k, st, m0, s0, t0, zy, pc);
+        prev = has_cur ? cur : -1;
+        pp = pc;
+        kp = k;
+        base_p = base;
+        if (has_cur) {
+          advance();
+          ++k;
         }
       }
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      if (tid == 0)
-        for (int w = 0; w < kConsumerWarps; ++w)
-          for (int k = 0; k < 5; ++k) sm.acc[k] += sm.wred[w][k];
-      err = 0;
+    } else {
+      for (; cur < a.R && !*abort_flag; ++k) {
+        if (RL_ZERO_WARP && tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = cur;
+        if constexpr (kMode == 1) {
+          ThreadStats st;
+          stats_init(st);
+          float zy = -INFINITY;
+          pass1(0, nchunks, st, zy, pc);
+          publish(k, st, kFloor, 0.f, 0.f, zy, pc);
+        } else {
+          pass2(cur, k, 0, pc);
+        }
+        advance();
+      }
     }
+    if (RL_ZERO_WARP && tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = a.R + 1;  // release the zero warp
+  }
 
-    // ---- per-CTA partial, then the last CTA reduces all partials in CTA order
-    if (tid == 0) {
-      WsPartial& P = a.partials[blockIdx.x];
-      for (int k = 0; k < 5; ++k) P.v[k] = sm.acc[k];
-      if (aborted || *abort_flag) err |= RL_DEVERR_TIMEOUT;
-      if (err) atomicOr(&a.ws->status, err);
-      __threadfence();
-      const unsigned int ticket = atomicInc(&a.ws->ticket, gridDim.x - 1);
-      sm.is_last = (ticket == gridDim.x - 1);
+  // ---- per-CTA partial (the warps' sums in warp order), then the last CTA
+  //      reduces all partials in CTA order
+  if (lane == 0) {
+    for (int q = 0; q < 5; ++q) sm.wred[warp][q] = wacc[q];
+    if (err) atomicOr(&a.ws->status, err);
+  }
+  named_barrier(kRedBarrier, kRedThreads);
+  if (tid == 0) {
+    WsPartial& P = a.partials[blockIdx.x];
+    for (int q = 0; q < 5; ++q) {
+      double v = 0.0;
+      for (int w = 0; w < kRedWarps; ++w) v += sm.wred[w][q];
+      P.v[q] = v;
     }
-    named_barrier(kConsumerBarrier, kConsumerThreads);
-    if (sm.is_last) {
-      __threadfence();
-      double v[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
-      for (int i = tid; i < static_cast<int>(gridDim.x); i += kConsumerThreads)
-        for (int k = 0; k < 5; ++k) v[k] += __ldcg(&a.partials[i].v[k]);
-      for (int k = 0; k < 5; ++k) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
-      }
-      if (lane == 0)
-        for (int k = 0; k < 5; ++k) sm.wred[warp][k] = v[k];
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      if (tid == 0) {
-        double tot[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
-        for (int w = 0; w < kConsumerWarps; ++w)
-          for (int k = 0; k < 5; ++k) tot[k] += sm.wred[w][k];
-        const unsigned int stw = atomicExch(&a.ws->status, 0u);
-        a.ws->last_status = stw;
-        rl_loss_stats out;
-        const double inv = N > 0 ? 1.0 / static_cast<double>(N) : 0.0;
-        out.loss = a.agg == RL_AGG_TOKEN_MEAN ? -tot[0] * inv : (N > 0 ? -tot[0] : 0.0);
-        out.pg_term = tot[1] * inv;
-        out.kl_term = tot[2] * inv;
-        out.ent_term = tot[3] * inv;
-        out.clip_frac = tot[4] * inv;
-        out.n_tokens = N_local;
-        out.n_clipped = static_cast<long long>(tot[4]);
-        out.device_error = static_cast<int>(stw);
-        out.reserved = 0;
-        *a.stats = out;
-      }
+    if (*abort_flag) atomicOr(&a.ws->status, static_cast<unsigned int>(RL_DEVERR_TIMEOUT));
+    __threadfence();
+    const unsigned int ticket = atomicInc(&a.ws->ticket, gridDim.x - 1);
+    sm.is_last = (ticket == gridDim.x - 1);
+  }
+  named_barrier(kRedBarrier, kRedThreads);
+  if (sm.is_last) {
+    __threadfence();
+    double v[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+    for (int i = tid; i < static_cast<int>(gridDim.x); i += kRedThreads)
+      for (int q = 0; q < 5; ++q) v[q] += __ldcg(&a.partials[i].v[q]);
+    for (int q = 0; q < 5; ++q) v[q] = warp_sum_d(v[q]);
+    if (lane == 0)
+      for (int q = 0; q < 5; ++q) sm.wred[warp][q] = v[q];
+    named_barrier(kRedBarrier, kRedThreads);
+    if (tid == 0) {
+      double tot[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+      for (int w = 0; w < kRedWarps; ++w)
+        for (int q = 0; q < 5; ++q) tot[q] += sm.wred[w][q];
+      const unsigned int stw = atomicExch(&a.ws->status, 0u);
+      a.ws->last_status = stw;
+      rl_loss_stats out;
+      const double inv = N > 0 ? 1.0 / static_cast<double>(N) : 0.0;
+      out.loss = a.agg == RL_AGG_TOKEN_MEAN ? -tot[0] * inv : (N > 0 ? -tot[0] : 0.0);
+      out.pg_term = tot[1] * inv;
+      out.kl_term = tot[2] * inv;
+      out.ent_term = tot[3] * inv;
+      out.clip_frac = tot[4] * inv;
+      out.n_tokens = N_local;
+      out.n_clipped = static_cast<long long>(tot[4]);
+      out.device_error = static_cast<int>(stw);
+      out.reserved = 0;
+      *a.stats = out;
     }
   }
-  cluster_sync_all();  // no CTA leaves while a peer may still touch its shared memory
 }
 
 // ------------------------------------------------------------------ host side
@@ -1184,37 +1444,19 @@ int elem_bytes(rl_dtype dt) {
 }
 
 struct Plan {
-  int cluster;      // CTAs per row
-  int n_clusters;   // clusters (rows in flight) in the persistent grid
-  long long slice;  // vocabulary elements per CTA
+  int cluster;      // CTAs per row (always 1; the launch shape reports it)
+  int n_clusters;   // CTAs (rows in flight) in the persistent grid
   bool stream;      // rows streamed twice (second pass from L2)
 };
 
-// Row layout: a row that fits the ring twice over stays on chip in one CTA;
-// a longer one is streamed (or, in comparison builds, split over the
-// smallest cluster whose slices fit the ring with room to prefetch).
+// Row layout: a row that fits the ring twice over stays in shared memory for
+// both passes; a longer one is streamed.
 bool choose_layout(int es, long long V, Plan* p) {
   if (V > (1LL << 30)) return false;  // element offsets within a row are 32-bit
   const long long row_chunks = ((V * es + 15) / 16 * 16 + kChunkBytes - 1) / kChunkBytes;
   p->cluster = 1;
-  p->slice = V;
-  p->stream = false;
-  if (row_chunks <= kMaxResidentChunks) return true;
-  if (!RL_CLUSTER_RESIDENT) {
-    p->stream = true;
-    return true;
-  }
-  const long long align = 16 / es;
-  for (int c = 2; c <= kMaxCluster; ++c) {
-    long long s = (V + c - 1) / c;
-    s = (s + align - 1) / align * align;
-    if ((s * es + kChunkBytes - 1) / kChunkBytes <= kSlots - 3) {
-      p->cluster = c;
-      p->slice = s;
-      return true;
-    }
-  }
-  return false;
+  p->stream = row_chunks > kMaxResidentChunks;
+  return true;
 }
 
 // The entropy term is a template argument (c_ent != 0); the statistics-only
@@ -1413,7 +1655,6 @@ RL_INTERNAL rl_status fwd_bwd(const rl_policy_loss_desc* d, void* stream) {
   args.T = T > 0 ? T : 1;
   args.V = V;
   args.row_bytes = row_bytes;
-  args.slice = pl.slice;
   args.adv_mode = d->adv_layout;
   args.group_size = d->group_size;
   args.ddof = d->ddof;
@@ -1476,7 +1717,10 @@ namespace {
 // Rows (this call's columns) of at most this many bytes take the short-row
 // build: two CTAs per SM measured faster up to 100 KB rows (V = 50,000
 // bf16) and slower from 128 KB on when most rows are masked.
-constexpr long long kShortRowBytes = 102400;
+#ifndef RL_SHORT_ROW_BYTES
+#define RL_SHORT_ROW_BYTES 102400
+#endif
+constexpr long long kShortRowBytes = RL_SHORT_ROW_BYTES;
 
 bool short_rows(rl_dtype dtype, long long V) {
   const int es = elem_bytes(dtype);

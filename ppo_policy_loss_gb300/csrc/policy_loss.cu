@@ -142,7 +142,9 @@ static_assert(kConsumerWarps <= 32, "the row warp takes one consumer partial per
 static_assert(kLeadChunks >= 0, "chunks of look-ahead");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kRedBarrier = 1;  // named barrier id (0 is __syncthreads): consumers + row warp
-constexpr int kZeroBytes = kChunkBytes / 2;  // zero block the masked rows are copied from
+// Zero block the masked rows are copied from (16 KB: with it two CTAs of the
+// short-row build fill the SM's 228 KB of shared memory).
+constexpr int kZeroBytes = 16384;
 constexpr long long kZeroLead = 8;           // rows a zero warp may run ahead of the consumers
 
 // A row's pass-2 coefficients: d_v = 2^x (a0 + a1 x) with x = z log2(e) - cL

@@ -577,10 +577,11 @@ rl_status rl_lmhead_plan(long long R, long long D, long long V, size_t workspace
 
 /*
  * The launch shape rl_policy_loss_fwd_bwd would use on the current device for
- * this row shape: CTAs per cluster (one vocabulary slice each), clusters in
- * the persistent grid and dynamic shared memory per CTA.  Rows of more than
- * 100 KB (V * element size) run one 576-thread CTA per SM; shorter rows run
- * two 320-thread CTAs per SM, so n_clusters is twice the SM count there.
+ * this row shape: CTAs per cluster (always 1: each CTA holds whole rows),
+ * CTAs in the persistent grid and dynamic shared memory per CTA.  Rows of
+ * more than 100 KB (V * element size) run one 608-thread CTA per SM; shorter
+ * rows run two 320-thread CTAs per SM, so n_clusters is twice the SM count
+ * there.
  * Host-only query.  Errors as for rl_policy_loss_fwd_bwd's shape checks.
  */
 rl_status rl_policy_loss_launch_shape(rl_dtype dtype, long long V, long long n_rows,

@@ -33,9 +33,11 @@ def _built():
 
 
 def _run_both(w, ld=None, grad_scales=(1.0, "N"), in_place=False, with_old=True,
-              with_ref=None):
-    """Full element-wise parity for a small workload."""
+              with_ref=None, ids=None):
+    """Full element-wise parity for a small workload (``ids`` replaces the sampled ids)."""
     small, logits = build_case(w, ld=ld)
+    if ids is not None:
+        small["ids"] = np.asarray(ids, dtype=np.int64)
     V, R, B, T = w.V, w.R, w.B, w.T
     ldv = logits.stride(0)
     mask, ids = small["mask"], small["ids"]
@@ -116,8 +118,52 @@ SMALL = {
     "bf16_v51208_long_min": W["qwen3_0p6b_grpo"].scaled(n_prompts=2, group=4, T=8, V=51208,
                                                         lengths=("uniform", 1, 8), c_ent=0.01),
 }
+# No masked row: a streamed row's second pass runs in reverse chunk order.
+ALL_VALID = {
+    "bf16_v151936_long_all_valid": W["ppo_gae"].scaled(n_prompts=8, T=4),
+    "bf16_v300001_long_all_valid": W["large_grpo"].scaled(n_prompts=1, group=4, T=4, V=300001,
+                                                          lengths=("full",), c_ent=0.0),
+    "f32_v100000_long_all_valid": W["tiny_grpo"].scaled(n_prompts=1, group=4, T=4, V=100000,
+                                                        lengths=("full",)),
+    "f16_v32000_short_all_valid": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8,
+                                                            lengths=("full",)),
+    "f16_v40003_short_all_valid": W["long_seq_grpo"].scaled(n_prompts=1, group=4, T=8, V=40003,
+                                                            lengths=("full",), c_ent=0.0,
+                                                            beta=0.04),
+    "bf16_v16384_short_resident_all_valid": W["qwen3_0p6b_grpo"].scaled(
+        n_prompts=2, group=4, T=8, V=16384, lengths=("full",), c_ent=0.01),
+}
+SMALL.update(ALL_VALID)
 PADDED_LD = {"f32_v12345_ragged": 12348, "bf16_v1001_ragged": 1008, "f16_v7_tiny": 8,
-             "bf16_v300001_stream": 300008}
+             "bf16_v300001_stream": 300008, "bf16_v300001_long_all_valid": 300008,
+             "f16_v40003_short_all_valid": 40008}
+
+
+def _edge_ids(w, chunk_bytes, es, n):
+    """Sampled ids on the edges of the ring's chunks and of the row: the first and
+    last column, both sides of each chunk boundary, and the last 8 columns."""
+    per = chunk_bytes // es
+    cols = [0, 1, w.V - 1, w.V - 2]
+    for c in range(per, w.V, per):
+        cols += [c - 1, c]
+    cols += list(range(max(0, w.V - 8), w.V))
+    cols = np.array(sorted(set(cols)), dtype=np.int64)
+    return cols[np.arange(n) % cols.size]
+
+
+@pytest.mark.parametrize("name,chunk", [
+    ("bf16_v151936_long_all_valid", 32768),   # long-row build, streamed, reverse order
+    ("bf16_v300001_stream", 32768),            # long-row build, streamed, load order
+    ("f16_v40003_short_all_valid", 16384),     # short-row build, streamed, reverse order
+    ("f16_v49152_stream", 16384),              # short-row build, streamed, load order
+    ("bf16_v16384_short_resident_all_valid", 16384),  # short-row build, resident rows
+])
+def test_sampled_id_on_chunk_edges(name, chunk):
+    """The sampled logit is read in pass 1 and its -g term written in pass 2 by the
+    thread that holds it: ids on every chunk edge, in both pass-2 orders."""
+    w = SMALL[name]
+    es = {"f32": 4, "bf16": 2, "f16": 2}[w.dtype]
+    _run_both(w, ld=PADDED_LD.get(name), ids=_edge_ids(w, chunk, es, w.R))
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))

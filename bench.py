@@ -408,7 +408,7 @@ def run_gpu(args):
         "config": {"workload": f"{args.workload}: {DESCRIBE.get(args.workload, '')}",
                    "B": w.B, "T": w.T, "V": w.V, "rows": w.R, "valid_tokens": n_valid,
                    "slice": (f"profiling shape: {w.B} sequences x T={w.T}, V={w.V} {w.dtype}, "
-                             f"lengths {w.lengths[0]}" if reshaped(args) else None),
+                             f"lengths {w.lengths[0]}, c_ent={w.c_ent}" if reshaped(args) else None),
                    "valid_tokens_per_s": world * n_valid / (ms_step / 1e3),
                    "l2": (f"inputs ({w.R * w.V * w.elem_bytes / 1e9:.1f} GB logits) vs 129 MB "
                           "L2; no flush"),

@@ -100,3 +100,14 @@ def test_profiling_shape_options_reshape_the_workload():
     assert bench.reshaped(b)
     mask = synth.small_inputs(w)["mask"]
     assert mask.size == w.R and int(mask.sum()) == w.R  # every position valid
+
+
+def test_entropy_coefficient_option():
+    import argparse
+    base = dict(workload="ppo_gae", seqs=0, vocab=0, dtype=None, seq_len=0, all_valid=False,
+                c_ent=None)
+    assert bench.workload_for(argparse.Namespace(**base)).c_ent == synth.WORKLOADS["ppo_gae"].c_ent
+    a = argparse.Namespace(**dict(base, c_ent=0.0))
+    w = bench.workload_for(a)
+    assert w.c_ent == 0.0 and bench.reshaped(a)  # 0 is a setting, not "unset"
+    assert (w.B, w.T, w.V) == (synth.WORKLOADS["ppo_gae"].B, 512, 151936)

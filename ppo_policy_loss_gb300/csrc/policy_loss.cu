@@ -35,9 +35,10 @@
 //     them into the row's loss terms and pass-2 coefficients: a long chain
 //     of dependent scalar arithmetic, run once per row instead of once per
 //     consumer warp.  Two rows are in flight between the consumers and the
-//     row warp (two mbarrier pairs); in the short-row build the consumers
-//     run the first chunk of the next row's pass 1 before a row's pass 2,
-//     which covers the row warp's time for that row.
+//     row warp (two mbarrier pairs).  In the short-row build, and in the
+//     long-row build when no row is masked, the consumers run the first
+//     chunk of the next row's pass 1 before a row's pass 2, which covers
+//     part of the row warp's time for that row.
 //   * Masked rows need no logits, only an all-zero gradient row, written as
 //     bulk copies of a zeroed shared-memory block (the copy engine, not the
 //     consumers' store path): by a zero warp kept within eight rows of the
@@ -105,12 +106,18 @@ namespace {
 #endif
 // Chunks of the next row's first pass that the consumers run before the
 // second pass of a row: the time the row warp has for that row's arithmetic.
+// RL_LEAD_ALL_VALID applies when no row of the batch is masked (the lead
+// widens the reuse distance of the L2 lines kept for pass 2, which masked
+// rows' zero writes also compete for).
 #ifndef RL_LEAD_CHUNKS
 #ifdef RL_SHORT_ROWS
 #define RL_LEAD_CHUNKS 1
 #else
 #define RL_LEAD_CHUNKS 0
 #endif
+#endif
+#ifndef RL_LEAD_ALL_VALID
+#define RL_LEAD_ALL_VALID 1
 #endif
 
 // Masked rows' zero gradient: 1 a warp of its own, kept within kZeroLead
@@ -135,11 +142,12 @@ constexpr int kThreads = kConsumerThreads + (RL_ZERO_WARP ? 96 : 64);
 constexpr int kRedWarps = kConsumerWarps + 1;  // consumers and the row warp: token counts and sums
 constexpr int kRedThreads = kRedWarps * 32;
 constexpr int kLeadChunks = RL_LEAD_CHUNKS;
+constexpr int kLeadAllValid = RL_LEAD_ALL_VALID;
 constexpr int kVecsPerChunk = kChunkBytes / 16;
 constexpr int kVecsPerThread = kVecsPerChunk / kConsumerThreads;
 static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly over consumers");
 static_assert(kConsumerWarps <= 32, "the row warp takes one consumer partial per lane");
-static_assert(kLeadChunks >= 0, "chunks of look-ahead");
+static_assert(kLeadChunks >= 0 && kLeadAllValid >= 0, "chunks of look-ahead");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kRedBarrier = 1;  // named barrier id (0 is __syncthreads): consumers + row warp
 // Zero block the masked rows are copied from (16 KB: with it two CTAs of the
@@ -997,10 +1005,13 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
     for (int w = 0; w < kThreads / 32; ++w) cnt += sm.wcount[w];
   }
   const long long N_local = cnt;
-  // A streamed row's second pass runs in reverse chunk order when no row is
-  // masked (its last chunks, loaded most recently, are read again first);
-  // with masked rows, whose zero writes also pass through L2, in load order.
-  const bool rev = kTwoPass && N_local == a.R;
+  // When no row is masked, a streamed row's second pass runs in reverse chunk
+  // order (its last chunks, loaded most recently, are read again first) and
+  // the consumers lead with kLeadAllValid chunks; with masked rows, whose zero
+  // writes also pass through L2, in load order with kLeadChunks.
+  const bool all_valid = N_local == a.R;
+  const bool rev = kTwoPass && all_valid;
+  const int lead_chunks = all_valid ? kLeadAllValid : kLeadChunks;
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
@@ -1043,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
     auto valid_row = [&](long long row) {
       if constexpr (kTwoPass) {
         if (prev >= 0) {
-          const int lead = min(nchunks, kLeadChunks);
+          const int lead = min(nchunks, lead_chunks);
           issue(row, 0, lead, pol_last, false);
           issue(prev, 0, nchunks, pol_first, rev);
           issue(row, lead, nchunks, pol_last, false);
@@ -1338,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       while ((cur < a.R || prev >= 0) && !*abort_flag) {
         const bool has_cur = cur < a.R;
         if (RL_ZERO_WARP && tid == 0 && has_cur) *reinterpret_cast<volatile long long*>(&sm.pace) = cur;
-        const int lead = !has_cur ? 0 : prev >= 0 ? min(nchunks, kLeadChunks) : nchunks;
+        const int lead = !has_cur ? 0 : prev >= 0 ? min(nchunks, lead_chunks) : nchunks;
         const uint32_t base = it;  // resident rows: ring position of the current row's first chunk
         ThreadStats st;
         stats_init(st);

@@ -34,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -52,6 +53,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 LMHEAD_METRIC = "fused LM-head + log-softmax rows/s (Qwen3 head, V=151936 bf16); % of tensor roofline"
 LMHEAD_SHAPE = dict(R=32 * 1024, D=1024, V=151936, logit_sd=3.0, seed=202)
 KERNEL_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "policy_loss.cu")
+# the loss kernel's translation unit: its source and the headers of this
+# project that it includes
+KERNEL_SRCS = (KERNEL_SRC, os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "rl_device.cuh"),
+               os.path.join(ROOT, "include", "rlloss.h"))
 LMHEAD_SRC = os.path.join(ROOT, "ppo_policy_loss_gb300", "csrc", "lmhead.cu")
 # the workloads timed after the headline (their kernel times and roofline
 # fractions go into the line's "workloads" object)
@@ -108,9 +113,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and blank
+    lines (the kernel's files hold no comment markers inside string
+    literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_sha(src=None) -> str:
-    with open(src or KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the sha256 of the loss kernel's code (`src`: a
+    path or a sequence of paths, by default its translation unit), comments
+    and blank lines left out: a change to the code gives a new value, an edit
+    to comments alone keeps the records taken on the kernel valid."""
+    paths = KERNEL_SRCS if src is None else ((src,) if isinstance(src, str) else tuple(src))
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
+        h.update(b"\0")
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload=WORKLOAD, path=None, src=None):

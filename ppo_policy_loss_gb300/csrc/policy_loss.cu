@@ -35,10 +35,13 @@
 //     them into the row's loss terms and pass-2 coefficients: a long chain
 //     of dependent scalar arithmetic, run once per row instead of once per
 //     consumer warp.  Two rows are in flight between the consumers and the
-//     row warp (two mbarrier pairs).  In the short-row build, and in the
-//     long-row build when no row is masked, the consumers run the first
-//     chunk of the next row's pass 1 before a row's pass 2, which covers
-//     part of the row warp's time for that row.
+//     row warp.  When no row of the batch is masked the consumers run the
+//     first chunks of the next row's pass 1 before a row's pass 2 (long
+//     rows one chunk; short rows two, or the whole row if it has at most
+//     four), which covers the row warp's time for that row.  Long rows pass
+//     the coefficients through an mbarrier per row in flight; in the
+//     short-row build the row warp and the consumer warps meet at a named
+//     barrier once a row.
 //   * Masked rows need no logits, only an all-zero gradient row, written as
 //     bulk copies of a zeroed shared-memory block (the copy engine, not the
 //     consumers' store path): by a zero warp kept within eight rows of the
@@ -53,7 +56,10 @@
 //     CTA order.  Same inputs, same device -> bitwise identical results.
 //   * Every wait on an mbarrier is bounded (1 s); on timeout the kernel
 //     raises RL_DEVERR_TIMEOUT, stops, drains its own bulk copies and
-//     exits.  No trap, no unbounded spin.
+//     exits.  In the short-row build the consumers and the row warp still
+//     walk their remaining rows after a timeout, without waiting (every
+//     bounded wait then returns at once), so that each meets the others at
+//     the named barrier once for every row.  No trap, no unbounded spin.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -108,16 +114,37 @@ namespace {
 // second pass of a row: the time the row warp has for that row's arithmetic.
 // RL_LEAD_ALL_VALID applies when no row of the batch is masked (the lead
 // widens the reuse distance of the L2 lines kept for pass 2, which masked
-// rows' zero writes also compete for).
+// rows' zero writes also compete for); rows of at most RL_FULL_LEAD_CHUNKS
+// chunks then lead with the whole next row.
 #ifndef RL_LEAD_CHUNKS
-#ifdef RL_SHORT_ROWS
-#define RL_LEAD_CHUNKS 1
-#else
 #define RL_LEAD_CHUNKS 0
 #endif
-#endif
 #ifndef RL_LEAD_ALL_VALID
+#ifdef RL_SHORT_ROWS
+#define RL_LEAD_ALL_VALID 2
+#else
 #define RL_LEAD_ALL_VALID 1
+#endif
+#endif
+#ifndef RL_FULL_LEAD_CHUNKS
+#ifdef RL_SHORT_ROWS
+#define RL_FULL_LEAD_CHUNKS 4
+#else
+#define RL_FULL_LEAD_CHUNKS 0
+#endif
+#endif
+
+// How a row's coefficients reach the consumers.  1: the row warp and every
+// consumer warp meet at a named barrier once a row (short rows; it wakes the
+// consumers sooner and lets them lead with a whole row).  0: an mbarrier per
+// row in flight that only the row warp arrives on (long rows, where the
+// rendezvous would also hold each of the 16 consumer warps for the slowest).
+#ifndef RL_ROW_RENDEZVOUS
+#ifdef RL_SHORT_ROWS
+#define RL_ROW_RENDEZVOUS 1
+#else
+#define RL_ROW_RENDEZVOUS 0
+#endif
 #endif
 
 // Masked rows' zero gradient: 1 a warp of its own, kept within kZeroLead
@@ -143,13 +170,16 @@ constexpr int kRedWarps = kConsumerWarps + 1;  // consumers and the row warp: to
 constexpr int kRedThreads = kRedWarps * 32;
 constexpr int kLeadChunks = RL_LEAD_CHUNKS;
 constexpr int kLeadAllValid = RL_LEAD_ALL_VALID;
+constexpr int kFullLeadChunks = RL_FULL_LEAD_CHUNKS;
+constexpr bool kRendezvous = RL_ROW_RENDEZVOUS;
 constexpr int kVecsPerChunk = kChunkBytes / 16;
 constexpr int kVecsPerThread = kVecsPerChunk / kConsumerThreads;
 static_assert(kVecsPerChunk % kConsumerThreads == 0, "chunk must split evenly over consumers");
 static_assert(kConsumerWarps <= 32, "the row warp takes one consumer partial per lane");
-static_assert(kLeadChunks >= 0 && kLeadAllValid >= 0, "chunks of look-ahead");
+static_assert(kLeadChunks >= 0 && kLeadAllValid >= 0 && kFullLeadChunks >= 0, "chunks of look-ahead");
 constexpr int kMaxResidentChunks = (kSlots - 1) / 2;  // two rows + one chunk of look-ahead
 constexpr uint32_t kRedBarrier = 1;  // named barrier id (0 is __syncthreads): consumers + row warp
+constexpr uint32_t kCoefBarrier = 2;  // named barrier id of the row rendezvous: the same threads
 // Zero block the masked rows are copied from (16 KB: with it two CTAs of the
 // short-row build fill the SM's 228 KB of shared memory).
 constexpr int kZeroBytes = 16384;
@@ -1007,11 +1037,19 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
   const long long N_local = cnt;
   // When no row is masked, a streamed row's second pass runs in reverse chunk
   // order (its last chunks, loaded most recently, are read again first) and
-  // the consumers lead with kLeadAllValid chunks; with masked rows, whose zero
-  // writes also pass through L2, in load order with kLeadChunks.
+  // the consumers lead with kLeadAllValid chunks, or the whole row for rows
+  // of at most kFullLeadChunks chunks; with masked rows, whose zero writes
+  // also pass through L2, in load order with kLeadChunks.
   const bool all_valid = N_local == a.R;
   const bool rev = kTwoPass && all_valid;
-  const int lead_chunks = all_valid ? kLeadAllValid : kLeadChunks;
+  const int lead_chunks = !all_valid                                   ? kLeadChunks
+                          : kFullLeadChunks > 0 && nchunks <= kFullLeadChunks ? nchunks
+                                                                       : kLeadAllValid;
+  // Rows whose coefficients reach the consumers through the rendezvous.  Its
+  // participants never leave their row loops early: after a timeout every
+  // bounded wait returns at once, so each of them still meets the others
+  // once for every row of the CTA and the barrier cannot be left waiting.
+  constexpr bool kMeet = kRendezvous && (kMode == 0 || kMode == 2);
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
@@ -1170,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       float M, S, Tt, zyr;
       if constexpr (kMode < 2) {
         // the consumer warps' partials of this row
-        if (!wait_bounded<false>(smem_addr(&sm.xbar[b]), (k >> 1) & 1, abort_flag)) break;
+        if (!wait_bounded<false>(smem_addr(&sm.xbar[b]), (k >> 1) & 1, abort_flag) && !kMeet) break;
         const float4 P = lane < kConsumerWarps ? sm.xpart[b][lane] : make_float4(kFloor, 0.f, 0.f, 0.f);
         M = P.x;
         S = P.y;
@@ -1181,7 +1219,9 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         if (lane == 0) sm.zy[b] = -INFINITY;  // for the row after next (written after cbar[b] below)
       } else {
         // consumers took row k - 2's coefficients before coef[b] is rewritten
-        if (k >= 2 && !wait_bounded<false>(smem_addr(&sm.xbar[b]), ((k - 2) >> 1) & 1, abort_flag)) break;
+        // (the rendezvous of row k - 1 already orders that)
+        if (!kMeet && k >= 2 && !wait_bounded<false>(smem_addr(&sm.xbar[b]), ((k - 2) >> 1) & 1, abort_flag))
+          break;
         merge_shards(a, row, lane, M, S, Tt, zyr);
       }
       if constexpr (kMode == 1) {  // this shard's statistics of the row, for the exchange
@@ -1191,7 +1231,12 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         }
       } else {
         const RowVals v = row_values<DT>(a, rs, cache, Bp, sc, M, S, Tt, zyr, lane);
-        if (lane == 0) {  // the consumers' coefficients first, the bookkeeping after
+        // the consumers' coefficients first, the bookkeeping after
+        if constexpr (kMeet) {
+          if (lane == 0) sm.coef[b] = v.cf;
+          __syncwarp();
+          named_barrier(kCoefBarrier, kRedThreads);
+        } else if (lane == 0) {
           sm.coef[b] = v.cf;
           mbar_arrive(smem_addr(&sm.cbar[b]));
         }
@@ -1240,7 +1285,8 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       merge_stats(m, s, t, m0, s0, t0);
       warp_stats(m, s, t, false);
       const uint32_t b = k & 1;
-      if (k >= 2) wait_bounded<false>(smem_addr(&sm.cbar[b]), ((k - 2) >> 1) & 1, abort_flag);
+      // (with the rendezvous, this warp's meeting for row k - 1 already orders that)
+      if (!kMeet && k >= 2) wait_bounded<false>(smem_addr(&sm.cbar[b]), ((k - 2) >> 1) & 1, abort_flag);
       if (p.cy >= 0) sm.zy[b] = zy;
       __syncwarp();
       if (lane == 0) {
@@ -1251,9 +1297,12 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
     // pass 2 of row `row` (the k-th of this CTA; resident rows start at ring position `base`)
     auto pass2 = [&](long long row, uint32_t k, uint32_t base, const IdPos& p) {
       const uint32_t b = k & 1;
-      wait_bounded<false>(smem_addr(&sm.cbar[b]), (k >> 1) & 1, abort_flag);
+      if constexpr (kMeet)
+        named_barrier(kCoefBarrier, kRedThreads);
+      else
+        wait_bounded<false>(smem_addr(&sm.cbar[b]), (k >> 1) & 1, abort_flag);
       const RowCoef cf = sm.coef[b];
-      if (kMode == 2) {  // coef[b] taken: the row warp may rewrite it for row k + 2
+      if (!kMeet && kMode == 2) {  // coef[b] taken: the row warp may rewrite it for row k + 2
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.xbar[b]));
       }
@@ -1346,7 +1395,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
       long long prev = -1;
       IdPos pp = pc;
       uint32_t kp = 0, base_p = 0;
-      while ((cur < a.R || prev >= 0) && !*abort_flag) {
+      while ((cur < a.R || prev >= 0) && (kMeet || !*abort_flag)) {
         const bool has_cur = cur < a.R;
         if (RL_ZERO_WARP && tid == 0 && has_cur) *reinterpret_cast<volatile long long*>(&sm.pace) = cur;
         const int lead = !has_cur ? 0 : prev >= 0 ? min(nchunks, lead_chunks) : nchunks;
@@ -1378,7 +1427,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         }
       }
     } else {
-      for (; cur < a.R && !*abort_flag; ++k) {
+      for (; cur < a.R && (kMeet || !*abort_flag); ++k) {
         if (RL_ZERO_WARP && tid == 0) *reinterpret_cast<volatile long long*>(&sm.pace) = cur;
         if constexpr (kMode == 1) {
           ThreadStats st;

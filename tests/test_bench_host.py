@@ -82,6 +82,21 @@ def test_traffic_record_ignored_when_kernel_changed(tmp_path):
     assert bench.recorded_traffic(path=str(f)) == 123.0
 
 
+def test_kernel_sha_follows_code_not_comments(tmp_path):
+    src = tmp_path / "k.cu"
+    body = "__global__ void k(int* p) {\n  p[0] = 1;  // one\n}\n"
+    src.write_text(body)
+    sha = bench.kernel_sha(str(src))
+    # comments, trailing blanks and blank lines do not count
+    src.write_text("/* a kernel\n   of one store */\n" + body.replace("// one", "// the first element") + "\n\n")
+    assert bench.kernel_sha(str(src)) == sha
+    # code does
+    src.write_text(body.replace("p[0] = 1", "p[0] = 2"))
+    assert bench.kernel_sha(str(src)) != sha
+    # the default covers the kernel source and the project headers it includes
+    assert len(bench.KERNEL_SRCS) == 3 and bench.kernel_sha() == bench.kernel_sha(bench.KERNEL_SRCS)
+
+
 def test_alg_bytes_ppo_counts_per_token_advantages_and_no_reference():
     w = synth.WORKLOADS["ppo_gae"]
     assert bench.alg_bytes(w, w.R) == 2 * w.R * w.V * 2 + w.R * 21 + w.R * 4

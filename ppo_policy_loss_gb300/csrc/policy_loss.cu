@@ -27,7 +27,11 @@
 //         row is masked the second pass runs in reverse chunk order.
 //   * Consumer warps: pass 1 keeps a per-thread online (max, sum 2^x,
 //     sum 2^x * x) in packed fp32x2 with independent accumulator chains;
-//     each warp then reduces its lanes and publishes one partial.  Pass 2
+//     each warp then reduces its lanes and publishes one partial.  In the
+//     short-row build a row's last, partly filled chunk is padded in shared
+//     memory with the format's floor and taken by the same routine as a full
+//     chunk (the row warp removes the padding's share in the rows where it
+//     can have one); long rows keep a predicated routine for it.  Pass 2
 //     writes the gradient with 16-byte streaming stores.  The entropy term
 //     is a template argument, so each launch runs only the pass-2 code it
 //     needs.
@@ -150,6 +154,17 @@ namespace {
 // Masked rows' zero gradient: 1 a warp of its own, kept within kZeroLead
 // rows of the consumers; 0 the producer writes them as it walks the rows
 // (one warp fewer: the short-row build keeps 96 registers per thread).
+// A row's last, partly filled chunk.  1: padded in shared memory to a full
+// one and taken by the full-chunk routine (short rows, where that routine
+// alone in the consumers' loop is 5% faster at V = 32000 fp16).  0: its own
+// predicated routine (long rows, where the padding measured 0.2% slower).
+#ifndef RL_PAD_TAIL
+#ifdef RL_SHORT_ROWS
+#define RL_PAD_TAIL 1
+#else
+#define RL_PAD_TAIL 0
+#endif
+#endif
 #ifndef RL_ZERO_WARP
 #ifdef RL_SHORT_ROWS
 #define RL_ZERO_WARP 0
@@ -245,7 +260,15 @@ struct LossArgs {
 // element at a large negative finite value (keeping NaN), so that a -inf
 // logit contributes exp = 0 and 0 * x = 0 instead of 0 * inf = NaN; vmax() is
 // the NaN-propagating maximum of a full vector; unpack() widens to fp32.
-constexpr float kFloor = -1.0e30f;
+// The fp32 and bf16 floor is -2^100: its product with log2 e is exact, so in
+// a lane whose running maximum is still the floor a floor element gets
+// exponent exactly 0 rather than the rounding error of a 1e30-sized product.
+constexpr float kFloor = -0x1p100f;
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 template <int DT>
 struct Elem;
@@ -253,7 +276,8 @@ struct Elem;
 template <>
 struct Elem<RL_F32> {
   static constexpr int kBytes = 4, kVec = 4;
-  static constexpr uint32_t kFloorWord = 0xF149F2CAu;  // kFloor
+  static constexpr uint32_t kFloorWord = 0xF1800000u;  // kFloor
+  __device__ static float floor_value() { return kFloor; }
   __device__ static void clamp(uint4& w) {
     w.x = __float_as_uint(max_nan(__uint_as_float(w.x), kFloor));
     w.y = __float_as_uint(max_nan(__uint_as_float(w.y), kFloor));
@@ -292,8 +316,9 @@ __device__ __forceinline__ uint32_t max_nan_f16x2(uint32_t a, uint32_t b) {
 template <>
 struct Elem<RL_BF16> {
   static constexpr int kBytes = 2, kVec = 8;
-  static constexpr uint32_t kFloor2 = 0xF149F149u;  // (-9.98e29, -9.98e29) in bf16
+  static constexpr uint32_t kFloor2 = 0xF180F180u;  // (-2^100, -2^100) in bf16
   static constexpr uint32_t kFloorWord = kFloor2;
+  __device__ static float floor_value() { return kFloor; }
   __device__ static void clamp(uint4& w) {
     w.x = max_nan_bf16x2(w.x, kFloor2);
     w.y = max_nan_bf16x2(w.y, kFloor2);
@@ -331,6 +356,7 @@ struct Elem<RL_F16> {
   static constexpr int kBytes = 2, kVec = 8;
   static constexpr uint32_t kFloor2 = 0xFBFFFBFFu;  // (-65504, -65504) in fp16
   static constexpr uint32_t kFloorWord = kFloor2;
+  __device__ static float floor_value() { return -65504.f; }
   __device__ static void clamp(uint4& w) {
     w.x = max_nan_f16x2(w.x, kFloor2);
     w.y = max_nan_f16x2(w.y, kFloor2);
@@ -504,6 +530,45 @@ __device__ __forceinline__ void accumulate_chunk_tail(uint32_t buf, int first, i
     }
     a.s[q] = s;
     a.t[q] = t;
+  }
+}
+
+// A row's last, partly filled chunk made a full one: this thread's vectors
+// past the row's end in the ring slot set to the format's floor (elements
+// too, where the end cuts a vector), so that the full-chunk routine can take
+// it.  They never raise the running maximum, and their exponentials are
+// exactly 0 unless the row's maximum lies within ~88 of the floor
+// (remove_padding takes their share out then).  Looped, not unrolled: the
+// per-row call adds little code to the consumers' loop.
+template <class E>
+__device__ __forceinline__ void pad_chunk_tail(uint32_t buf, int first, int nelem) {
+  const int rem = nelem - first;  // elements from this thread's vector 0 to the row's end
+#pragma unroll 1
+  for (int q = 0; q < kVecsPerThread; ++q) {
+    const int nv = rem - q * kConsumerThreads * E::kVec;
+    if (nv < E::kVec) {
+      const uint32_t at = buf + q * kConsumerThreads * 16;  // inside the ring slot
+      uint4 w = nv > 0 ? ld_shared_v4(at) : make_uint4(0u, 0u, 0u, 0u);
+      fill_floor<E>(w, max(nv, 0));
+      st_shared_v4(at, w);
+    }
+  }
+  // bulk copies (the async proxy) write the slot again once it is released
+  fence_proxy_async_shared();
+}
+
+// A row's (M, S, T) with the share of its n_pad padding elements taken out.
+// Each entered the first pass as the floor F and added 2^x to S and 2^x x to
+// T, with x = F log2 e - M log2 e in the row's frame (the consumers' own
+// rounding): 0 unless x is above -126, i.e. unless every logit of the row is
+// within ~88 of F (-inf or floor-valued logits).  Only such rows change.
+template <class E>
+__device__ __forceinline__ void remove_padding(float M, float& S, float& T, int n_pad) {
+  const float x = fmaf(E::floor_value(), kLog2e, -M * kLog2e);
+  if (n_pad > 0 && x > -127.f) {
+    const float e = ex2_approx(x);
+    S -= static_cast<float>(n_pad) * e;
+    T -= static_cast<float>(n_pad) * e * x;
   }
 }
 
@@ -1214,6 +1279,7 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         S = P.y;
         Tt = P.z;
         warp_stats(M, S, Tt, true);
+        if (RL_PAD_TAIL) remove_padding<E>(M, S, Tt, nchunks * kChunkElems - nelem);
         zyr = sm.zy[b];
         __syncwarp();
         if (lane == 0) sm.zy[b] = -INFINITY;  // for the row after next (written after cbar[b] below)
@@ -1255,10 +1321,14 @@ __global__ void __launch_bounds__(kThreads, RL_MIN_CTAS_PER_SM) RL_LOSS_KERNEL(c
         wait_bounded<false>(smem_addr(&sm.full[slot]), (k / kSlots) & 1, abort_flag);
         const uint32_t buf = smem_addr(sm.ring[slot]) + tid * 16;
         const int e0 = c * kChunkElems;
-        if (e0 + kChunkElems <= nelem)
+        if (RL_PAD_TAIL) {
+          if (e0 + kChunkElems > nelem) pad_chunk_tail<E>(buf, e0 + tid * kVec, nelem);
           accumulate_chunk<E>(buf, st);
-        else
+        } else if (e0 + kChunkElems <= nelem) {
+          accumulate_chunk<E>(buf, st);
+        } else {
           accumulate_chunk_tail<E>(buf, e0 + tid * kVec, nelem, st);
+        }
         if (c == p.cy) zy = element_of<E>(ld_shared_v4(smem_addr(sm.ring[slot]) + p.jv / kVec * 16), p.jv % kVec);
         if (kStream || kMode == 1) {  // read again from L2 in pass 2 (or no pass 2): free it now
           __syncwarp();

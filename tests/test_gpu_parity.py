@@ -714,6 +714,51 @@ def test_loss_waits_for_the_kernel_before_it():
     assert_stats_match(torch_api.read_stats(out["stats"]), ref, int(band.sum()))
 
 
+@pytest.mark.parametrize("V", [9, 32000, 151936])
+def test_rows_at_the_fp16_floor(V):
+    """Rows whose every logit is -65504, the lowest finite fp16 value: a
+    uniform distribution, logp = -ln V and entropy ln V.  In the vector that a
+    row's end cuts, the first pass sets the elements past the end to the
+    format's floor (-65504 in fp16), and only in rows whose maximum is that
+    floor do they reach the softmax sums; the kernel takes their share out
+    again.  At V = 9 (a 16-element row stride) those are 7 elements, and
+    without the correction the row would read as uniform over 16 (logp off by
+    0.58).  V = 32000 (short-row build) and 151936 (long-row build) end on a
+    vector boundary and have partly filled last chunks.  At |z| = 65504 fp32
+    resolves about 2^-8 in any implementation, so these rows are checked to
+    1e-2; every other row to the usual tolerance."""
+    w = W["long_seq_grpo"].scaled(dtype="f16", V=V, n_prompts=1, group=4, T=4,
+                                  lengths=("full",), c_ent=0.02, beta=0.05, seed=91)
+    ld = -(-V // 8) * 8
+    small, logits = build_case(w, ld=ld)
+    R = w.R
+    ids = small["ids"].copy()
+    floor_rows = [1, 6]
+    for r in floor_rows:
+        logits[r, :V] = -65504.0
+    host = storage_np(logits)[:, :V]
+    mask = small["mask"]
+    assert mask.all()
+    arow, adv = adv_rows(w, small)
+    lse, logp, ent = oracle.row_stats(host, "f16", V, ids, mask)
+    lo, rf = composed_old_ref(logp, small, mask, R)
+    out = torch_api.policy_loss(logits, to_dev(ids), to_dev(mask), to_dev(adv.astype(np.float32)),
+                                w.B, w.T, V=V, logp_old=to_dev(lo), ref_logp=to_dev(rf), eps=w.eps,
+                                beta=w.beta, c_ent=w.c_ent, grad_scale=1.0)
+    torch.cuda.synchronize()
+    lp_gpu = out["logp"].cpu().numpy()
+    h_gpu = out["entropy"].cpu().numpy()
+    for r in floor_rows:
+        assert abs(logp[r] + np.log(V)) < 1e-9 and abs(ent[r] - np.log(V)) < 1e-9  # the oracle
+        assert abs(lp_gpu[r] + np.log(V)) < 1e-2, (r, lp_gpu[r], -np.log(V))
+        assert abs(h_gpu[r] - np.log(V)) < 1e-2, (r, h_gpu[r], np.log(V))
+    keep = np.ones(R, dtype=bool)
+    keep[floor_rows] = False
+    assert np.abs(lp_gpu[keep] - logp[keep]).max() <= LOGP_ATOL
+    assert np.abs(h_gpu[keep] - ent[keep]).max() <= LOGP_ATOL
+    assert not torch.isnan(out["dlogits"][:, :V].float()).any()
+
+
 @pytest.mark.parametrize("dtype,V", [("bf16", 151936), ("f16", 32000), ("f32", 5000)])
 def test_minus_infinity_and_extreme_logits(dtype, V):
     """Padded-vocabulary rows: the last 267 entries of every row are -inf (as

@@ -151,9 +151,6 @@ namespace {
 #endif
 #endif
 
-// Masked rows' zero gradient: 1 a warp of its own, kept within kZeroLead
-// rows of the consumers; 0 the producer writes them as it walks the rows
-// (one warp fewer: the short-row build keeps 96 registers per thread).
 // A row's last, partly filled chunk.  1: padded in shared memory to a full
 // one and taken by the full-chunk routine (short rows, where that routine
 // alone in the consumers' loop is 5% faster at V = 32000 fp16).  0: its own
@@ -165,6 +162,10 @@ namespace {
 #define RL_PAD_TAIL 0
 #endif
 #endif
+
+// Masked rows' zero gradient: 1 a warp of its own, kept within kZeroLead
+// rows of the consumers; 0 the producer writes them as it walks the rows
+// (one warp fewer: the short-row build keeps 96 registers per thread).
 #ifndef RL_ZERO_WARP
 #ifdef RL_SHORT_ROWS
 #define RL_ZERO_WARP 0

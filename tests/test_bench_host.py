@@ -97,6 +97,23 @@ def test_kernel_sha_follows_code_not_comments(tmp_path):
     assert len(bench.KERNEL_SRCS) == 3 and bench.kernel_sha() == bench.kernel_sha(bench.KERNEL_SRCS)
 
 
+def test_committed_loss_profiles_name_the_current_kernel():
+    """Every traffic record and ncu summary of the loss kernel under profiles/
+    was taken on the kernel's current code (the records feed the bench line's
+    roofline traffic; a kernel change without new captures fails here)."""
+    prof = os.path.join(ROOT, "profiles")
+    sha = bench.kernel_sha()
+    records = sorted(f for f in os.listdir(prof) if f.startswith("policy_loss_") and f.endswith("_traffic.txt"))
+    summaries = sorted(f for f in os.listdir(prof) if f.startswith("policy_loss_") and f.endswith(".md"))
+    assert records and summaries
+    for f in records:
+        name = f[len("policy_loss_"):-len("_traffic.txt")]
+        assert bench.recorded_traffic(name) is not None, f
+    for f in summaries:
+        with open(os.path.join(prof, f)) as fh:
+            assert f"kernel_sha {sha}" in fh.read(), f
+
+
 def test_alg_bytes_ppo_counts_per_token_advantages_and_no_reference():
     w = synth.WORKLOADS["ppo_gae"]
     assert bench.alg_bytes(w, w.R) == 2 * w.R * w.V * 2 + w.R * 21 + w.R * 4
